@@ -1,0 +1,196 @@
+/*
+ * capattn — soft-capped unified attention (forward and backward) on GB300.
+ *
+ * C ABI of the library libcapattn.so.  Plain pointers and sizes only.
+ *
+ * What the calls compute (pages "triton_kernels.py" and "mosaic_backward.py",
+ * xrex_unified unified attention; notation per batch b and query head h, with
+ * KV head g = h / q_heads_per_kv_head as in mosaic_backward.py
+ * make_mosaic_backward_dq_kernel):
+ *
+ *   s_ij = sm_scale * <Q_i, K_j>                  (triton_kernels.py forward kernel)
+ *   c_ij = cap(s_ij)                              (mosaic_backward.py _apply_cap_mosaic)
+ *            none / cap <= 0 : s
+ *            tanh            : cap * tanh(s / cap)
+ *            soft_sign       : s / (1 + |s| / cap)
+ *            alsc            : cap * (sig(a(s/cap + b)) - sig(ab)) / (sig(ab)(1 - sig(ab)) + 1e-12)
+ *   t_ij = temp_i * c_ij                          (triton_kernels.py dQ kernel, temperature)
+ *   live_ij = [seg_i == seg_j] and (!causal or i >= j) and
+ *             (window_len == 0 or j > i - window_len) and ranker_ij
+ *                                                 (triton_kernels.py forward kernel masks;
+ *                                                  mosaic_backward.py ranker_mask_mosaic_kv_q)
+ *   ranker_ij = (j in [hl,hu) and (i in [hl,hu) or i in [cl,cu)))
+ *               or (i in [cl,cu) and i == j)
+ *   LSE_i = log sum_{live j} exp(t_ij)   (natural log; -inf for a fully masked row)
+ *   P_ij  = live_ij ? exp(t_ij - LSE_i) : 0,   O_i = sum_j P_ij V_j
+ *
+ * Backward (mosaic_backward.py backward kernels and delta pre-pass):
+ *   delta_i = sum_d O_id dO_id
+ *   dT_ij   = P_ij (dO_i . V_j - delta_i) + z_loss_weight * P_ij * LSE_i
+ *   dX_ij   = sm_scale * cap'(s_ij) * temp_i * dT_ij   (cap' is the exact derivative of cap)
+ *   dQ_i = sum_j dX_ij K_j;  dK_j = sum_{h in g} sum_i dX_ij Q_i;  dV_j = sum_{h in g} sum_i P_ij dO_i
+ * which is the gradient of sum(O * dO) + (z_loss_weight / 2) * sum over live rows of LSE^2.
+ *
+ * Layouts (all contiguous, row-major):
+ *   q, o, dO, dq : [B, L, Hq, D]      k, v, dk, dv : [B, L, Hkv, D]
+ *   lse, m, l, delta : [B, Hq, L] float32
+ *   temp : [B, L] float32 (NULL means 1)
+ *   seg  : [B, L] int32 segment ids, non-decreasing along each batch row
+ *          (packed documents); NULL means one segment.
+ *   bounds : [B, 4] int32 (hl, hu, cl, cu) per batch row with
+ *            0 <= hl <= hu <= L and 0 <= cl <= cu <= L; NULL disables the ranker mask.
+ *   Element type of q/k/v/o/dO/dq/dk/dv: bf16 (CAPATTN_BF16) or float32 (CAPATTN_FP32).
+ *   Every tensor pointer must be 16-byte aligned.
+ *
+ * Ownership: the caller owns every buffer, including the workspace; the
+ * library allocates no device memory on these calls.  All calls enqueue work on
+ * `stream` and return without synchronising.  Argument errors are detected on
+ * the host before anything is launched and returned synchronously.  Errors in
+ * device-resident data (segment ids that decrease, ranker bounds out of range)
+ * and bounded-wait timeouts inside kernels are recorded in a status word in the
+ * workspace; read it with capattn_device_status.
+ */
+#ifndef CAPATTN_H_
+#define CAPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum capattn_status {
+  CAPATTN_OK = 0,
+  CAPATTN_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment or parameter */
+  CAPATTN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. bf16 with D != 128) */
+  CAPATTN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  CAPATTN_ERR_DEVICE_TIMEOUT = 4,/* a kernel gave up on a bounded wait (device status) */
+  CAPATTN_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than capattn_workspace_bytes */
+  CAPATTN_ERR_DEVICE_DATA = 6    /* device status: bad segment ids or ranker bounds */
+} capattn_status;
+
+/* Cap methods (mosaic_backward.py _apply_cap_mosaic).  A cap <= 0 behaves as none. */
+enum { CAPATTN_CAP_NONE = 0, CAPATTN_CAP_TANH = 1, CAPATTN_CAP_SOFT_SIGN = 2, CAPATTN_CAP_ALSC = 3 };
+
+/* Element types of the attention tensors. */
+enum { CAPATTN_BF16 = 0, CAPATTN_FP32 = 1 };
+
+/* Which pass a workspace size or visit map refers to. */
+enum { CAPATTN_PASS_FWD = 0, CAPATTN_PASS_BWD = 1 };
+enum { CAPATTN_VISIT_Q_TILES = 0, CAPATTN_VISIT_KV_TILES = 1 };
+
+/*
+ * Configuration (the pages' KernelConfig: cap method and parameters, sm_scale,
+ * causal, window_len, z_loss_weight, and the GQA factor of
+ * mosaic_attention_backward).  struct_size must be sizeof(capattn_config).
+ */
+typedef struct capattn_config {
+  uint32_t struct_size;
+  int32_t cap_method;          /* CAPATTN_CAP_* */
+  float cap, alpha, beta;      /* cap > 0 activates the method; alpha, beta for ALSC */
+  float sm_scale;              /* multiplies Q.K before the cap */
+  int32_t causal;              /* nonzero: key j visible only if j <= i */
+  int32_t window_len;          /* > 0: key j visible only if j > i - window_len; 0: off */
+  float z_loss_weight;         /* >= 0; adds z * P * LSE to dT */
+  int32_t q_heads_per_kv_head; /* G = Hq / Hkv */
+  int32_t B, L, Hq, Hkv, D;    /* batch, sequence length, heads, head dim */
+  int32_t dtype;               /* CAPATTN_BF16 or CAPATTN_FP32 */
+} capattn_config;
+
+/* Human-readable name of a status code (static string). */
+const char* capattn_status_string(capattn_status s);
+
+/* Checks a configuration without touching any pointer (same rules as the compute calls). */
+capattn_status capattn_validate_config(const capattn_config* cfg);
+
+/*
+ * Bytes of device workspace needed by capattn_fwd (pass CAPATTN_PASS_FWD) or
+ * capattn_bwd (CAPATTN_PASS_BWD) for this configuration; 0 if cfg is invalid.
+ * The workspace must be 256-byte aligned.  Its first word is the device status.
+ */
+size_t capattn_workspace_bytes(const capattn_config* cfg, int pass);
+
+/*
+ * Tile sizes the kernels use for this configuration (the granularity of the
+ * visit maps): bf16 uses 128 x 128 tiles, fp32 64 x 64.
+ */
+capattn_status capattn_tile_sizes(const capattn_config* cfg, int32_t* block_q, int32_t* block_kv);
+
+/*
+ * Forward (triton_kernels.py make_triton_forward_kernel, with its residuals).
+ * Inputs q, k, v, temp (nullable), seg (nullable), bounds (nullable): device.
+ * Outputs (device): o [B,L,Hq,D] in the input element type; lse [B,Hq,L]
+ * natural-log log-sum-exp; m and l [B,Hq,L] (nullable): row max of t and
+ * sum of exp(t - m), so that lse = m + log(l).  A fully masked row gives
+ * o = 0, lse = m = -inf, l = 0.
+ * workspace: device, >= capattn_workspace_bytes(cfg, CAPATTN_PASS_FWD).
+ */
+capattn_status capattn_fwd(const capattn_config* cfg, const void* q, const void* k, const void* v,
+                           const float* temp, const int32_t* seg, const int32_t* bounds, void* o,
+                           float* lse, float* m, float* l, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
+ * Backward (mosaic_backward.py make_preprocess_backward_kernel,
+ * make_mosaic_backward_dkv_kernel, make_mosaic_backward_dq_kernel and the
+ * mosaic_attention_backward orchestration, with the group sum over query heads
+ * done inside the dK/dV kernel).
+ * Inputs (device): q, k, v, temp, seg, bounds as in capattn_fwd; o and lse as
+ * written by capattn_fwd; dO [B,L,Hq,D] upstream gradient.
+ * Outputs (device): dq [B,L,Hq,D], dk and dv [B,L,Hkv,D] (input element type,
+ * fully overwritten); delta [B,Hq,L] float32 = rowsum(o * dO).
+ * workspace: device, >= capattn_workspace_bytes(cfg, CAPATTN_PASS_BWD).
+ */
+capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void* k, const void* v,
+                           const float* temp, const int32_t* seg, const int32_t* bounds,
+                           const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                           void* dv, float* delta, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device status word at the start
+ * of `workspace`.  Returns CAPATTN_OK, CAPATTN_ERR_DEVICE_TIMEOUT or
+ * CAPATTN_ERR_DEVICE_DATA; *raw_bits (nullable) receives the raw bits
+ * (1 = wait timeout, 2 = decreasing segment ids, 4 = ranker bounds out of range).
+ */
+capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint32_t* raw_bits);
+
+/*
+ * Visit maps (host computation).  For which = CAPATTN_VISIT_Q_TILES, out holds
+ * for every (b, query tile) a bitmap over KV tiles: bit t of word
+ * out[(b * n_q_tiles + qt) * words_kv + t / 32] is set iff the tile pair
+ * holds at least one live (i, j); words_kv = ceil(n_kv_tiles / 32).  For
+ * CAPATTN_VISIT_KV_TILES, the transpose: per (b, KV tile) a bitmap over query
+ * tiles.  Tile sizes as capattn_tile_sizes.  seg and bounds: host, nullable.
+ * out_words must be at least the map size; *n_words receives it.
+ */
+capattn_status capattn_visit_map_host(const capattn_config* cfg, const int32_t* seg,
+                                      const int32_t* bounds, int which, uint32_t* out,
+                                      size_t out_words, size_t* n_words);
+
+/*
+ * The same maps built by the device pre-pass that capattn_fwd / capattn_bwd
+ * run, copied to the device buffer out (same format).  seg, bounds: device.
+ * Uses `workspace` (>= capattn_workspace_bytes(cfg, CAPATTN_PASS_BWD)).
+ */
+capattn_status capattn_visit_map_device(const capattn_config* cfg, const int32_t* seg,
+                                        const int32_t* bounds, int which, uint32_t* out,
+                                        size_t out_words, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Live-pair bit matrix of batch row b (host computation with the same per-row
+ * rule the kernels use): bit j of word bits[i * ceil(L/64) + j / 64] is set iff
+ * pair (i, j) is live.  seg and bounds: host, nullable (full [B, L] / [B, 4]).
+ */
+capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* seg,
+                                      const int32_t* bounds, int32_t b, uint64_t* bits,
+                                      size_t n_words);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAPATTN_H_ */

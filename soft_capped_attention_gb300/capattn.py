@@ -1,0 +1,281 @@
+"""Python binding of libcapattn.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; PyTorch only
+provides device memory and the current stream.  The names mirror the C ABI in
+include/capattn.h: ``capattn_fwd`` / ``capattn_bwd`` (device tensors),
+``capattn_workspace_bytes``, ``capattn_device_status`` and the visit-map /
+mask-bit debug exports.  ``CapAttnFunction`` wraps the pair as a
+``torch.autograd.Function``.
+
+There is no fallback: if the shared library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcapattn.so")
+
+CAP_METHODS = {"none": 0, "tanh": 1, "soft_sign": 2, "alsc": 3}
+DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+PASS_FWD, PASS_BWD = 0, 1
+VISIT_Q_TILES, VISIT_KV_TILES = 0, 1
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+                4: "device wait timeout", 5: "workspace missing, misaligned or too small",
+                6: "invalid device data (segment ids or ranker bounds)"}
+
+
+class CapattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} (status {status})")
+
+
+class CapattnConfig(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_uint32), ("cap_method", ctypes.c_int32),
+                ("cap", ctypes.c_float), ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("sm_scale", ctypes.c_float), ("causal", ctypes.c_int32),
+                ("window_len", ctypes.c_int32), ("z_loss_weight", ctypes.c_float),
+                ("q_heads_per_kv_head", ctypes.c_int32), ("B", ctypes.c_int32),
+                ("L", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_lib_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m soft_capped_attention_gb300.build`")
+        h = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+        cfgp = ctypes.POINTER(CapattnConfig)
+        h.capattn_status_string.restype = ctypes.c_char_p
+        h.capattn_status_string.argtypes = [ctypes.c_int]
+        h.capattn_validate_config.restype = ctypes.c_int
+        h.capattn_validate_config.argtypes = [cfgp]
+        h.capattn_workspace_bytes.restype = sz
+        h.capattn_workspace_bytes.argtypes = [cfgp, ctypes.c_int]
+        h.capattn_tile_sizes.restype = ctypes.c_int
+        h.capattn_tile_sizes.argtypes = [cfgp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        h.capattn_fwd.restype = ctypes.c_int
+        h.capattn_fwd.argtypes = [cfgp] + [vp] * 10 + [vp, sz, vp]
+        h.capattn_bwd.restype = ctypes.c_int
+        h.capattn_bwd.argtypes = [cfgp] + [vp] * 13 + [vp, sz, vp]
+        h.capattn_device_status.restype = ctypes.c_int
+        h.capattn_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        h.capattn_visit_map_host.restype = ctypes.c_int
+        h.capattn_visit_map_host.argtypes = [cfgp, vp, vp, ctypes.c_int, vp, sz,
+                                             ctypes.POINTER(sz)]
+        h.capattn_visit_map_device.restype = ctypes.c_int
+        h.capattn_visit_map_device.argtypes = [cfgp, vp, vp, ctypes.c_int, vp, sz, vp, sz, vp]
+        h.capattn_mask_bits_host.restype = ctypes.c_int
+        h.capattn_mask_bits_host.argtypes = [cfgp, vp, vp, i32, vp, sz]
+        _lib_handle = h
+    return _lib_handle
+
+
+EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn_workspace_bytes",
+                    "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_device_status",
+                    "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host")
+
+
+@dataclass(frozen=True)
+class AttnParams:
+    """The method's parameters (the pages' KernelConfig fields)."""
+    sm_scale: float
+    cap_method: str = "none"
+    cap: float = 0.0
+    alpha: float = 0.0
+    beta: float = 0.0
+    causal: bool = False
+    window_len: int = 0
+    z_loss_weight: float = 0.0
+
+
+def params_from_workload(w) -> AttnParams:
+    return AttnParams(sm_scale=float(w.sm_scale), cap_method=w.cap_method, cap=float(w.cap),
+                      alpha=float(w.alpha), beta=float(w.beta), causal=bool(w.causal),
+                      window_len=int(w.window_len), z_loss_weight=float(w.z_loss_weight))
+
+
+def make_config(ap: AttnParams, B: int, L: int, Hq: int, Hkv: int, D: int,
+                dtype: torch.dtype) -> CapattnConfig:
+    if dtype not in DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    if ap.cap_method not in CAP_METHODS:
+        raise ValueError(f"unknown cap method {ap.cap_method!r}")
+    c = CapattnConfig()
+    c.struct_size = ctypes.sizeof(CapattnConfig)
+    c.cap_method = CAP_METHODS[ap.cap_method]
+    c.cap, c.alpha, c.beta = ap.cap, ap.alpha, ap.beta
+    c.sm_scale = ap.sm_scale
+    c.causal = 1 if ap.causal else 0
+    c.window_len = ap.window_len
+    c.z_loss_weight = ap.z_loss_weight
+    c.q_heads_per_kv_head = Hq // Hkv if Hkv > 0 else 0
+    c.B, c.L, c.Hq, c.Hkv, c.D = B, L, Hq, Hkv, D
+    c.dtype = DTYPES[dtype]
+    return c
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise CapattnError(status, where)
+
+
+def workspace_bytes(cfg: CapattnConfig, pass_: int) -> int:
+    return int(lib().capattn_workspace_bytes(ctypes.byref(cfg), pass_))
+
+
+def new_workspace(cfg: CapattnConfig, device) -> torch.Tensor:
+    n = max(workspace_bytes(cfg, PASS_FWD), workspace_bytes(cfg, PASS_BWD))
+    if n == 0:
+        _check(lib().capattn_validate_config(ctypes.byref(cfg)), "capattn_workspace_bytes")
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _shape(q, k):
+    B, L, Hq, D = q.shape
+    Hkv = k.shape[2]
+    return B, L, Hq, Hkv, D
+
+
+def capattn_fwd(q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None, workspace=None,
+                want_ml=False, stream=None):
+    """Forward.  q [B,L,Hq,D], k/v [B,L,Hkv,D] (bf16 or fp32, contiguous, on the GPU).
+    Returns (o, lse, m, l); m and l are None unless want_ml."""
+    B, L, Hq, Hkv, D = _shape(q, k)
+    cfg = make_config(ap, B, L, Hq, Hkv, D, q.dtype)
+    if workspace is None:
+        workspace = new_workspace(cfg, q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    m = torch.empty_like(lse) if want_ml else None
+    l = torch.empty_like(lse) if want_ml else None
+    st = lib().capattn_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(temp), _ptr(seg),
+                           _ptr(bounds), _ptr(o), _ptr(lse), _ptr(m), _ptr(l), _ptr(workspace),
+                           workspace.numel(), _stream(stream))
+    _check(st, "capattn_fwd")
+    return o, lse, m, l
+
+
+def capattn_bwd(q, k, v, o, lse, do, ap: AttnParams, temp=None, seg=None, bounds=None,
+                workspace=None, stream=None):
+    """Backward.  Returns (dq, dk, dv, delta)."""
+    B, L, Hq, Hkv, D = _shape(q, k)
+    cfg = make_config(ap, B, L, Hq, Hkv, D, q.dtype)
+    if workspace is None:
+        workspace = new_workspace(cfg, q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    delta = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    st = lib().capattn_bwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(temp), _ptr(seg),
+                           _ptr(bounds), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                           _ptr(dv), _ptr(delta), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    _check(st, "capattn_bwd")
+    return dq, dk, dv, delta
+
+
+def capattn_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
+    """Synchronises the stream; returns (status, raw bits) and clears the word."""
+    bits = ctypes.c_uint32(0)
+    st = lib().capattn_device_status(_ptr(workspace), _stream(stream), ctypes.byref(bits))
+    return int(st), int(bits.value)
+
+
+def capattn_tile_sizes(cfg: CapattnConfig):
+    bq, bk = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().capattn_tile_sizes(ctypes.byref(cfg), ctypes.byref(bq), ctypes.byref(bk)),
+           "capattn_tile_sizes")
+    return bq.value, bk.value
+
+
+def _np_ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def capattn_visit_map_host(cfg: CapattnConfig, seg=None, bounds=None, which=VISIT_Q_TILES):
+    """Visit bitmap (numpy uint32) from host seg / bounds (numpy int32, C-contiguous)."""
+    import numpy as np
+    n = ctypes.c_size_t(0)
+    _check(lib().capattn_visit_map_host(ctypes.byref(cfg), _np_ptr(seg), _np_ptr(bounds), which,
+                                        None, 0, ctypes.byref(n)), "capattn_visit_map_host")
+    out = np.zeros(n.value, dtype=np.uint32)
+    _check(lib().capattn_visit_map_host(ctypes.byref(cfg), _np_ptr(seg), _np_ptr(bounds), which,
+                                        _np_ptr(out), out.size, ctypes.byref(n)),
+           "capattn_visit_map_host")
+    return out
+
+
+def capattn_visit_map_device(cfg: CapattnConfig, seg=None, bounds=None, which=VISIT_Q_TILES,
+                             workspace=None, stream=None):
+    """The same bitmap built by the device pre-pass (seg / bounds: device tensors)."""
+    import numpy as np
+    bq, bk = capattn_tile_sizes(cfg)
+    nq, nk = -(-cfg.L // bq), -(-cfg.L // bk)
+    words = cfg.B * (nq * (-(-nk // 32)) if which == VISIT_Q_TILES else nk * (-(-nq // 32)))
+    dev = torch.device("cuda")
+    if workspace is None:
+        workspace = new_workspace(cfg, dev)
+    out = torch.zeros(words, dtype=torch.int32, device=dev)
+    _check(lib().capattn_visit_map_device(ctypes.byref(cfg), _ptr(seg), _ptr(bounds), which,
+                                          _ptr(out), words, _ptr(workspace), workspace.numel(),
+                                          _stream(stream)), "capattn_visit_map_device")
+    return out.cpu().numpy().view(np.uint32)
+
+
+def capattn_mask_bits_host(cfg: CapattnConfig, b: int, seg=None, bounds=None):
+    """Live-pair bit matrix of batch row b as a numpy bool array [L, L]."""
+    import numpy as np
+    wpr = -(-cfg.L // 64)
+    bits = np.zeros(wpr * cfg.L, dtype=np.uint64)
+    _check(lib().capattn_mask_bits_host(ctypes.byref(cfg), _np_ptr(seg), _np_ptr(bounds), b,
+                                        _np_ptr(bits), bits.size), "capattn_mask_bits_host")
+    by = bits.reshape(cfg.L, wpr).view(np.uint8)
+    return np.unpackbits(by, axis=1, bitorder="little")[:, :cfg.L].astype(bool)
+
+
+class CapAttnFunction(torch.autograd.Function):
+    """Autograd wrapper: forward saves (o, lse); backward calls capattn_bwd.
+    Gradients flow to q, k, v; temperature, segment ids and bounds are inputs only."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None):
+        o, lse, _, _ = capattn_fwd(q, k, v, ap, temp, seg, bounds)
+        ctx.save_for_backward(q, k, v, o, lse, temp, seg, bounds)
+        ctx.ap = ap
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, dlse):
+        q, k, v, o, lse, temp, seg, bounds = ctx.saved_tensors
+        dq, dk, dv, _ = capattn_bwd(q, k, v, o, lse, do.contiguous(), ctx.ap, temp, seg, bounds)
+        return dq, dk, dv, None, None, None, None
+
+
+def attention(q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None):
+    """Soft-capped attention output O (differentiable in q, k, v)."""
+    o, _ = CapAttnFunction.apply(q, k, v, ap, temp, seg, bounds)
+    return o

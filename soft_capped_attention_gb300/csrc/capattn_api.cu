@@ -1,0 +1,307 @@
+// C-ABI entry points: argument validation, workspace layout, cap constants,
+// host-side visit maps and mask bits, and the launch sequence of each pass.
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
+#include "capattn_internal.h"
+#include "row_span.h"
+
+namespace capattn {
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int tile_q(const capattn_config& c) { return c.dtype == CAPATTN_BF16 ? 128 : 64; }
+static int tile_kv(const capattn_config& c) { return c.dtype == CAPATTN_BF16 ? 128 : 64; }
+
+WorkspaceLayout workspace_layout(const capattn_config& c, int bq, int bk) {
+  WorkspaceLayout w;
+  const size_t nq = (c.L + bq - 1) / bq, nk = (c.L + bk - 1) / bk;
+  const size_t wq = (nq + 31) / 32, wk = (nk + 31) / 32;
+  w.status_off = 0;
+  w.rowinfo_off = 256;
+  w.qmap_off = align256(w.rowinfo_off + sizeof(int4) * (size_t)c.B * c.L);
+  w.kmap_off = align256(w.qmap_off + sizeof(uint32_t) * (size_t)c.B * nq * wk);
+  w.qfull_off = align256(w.kmap_off + sizeof(uint32_t) * (size_t)c.B * nk * wq);
+  w.total = align256(w.qfull_off + sizeof(int2) * (size_t)c.B * nq);
+  return w;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static capattn_status validate(const capattn_config* c) {
+  if (!c) return CAPATTN_ERR_INVALID_ARG;
+  if (c->struct_size != sizeof(capattn_config)) return CAPATTN_ERR_INVALID_ARG;
+  if (c->B < 1 || c->L < 1 || c->Hq < 1 || c->Hkv < 1 || c->D < 1) return CAPATTN_ERR_INVALID_ARG;
+  if (c->q_heads_per_kv_head < 1 || c->Hkv * c->q_heads_per_kv_head != c->Hq)
+    return CAPATTN_ERR_INVALID_ARG;
+  if (c->dtype != CAPATTN_BF16 && c->dtype != CAPATTN_FP32) return CAPATTN_ERR_INVALID_ARG;
+  if (c->cap_method < CAPATTN_CAP_NONE || c->cap_method > CAPATTN_CAP_ALSC)
+    return CAPATTN_ERR_INVALID_ARG;
+  if (!(isfinite(c->sm_scale)) || !(isfinite(c->cap)) || !(isfinite(c->alpha)) ||
+      !(isfinite(c->beta)) || !(isfinite(c->z_loss_weight)) || c->z_loss_weight < 0.f)
+    return CAPATTN_ERR_INVALID_ARG;
+  if (c->window_len < 0) return CAPATTN_ERR_INVALID_ARG;
+  // Index arithmetic in the kernels is 32-bit per (batch, head) plane and
+  // 64-bit across planes; keep one plane comfortably inside int32.
+  if ((int64_t)c->L * c->Hq * c->D >= (1ll << 31)) return CAPATTN_ERR_UNSUPPORTED;
+  if (c->dtype == CAPATTN_BF16 && c->D != 128) return CAPATTN_ERR_UNSUPPORTED;
+  if (c->dtype == CAPATTN_FP32 && c->D != 64 && c->D != 128) return CAPATTN_ERR_UNSUPPORTED;
+  return CAPATTN_OK;
+}
+
+static CapConsts make_cap(const capattn_config& c) {
+  CapConsts k;
+  memset(&k, 0, sizeof(k));
+  k.method = (c.cap > 0.f) ? c.cap_method : CAPATTN_CAP_NONE;
+  const double cap = c.cap > 0.f ? (double)c.cap : 1.0;
+  k.cap = (float)cap;
+  k.inv_cap = (float)(1.0 / cap);
+  if (k.method == CAPATTN_CAP_ALSC) {
+    const double ab = (double)c.alpha * (double)c.beta;
+    const double sb = 1.0 / (1.0 + exp(-ab));
+    const double denom = sb * (1.0 - sb) + 1e-12;
+    k.alsc_a = (float)((double)c.alpha / cap);
+    k.alsc_b = (float)ab;
+    k.alsc_out = (float)(cap / denom);
+    k.alsc_sb = (float)sb;
+    k.alsc_dout = (float)((double)c.alpha / denom);
+  }
+  return k;
+}
+
+static void fill_params(Params& p, const capattn_config& c, void* ws) {
+  memset(&p, 0, sizeof(p));
+  p.B = c.B; p.L = c.L; p.Hq = c.Hq; p.Hkv = c.Hkv; p.D = c.D; p.G = c.q_heads_per_kv_head;
+  p.block_q = tile_q(c);
+  p.block_kv = tile_kv(c);
+  p.nq = (c.L + p.block_q - 1) / p.block_q;
+  p.nk = (c.L + p.block_kv - 1) / p.block_kv;
+  p.wq = (p.nq + 31) / 32;
+  p.wk = (p.nk + 31) / 32;
+  p.sm_scale = c.sm_scale;
+  p.causal = c.causal ? 1 : 0;
+  p.window_len = c.window_len;
+  p.z_loss_weight = c.z_loss_weight;
+  p.cap = make_cap(c);
+  WorkspaceLayout w = workspace_layout(c, p.block_q, p.block_kv);
+  char* base = static_cast<char*>(ws);
+  p.status = reinterpret_cast<uint32_t*>(base + w.status_off);
+  p.rowinfo = reinterpret_cast<int4*>(base + w.rowinfo_off);
+  p.qmap = reinterpret_cast<uint32_t*>(base + w.qmap_off);
+  p.kmap = reinterpret_cast<uint32_t*>(base + w.kmap_off);
+  p.qfull = reinterpret_cast<int2*>(base + w.qfull_off);
+}
+
+static capattn_status check_ws(const capattn_config& c, void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return CAPATTN_ERR_WORKSPACE;
+  if (bytes < workspace_layout(c, tile_q(c), tile_kv(c)).total) return CAPATTN_ERR_WORKSPACE;
+  return CAPATTN_OK;
+}
+
+static capattn_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? CAPATTN_OK : CAPATTN_ERR_CUDA;
+}
+
+// Host restatement of the pre-pass, for the debug exports.
+static void host_spans(const capattn_config& c, const int32_t* seg, const int32_t* bounds, int b,
+                       std::vector<RowSpan>& spans) {
+  spans.resize(c.L);
+  const int32_t* srow = seg ? seg + (size_t)b * c.L : nullptr;
+  int32_t hl = 0, hu = 0, cl = 0, cu = 0;
+  if (bounds) {
+    hl = imin32(imax32(bounds[4 * b + 0], 0), c.L);
+    hu = imin32(imax32(bounds[4 * b + 1], 0), c.L);
+    cl = imin32(imax32(bounds[4 * b + 2], 0), c.L);
+    cu = imin32(imax32(bounds[4 * b + 3], 0), c.L);
+  }
+  for (int i = 0; i < c.L; ++i) {
+    int32_t first = 0, last1 = c.L;
+    if (srow) {
+      first = lower_bound_i32(srow, c.L, srow[i]);
+      last1 = upper_bound_i32(srow, c.L, srow[i]);
+    }
+    spans[i] = row_span(i, c.L, c.causal ? 1 : 0, c.window_len, first, last1, bounds ? 1 : 0, hl,
+                        hu, cl, cu);
+  }
+}
+
+}  // namespace capattn
+
+using namespace capattn;
+
+extern "C" {
+
+const char* capattn_status_string(capattn_status s) {
+  switch (s) {
+    case CAPATTN_OK: return "ok";
+    case CAPATTN_ERR_INVALID_ARG: return "invalid argument";
+    case CAPATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CAPATTN_ERR_CUDA: return "CUDA error";
+    case CAPATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case CAPATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case CAPATTN_ERR_DEVICE_DATA: return "invalid device data (segment ids or ranker bounds)";
+  }
+  return "unknown status";
+}
+
+capattn_status capattn_validate_config(const capattn_config* cfg) { return validate(cfg); }
+
+size_t capattn_workspace_bytes(const capattn_config* cfg, int pass) {
+  if (validate(cfg) != CAPATTN_OK) return 0;
+  if (pass != CAPATTN_PASS_FWD && pass != CAPATTN_PASS_BWD) return 0;
+  return workspace_layout(*cfg, tile_q(*cfg), tile_kv(*cfg)).total;
+}
+
+capattn_status capattn_tile_sizes(const capattn_config* cfg, int32_t* block_q, int32_t* block_kv) {
+  capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (block_q) *block_q = tile_q(*cfg);
+  if (block_kv) *block_kv = tile_kv(*cfg);
+  return CAPATTN_OK;
+}
+
+capattn_status capattn_fwd(const capattn_config* cfg, const void* q, const void* k, const void* v,
+                           const float* temp, const int32_t* seg, const int32_t* bounds, void* o,
+                           float* lse, float* m, float* l, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (!q || !k || !v || !o || !lse) return CAPATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, temp, seg, bounds, m, l};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
+  st = check_ws(*cfg, workspace, workspace_bytes);
+  if (st != CAPATTN_OK) return st;
+  Params p;
+  fill_params(p, *cfg, workspace);
+  p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
+  p.o = o; p.lse = lse; p.m = m; p.l = l;
+  cudaError_t e = launch_prepass(p, false, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = (cfg->dtype == CAPATTN_BF16) ? launch_fwd_bf16(p, stream) : launch_fwd_fp32(p, stream);
+  return cuda_status(e);
+}
+
+capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void* k, const void* v,
+                           const float* temp, const int32_t* seg, const int32_t* bounds,
+                           const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                           void* dv, float* delta, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
+    return CAPATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, temp, seg, bounds};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
+  st = check_ws(*cfg, workspace, workspace_bytes);
+  if (st != CAPATTN_OK) return st;
+  Params p;
+  fill_params(p, *cfg, workspace);
+  p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
+  p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
+  p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta;
+  cudaError_t e = launch_prepass(p, true, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_delta(p, cfg->dtype == CAPATTN_BF16, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = (cfg->dtype == CAPATTN_BF16) ? launch_bwd_bf16(p, stream) : launch_bwd_fp32(p, stream);
+  return cuda_status(e);
+}
+
+capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint32_t* raw_bits) {
+  if (!workspace) return CAPATTN_ERR_WORKSPACE;
+  uint32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return CAPATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CAPATTN_ERR_CUDA;
+  if (bits && cudaMemsetAsync(workspace, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return CAPATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CAPATTN_ERR_CUDA;
+  if (raw_bits) *raw_bits = bits;
+  if (bits & kStatusTimeoutBit) return CAPATTN_ERR_DEVICE_TIMEOUT;
+  if (bits) return CAPATTN_ERR_DEVICE_DATA;
+  return CAPATTN_OK;
+}
+
+capattn_status capattn_visit_map_host(const capattn_config* cfg, const int32_t* seg,
+                                      const int32_t* bounds, int which, uint32_t* out,
+                                      size_t out_words, size_t* n_words) {
+  capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (which != CAPATTN_VISIT_Q_TILES && which != CAPATTN_VISIT_KV_TILES)
+    return CAPATTN_ERR_INVALID_ARG;
+  const int bq = tile_q(*cfg), bk = tile_kv(*cfg);
+  const int nq = (cfg->L + bq - 1) / bq, nk = (cfg->L + bk - 1) / bk;
+  const int wq = (nq + 31) / 32, wk = (nk + 31) / 32;
+  const size_t need = which == CAPATTN_VISIT_Q_TILES ? (size_t)cfg->B * nq * wk
+                                                     : (size_t)cfg->B * nk * wq;
+  if (n_words) *n_words = need;
+  if (!out) return out_words == 0 ? CAPATTN_OK : CAPATTN_ERR_INVALID_ARG;
+  if (out_words < need) return CAPATTN_ERR_INVALID_ARG;
+  memset(out, 0, need * sizeof(uint32_t));
+  std::vector<RowSpan> spans;
+  for (int b = 0; b < cfg->B; ++b) {
+    host_spans(*cfg, seg, bounds, b, spans);
+    for (int i = 0; i < cfg->L; ++i) {
+      const RowSpan& r = spans[i];
+      const int qt = i / bq;
+      auto mark = [&](int kt) {
+        if (which == CAPATTN_VISIT_Q_TILES)
+          out[((size_t)b * nq + qt) * wk + kt / 32] |= 1u << (kt % 32);
+        else
+          out[((size_t)b * nk + kt) * wq + qt / 32] |= 1u << (qt % 32);
+      };
+      if (r.hi > r.lo)
+        for (int kt = r.lo / bk; kt <= (r.hi - 1) / bk; ++kt) mark(kt);
+      if (r.e >= 0) mark(r.e / bk);
+    }
+  }
+  return CAPATTN_OK;
+}
+
+capattn_status capattn_visit_map_device(const capattn_config* cfg, const int32_t* seg,
+                                        const int32_t* bounds, int which, uint32_t* out,
+                                        size_t out_words, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (which != CAPATTN_VISIT_Q_TILES && which != CAPATTN_VISIT_KV_TILES)
+    return CAPATTN_ERR_INVALID_ARG;
+  st = check_ws(*cfg, workspace, workspace_bytes);
+  if (st != CAPATTN_OK) return st;
+  Params p;
+  fill_params(p, *cfg, workspace);
+  p.seg = seg;
+  p.bounds = bounds;
+  const size_t need = which == CAPATTN_VISIT_Q_TILES ? (size_t)p.B * p.nq * p.wk
+                                                     : (size_t)p.B * p.nk * p.wq;
+  if (!out || out_words < need) return CAPATTN_ERR_INVALID_ARG;
+  cudaError_t e = launch_prepass(p, true, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = cudaMemcpyAsync(out, which == CAPATTN_VISIT_Q_TILES ? p.qmap : p.kmap,
+                      need * sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream);
+  return cuda_status(e);
+}
+
+capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* seg,
+                                      const int32_t* bounds, int32_t b, uint64_t* bits,
+                                      size_t n_words) {
+  capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (b < 0 || b >= cfg->B || !bits) return CAPATTN_ERR_INVALID_ARG;
+  const size_t wpr = (cfg->L + 63) / 64;
+  if (n_words < wpr * cfg->L) return CAPATTN_ERR_INVALID_ARG;
+  memset(bits, 0, wpr * cfg->L * sizeof(uint64_t));
+  std::vector<RowSpan> spans;
+  host_spans(*cfg, seg, bounds, b, spans);
+  for (int i = 0; i < cfg->L; ++i)
+    for (int j = 0; j < cfg->L; ++j)
+      if (span_live(spans[i], j)) bits[i * wpr + j / 64] |= 1ull << (j % 64);
+  return CAPATTN_OK;
+}
+
+}  // extern "C"

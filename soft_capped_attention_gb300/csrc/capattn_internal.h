@@ -1,0 +1,73 @@
+// Internal interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/capattn.h"
+#include "status_bits.h"
+
+namespace capattn {
+
+// Cap constants, precomputed on the host in double precision
+// (mosaic_backward.py _apply_cap_mosaic; derivative of each branch).
+struct CapConsts {
+  int32_t method;     // CAPATTN_CAP_*, NONE when cap <= 0
+  float cap;          // tanh: output scale
+  float inv_cap;      // tanh: 1/cap (argument scale); soft_sign: 1/cap
+  float alsc_a;       // ALSC: z = alsc_a * s + alsc_b, alsc_a = alpha / cap
+  float alsc_b;       //       alsc_b = alpha * beta
+  float alsc_out;     // ALSC: cap / denom
+  float alsc_sb;      // ALSC: sigma(alpha * beta)
+  float alsc_dout;    // ALSC: derivative scale alpha / denom
+};
+
+struct Params {
+  // tensors
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* temp;      // [B, L] or null
+  const int32_t* seg;     // [B, L] or null
+  const int32_t* bounds;  // [B, 4] or null
+  void* o;
+  float* lse;
+  float* m;               // nullable
+  float* l;               // nullable
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;
+  // workspace pieces
+  uint32_t* status;
+  int4* rowinfo;          // [B, L] (lo, hi, e, 0)
+  uint32_t* qmap;         // [B, nq, wk]
+  uint32_t* kmap;         // [B, nk, wq]
+  int2* qfull;            // [B, nq]: KV tiles [x, y) in which every pair is live
+  // shapes
+  int32_t B, L, Hq, Hkv, D, G;
+  int32_t block_q, block_kv, nq, nk, wq, wk;
+  // method
+  float sm_scale;
+  int32_t causal, window_len;
+  float z_loss_weight;
+  CapConsts cap;
+};
+
+struct WorkspaceLayout {
+  size_t status_off, rowinfo_off, qmap_off, kmap_off, qfull_off, total;
+};
+
+WorkspaceLayout workspace_layout(const capattn_config& c, int block_q, int block_kv);
+
+// Launchers.  Each returns cudaGetLastError() after the launch.
+cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s);
+cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
+cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
+cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);
+cudaError_t launch_bwd_bf16(const Params& p, cudaStream_t s);
+
+}  // namespace capattn

@@ -1,0 +1,169 @@
+// Pre-pass kernels: per-row live key spans, block visit maps, and the delta
+// pre-pass of the backward (mosaic_backward.py make_preprocess_backward_kernel,
+// with delta = rowsum(O * dO) on the normalised O and the unscaled dO).
+#include <cuda_bf16.h>
+
+#include "capattn_internal.h"
+#include "row_span.h"
+
+namespace capattn {
+
+// One thread per (b, i): the run of equal segment ids around i (binary search
+// on a non-decreasing row), the clamped ranker bounds, and the row's span.
+__global__ void rowinfo_kernel(Params p) {
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= p.L) return;
+  int32_t first = 0, last1 = p.L;
+  if (p.seg) {
+    const int32_t* srow = p.seg + (size_t)b * p.L;
+    const int32_t x = srow[i];
+    if (i > 0 && srow[i - 1] > x) atomicOr(p.status, kStatusBadSegmentsBit);
+    first = lower_bound_i32(srow, p.L, x);
+    last1 = upper_bound_i32(srow, p.L, x);
+  }
+  int32_t hl = 0, hu = 0, cl = 0, cu = 0;
+  if (p.bounds) {
+    const int4 bd = reinterpret_cast<const int4*>(p.bounds)[b];
+    if (i == 0 && !(bd.x >= 0 && bd.x <= bd.y && bd.y <= p.L && bd.z >= 0 && bd.z <= bd.w &&
+                    bd.w <= p.L))
+      atomicOr(p.status, kStatusBadBoundsBit);
+    hl = imin32(imax32(bd.x, 0), p.L);
+    hu = imin32(imax32(bd.y, 0), p.L);
+    cl = imin32(imax32(bd.z, 0), p.L);
+    cu = imin32(imax32(bd.w, 0), p.L);
+  }
+  const RowSpan r = row_span(i, p.L, p.causal, p.window_len, first, last1, p.bounds ? 1 : 0, hl,
+                             hu, cl, cu);
+  p.rowinfo[(size_t)b * p.L + i] = make_int4(r.lo, r.hi, r.e, 0);
+}
+
+__device__ __forceinline__ void set_bit_range(uint32_t* bm, int a, int c) {
+  for (int w = a >> 5; w <= (c >> 5); ++w) {
+    const int lo = (w == (a >> 5)) ? (a & 31) : 0;
+    const int hi = (w == (c >> 5)) ? (c & 31) : 31;
+    const uint32_t upto = hi == 31 ? 0xFFFFFFFFu : ((1u << (hi + 1)) - 1u);
+    atomicOr(&bm[w], upto & ~((1u << lo) - 1u));
+  }
+}
+
+// One CTA per (query tile, b): OR of the KV tiles touched by the tile's rows,
+// and the range of KV tiles every row of the tile covers completely (the
+// tiles in which no pair needs a mask test).  A tile with rows past L has no
+// fully covered KV tile.
+__global__ void qmap_kernel(Params p) {
+  extern __shared__ uint32_t bm[];
+  __shared__ int full_lo, full_hi;
+  const int qt = blockIdx.x, b = blockIdx.y;
+  for (int w = threadIdx.x; w < p.wk; w += blockDim.x) bm[w] = 0u;
+  if (threadIdx.x == 0) {
+    full_lo = 0;
+    full_hi = p.nk;
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < p.block_q; t += blockDim.x) {
+    const int i = qt * p.block_q + t;
+    int fa = 1, fb = 0;  // empty
+    if (i < p.L) {
+      const int4 r = p.rowinfo[(size_t)b * p.L + i];
+      if (r.y > r.x) {
+        set_bit_range(bm, r.x / p.block_kv, (r.y - 1) / p.block_kv);
+        fa = (r.x + p.block_kv - 1) / p.block_kv;
+        fb = r.y / p.block_kv;
+      }
+      if (r.z >= 0) {
+        const int kt = r.z / p.block_kv;
+        atomicOr(&bm[kt >> 5], 1u << (kt & 31));
+      }
+    }
+    atomicMax(&full_lo, fa);
+    atomicMin(&full_hi, fb);
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < p.wk; w += blockDim.x)
+    p.qmap[((size_t)b * p.nq + qt) * p.wk + w] = bm[w];
+  if (threadIdx.x == 0) p.qfull[(size_t)b * p.nq + qt] = make_int2(full_lo, full_hi);
+}
+
+// One CTA per (KV tile, b): transpose of the query-tile map.
+__global__ void kmap_kernel(Params p) {
+  const int kt = blockIdx.x, b = blockIdx.y;
+  for (int w = threadIdx.x; w < p.wq; w += blockDim.x) {
+    uint32_t word = 0u;
+    for (int bit = 0; bit < 32; ++bit) {
+      const int qt = w * 32 + bit;
+      if (qt >= p.nq) break;
+      const uint32_t src = p.qmap[((size_t)b * p.nq + qt) * p.wk + (kt >> 5)];
+      word |= ((src >> (kt & 31)) & 1u) << bit;
+    }
+    p.kmap[((size_t)b * p.nk + kt) * p.wq + w] = word;
+  }
+}
+
+cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
+  dim3 g1((p.L + 255) / 256, p.B);
+  rowinfo_kernel<<<g1, 256, 0, s>>>(p);
+  dim3 g2(p.nq, p.B);
+  qmap_kernel<<<g2, 128, p.wk * sizeof(uint32_t), s>>>(p);
+  if (build_kmap) {
+    dim3 g3(p.nk, p.B);
+    kmap_kernel<<<g3, 32, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ delta
+// One warp per (b, i, h) row of D elements: delta[b, h, i] = sum_d O * dO.
+template <typename T, int D>
+__global__ void delta_kernel(Params p) {
+  constexpr int VEC = D / 32;
+  const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const long long nrows = (long long)p.B * p.L * p.Hq;
+  if (row >= nrows) return;
+  const T* o = static_cast<const T*>(p.o) + row * D + lane * VEC;
+  const T* g = static_cast<const T*>(p.dO) + row * D + lane * VEC;
+  float acc = 0.f;
+  if constexpr (sizeof(T) == 2) {
+    static_assert(VEC == 4, "bf16 path expects D = 128");
+    const uint2 a = *reinterpret_cast<const uint2*>(o);
+    const uint2 c = *reinterpret_cast<const uint2*>(g);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const float2 x = __bfloat1622float2(a2[t]);
+      const float2 y = __bfloat1622float2(c2[t]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < VEC; ++t) acc = fmaf(o[t], g[t], acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) {
+    const int h = (int)(row % p.Hq);
+    const long long bi = row / p.Hq;
+    const int i = (int)(bi % p.L);
+    const int b = (int)(bi / p.L);
+    p.delta[((size_t)b * p.Hq + h) * p.L + i] = acc;
+  }
+}
+
+cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
+  const long long nrows = (long long)p.B * p.L * p.Hq;
+  const int warps = 8;
+  const unsigned grid = (unsigned)((nrows + warps - 1) / warps);
+  if (bf16) {
+    delta_kernel<__nv_bfloat16, 128><<<grid, warps * 32, 0, s>>>(p);
+  } else if (p.D == 64) {
+    delta_kernel<float, 64><<<grid, warps * 32, 0, s>>>(p);
+  } else {
+    delta_kernel<float, 128><<<grid, warps * 32, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace capattn

@@ -1,0 +1,204 @@
+"""CPU tests of the C-ABI boundary: the library loads, exports what the header
+declares, validates arguments on the host, and its host-side mask bits and
+visit maps are bit-exact against the oracle's brute force."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import capattn_oracle as orc
+from soft_capped_attention_gb300 import capattn as ca
+from soft_capped_attention_gb300.workloads import WORKLOADS, make_aux
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ca.LIB_PATH):
+        from soft_capped_attention_gb300 import build
+        build.build()
+    return ca.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "capattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(capattn_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(ca.EXPORTED_SYMBOLS)
+
+
+def _cfg(**kw):
+    base = dict(B=2, L=300, Hq=4, Hkv=2, D=128, dtype=torch.bfloat16)
+    base.update(kw)
+    ap = ca.AttnParams(sm_scale=0.1, cap_method=base.pop("cap_method", "tanh"),
+                       cap=base.pop("cap", 5.0), causal=base.pop("causal", True),
+                       window_len=base.pop("window_len", 0))
+    return ca.make_config(ap, **base)
+
+
+def test_validation_codes(lib):
+    v = lambda c: lib.capattn_validate_config(ctypes.byref(c))
+    assert v(_cfg()) == 0
+    assert v(_cfg(Hq=3)) == 1                 # Hq not a multiple of Hkv
+    assert v(_cfg(L=0)) == 1
+    assert v(_cfg(D=64)) == 2                 # bf16 needs D = 128
+    assert v(_cfg(D=64, dtype=torch.float32)) == 0
+    assert v(_cfg(D=96, dtype=torch.float32)) == 2
+    c = _cfg()
+    c.struct_size = 4
+    assert v(c) == 1
+    c = _cfg()
+    c.cap_method = 7
+    assert v(c) == 1
+    c = _cfg()
+    c.z_loss_weight = -1.0
+    assert v(c) == 1
+    c = _cfg()
+    c.window_len = -3
+    assert v(c) == 1
+    assert lib.capattn_workspace_bytes(ctypes.byref(_cfg(Hq=3)), 0) == 0
+    assert lib.capattn_workspace_bytes(ctypes.byref(_cfg()), 0) > 0
+    assert lib.capattn_status_string(4) == b"a kernel gave up on a bounded wait"
+
+
+def test_compute_calls_reject_bad_arguments_before_launch(lib):
+    c = _cfg()
+    ws = (ctypes.c_uint8 * 4096)()
+    # null q: rejected on the host, nothing is launched
+    st = lib.capattn_fwd(ctypes.byref(c), None, ctypes.c_void_p(16), ctypes.c_void_p(16), None,
+                         None, None, ctypes.c_void_p(16), ctypes.c_void_p(16), None, None,
+                         ctypes.c_void_p(256), 1 << 20, None)
+    assert st == 1
+    # misaligned pointer
+    st = lib.capattn_fwd(ctypes.byref(c), ctypes.c_void_p(18), ctypes.c_void_p(16),
+                         ctypes.c_void_p(16), None, None, None, ctypes.c_void_p(16),
+                         ctypes.c_void_p(16), None, None, ctypes.c_void_p(256), 1 << 20, None)
+    assert st == 1
+    # workspace too small
+    st = lib.capattn_fwd(ctypes.byref(c), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                         ctypes.c_void_p(16), None, None, None, ctypes.c_void_p(16),
+                         ctypes.c_void_p(16), None, None, ctypes.c_void_p(256), 8, None)
+    assert st == 5
+    st = lib.capattn_bwd(ctypes.byref(c), *([ctypes.c_void_p(16)] * 3), None, None, None,
+                         *([ctypes.c_void_p(16)] * 3), None, *([ctypes.c_void_p(16)] * 3),
+                         ctypes.c_void_p(256), 1 << 20, None)
+    assert st == 1  # null dq
+
+
+def _oracle_cfg(causal, window_len):
+    return orc.OracleConfig(sm_scale=1.0, causal=causal, window_len=window_len)
+
+
+CASES = [
+    dict(causal=False, window_len=0, seg=None, bounds=None),
+    dict(causal=True, window_len=0, seg=None, bounds=None),
+    dict(causal=True, window_len=37, seg=None, bounds=None),
+    dict(causal=False, window_len=50, seg=None, bounds=None),
+    dict(causal=True, window_len=0, seg="packed", bounds=None),
+    dict(causal=False, window_len=0, seg="packed", bounds=None),
+    dict(causal=True, window_len=29, seg="packed", bounds=None),
+    dict(causal=False, window_len=0, seg=None, bounds="ranker"),
+    dict(causal=True, window_len=0, seg=None, bounds="ranker"),
+    dict(causal=True, window_len=40, seg="packed", bounds="ranker"),
+]
+
+
+def _aux(case, B, L, rng):
+    seg = bounds = None
+    if case["seg"]:
+        seg = np.zeros((B, L), np.int32)
+        for b in range(B):
+            cuts = np.sort(rng.choice(np.arange(1, L), size=5, replace=False))
+            for c in cuts:
+                seg[b, c:] += 1
+    if case["bounds"]:
+        bounds = np.zeros((B, 4), np.int32)
+        for b in range(B):
+            hl = int(rng.integers(0, L // 3))
+            hu = int(rng.integers(hl, L))
+            cl = int(rng.integers(hu // 2, L))
+            cu = int(rng.integers(cl, L + 1))
+            bounds[b] = (hl, hu, cl, cu)
+    return seg, bounds
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("L", [1, 63, 130, 300])
+def test_mask_bits_match_oracle(lib, case, L):
+    cs = CASES[case]
+    rng = np.random.default_rng(case * 1000 + L)
+    B = 2
+    seg, bounds = _aux(cs, B, L, rng) if L > 8 else (None, None)
+    c = _cfg(B=B, L=L, causal=cs["causal"], window_len=cs["window_len"])
+    ocfg = _oracle_cfg(cs["causal"], cs["window_len"])
+    for b in range(B):
+        bits = ca.capattn_mask_bits_host(c, b, seg, bounds)
+        ref = orc.mask_matrix(L, ocfg, None if seg is None else seg[b],
+                              None if bounds is None else bounds[b])
+        assert np.array_equal(bits, ref)
+
+
+def _pack(V):
+    nr, nc = V.shape
+    words = -(-nc // 32)
+    out = np.zeros((nr, words), np.uint32)
+    for w in range(words):
+        blk = V[:, w * 32:(w + 1) * 32]
+        for bit in range(blk.shape[1]):
+            out[:, w] |= blk[:, bit].astype(np.uint32) << np.uint32(bit)
+    return out
+
+
+def oracle_visit_words(B, L, bq, bk, ocfg, seg, bounds, which):
+    rows = []
+    for b in range(B):
+        V = orc.visit_matrix(L, bq, bk, ocfg, None if seg is None else seg[b],
+                             None if bounds is None else bounds[b])
+        rows.append(_pack(V if which == ca.VISIT_Q_TILES else V.T))
+    return np.concatenate(rows, axis=0).reshape(-1)
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("L,dtype", [(300, torch.bfloat16), (777, torch.bfloat16),
+                                     (200, torch.float32), (4100, torch.bfloat16)])
+def test_visit_maps_match_oracle(lib, case, L, dtype):
+    cs = CASES[case]
+    rng = np.random.default_rng(case + 7 * L)
+    B = 2
+    seg, bounds = _aux(cs, B, L, rng)
+    D = 128 if dtype == torch.bfloat16 else 64
+    c = _cfg(B=B, L=L, D=D, dtype=dtype, causal=cs["causal"], window_len=cs["window_len"])
+    bq, bk = ca.capattn_tile_sizes(c)
+    ocfg = _oracle_cfg(cs["causal"], cs["window_len"])
+    for which in (ca.VISIT_Q_TILES, ca.VISIT_KV_TILES):
+        got = ca.capattn_visit_map_host(c, seg, bounds, which)
+        ref = oracle_visit_words(B, L, bq, bk, ocfg, seg, bounds, which)
+        assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4, 5])
+def test_visit_maps_of_the_five_workloads(lib, idx):
+    w = WORKLOADS[idx]
+    aux = make_aux(w, seed=idx)
+    B = min(w.B, 4)
+    seg = None if aux["seg"] is None else np.ascontiguousarray(aux["seg"][:B])
+    bounds = None if aux["bounds"] is None else np.ascontiguousarray(aux["bounds"][:B])
+    c = ca.make_config(ca.params_from_workload(w), B, w.L, w.Hq, w.Hkv, w.D, torch.bfloat16)
+    bq, bk = ca.capattn_tile_sizes(c)
+    ocfg = orc.config_from_workload(w)
+    for which in (ca.VISIT_Q_TILES, ca.VISIT_KV_TILES):
+        got = ca.capattn_visit_map_host(c, seg, bounds, which)
+        ref = oracle_visit_words(B, w.L, bq, bk, ocfg, seg, bounds, which)
+        assert np.array_equal(got, ref)

@@ -1,0 +1,178 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle,
+element by element, on shapes that span several tiles and a ragged tail."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import capattn_oracle as orc
+from soft_capped_attention_gb300 import capattn as ca
+from soft_capped_attention_gb300.workloads import WORKLOADS, make_inputs, round_to_bf16
+
+from parity_utils import compare, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+CAPS = {"none": (0.0, 0.0, 0.0), "tanh": (50.0, 0.0, 0.0), "soft_sign": (20.0, 0.0, 0.0),
+        "alsc": (30.0, 2.0, 0.5)}
+MASKS = {
+    "full": dict(causal=False, window_len=0, seg=False, ranker=False),
+    "causal": dict(causal=True, window_len=0, seg=False, ranker=False),
+    "window": dict(causal=True, window_len=200, seg=False, ranker=False),
+    "window_nc": dict(causal=False, window_len=77, seg=False, ranker=False),
+    "packed": dict(causal=True, window_len=0, seg=True, ranker=False),
+    "ranker": dict(causal=False, window_len=0, seg=False, ranker=True),
+}
+
+
+def make_case(B, L, Hq, Hkv, D, dtype, mask, temp, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    r = lambda *s: (rng.standard_normal(s) * scale).astype(np.float32)
+    inp = {"q": r(B, L, Hq, D), "k": r(B, L, Hkv, D), "v": rng.standard_normal((B, L, Hkv, D)).astype(np.float32),
+           "do": rng.standard_normal((B, L, Hq, D)).astype(np.float32)}
+    if dtype == torch.bfloat16:
+        for n in ("q", "k", "v", "do"):
+            inp[n] = round_to_bf16(inp[n])
+    inp["temp"] = rng.uniform(0.5, 1.5, size=(B, L)).astype(np.float32) if temp else None
+    inp["seg"] = None
+    inp["bounds"] = None
+    m = MASKS[mask]
+    if m["seg"]:
+        seg = np.zeros((B, L), np.int32)
+        for b in range(B):
+            cuts = np.sort(rng.choice(np.arange(1, L), size=min(4, L - 1), replace=False))
+            for c in cuts:
+                seg[b, c:] += 1
+        inp["seg"] = seg
+    if m["ranker"]:
+        bd = np.zeros((B, 4), np.int32)
+        for b in range(B):
+            hu = int(rng.integers(L // 4, 3 * L // 4))
+            bd[b] = (0, hu, hu, min(L, hu + int(rng.integers(5, 60))))
+        inp["bounds"] = bd
+    return inp
+
+
+def params(cap, mask, z):
+    c, a, bta = CAPS[cap]
+    m = MASKS[mask]
+    return ca.AttnParams(sm_scale=float(1.0 / np.sqrt(128.0)), cap_method=cap, cap=c, alpha=a,
+                         beta=bta, causal=m["causal"], window_len=m["window_len"], z_loss_weight=z)
+
+
+BF16_CASES = [
+    # (B, L, Hq, Hkv, cap, mask, temp, z)
+    (1, 128, 2, 2, "none", "full", False, 0.0),
+    (2, 300, 4, 2, "tanh", "causal", False, 0.0),
+    (1, 513, 4, 1, "alsc", "window", True, 1e-4),
+    (2, 384, 2, 2, "soft_sign", "packed", False, 0.0),
+    (2, 400, 4, 2, "alsc", "ranker", False, 0.0),
+    (1, 257, 2, 1, "tanh", "window_nc", True, 0.01),
+    (1, 1000, 2, 2, "soft_sign", "causal", True, 0.0),
+    (2, 640, 8, 2, "none", "packed", True, 0.001),
+    (1, 77, 2, 2, "alsc", "full", False, 0.0),
+    (1, 1, 2, 1, "tanh", "causal", False, 0.0),
+    (1, 130, 2, 2, "none", "ranker", True, 0.05),
+]
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_bf16_matches_oracle(case):
+    B, L, Hq, Hkv, cap, mask, temp, z = case
+    inp = make_case(B, L, Hq, Hkv, 128, torch.bfloat16, mask, temp, seed=L * 7 + Hq)
+    ap = params(cap, mask, z)
+    got = run_gpu(inp, ap, torch.bfloat16)
+    ref = run_oracle(inp, ap)
+    compare(got, ref, torch.bfloat16)
+
+
+FP32_CASES = [
+    (1, 128, 2, 2, 64, "none", "full", False, 0.0),
+    (2, 200, 4, 2, 64, "tanh", "causal", True, 0.0),
+    (1, 131, 2, 1, 128, "alsc", "window", True, 1e-3),
+    (2, 190, 2, 2, 64, "soft_sign", "packed", False, 0.0),
+    (2, 150, 4, 2, 128, "alsc", "ranker", False, 0.02),
+    (1, 65, 2, 2, 64, "none", "window_nc", True, 0.0),
+]
+
+
+@pytest.mark.parametrize("case", FP32_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_fp32_matches_oracle(case):
+    B, L, Hq, Hkv, D, cap, mask, temp, z = case
+    inp = make_case(B, L, Hq, Hkv, D, torch.float32, mask, temp, seed=L * 3 + D)
+    ap = params(cap, mask, z)
+    got = run_gpu(inp, ap, torch.float32)
+    ref = run_oracle(inp, ap)
+    compare(got, ref, torch.float32)
+
+
+def test_workload_1_tiny_fp32_full():
+    w = WORKLOADS[1]
+    inp = make_inputs(w, seed=1)
+    ap = ca.params_from_workload(w)
+    got = run_gpu(inp, ap, torch.float32, want_ml=True)
+    ref = run_oracle(inp, ap)
+    compare(got, ref, torch.float32)
+    np.testing.assert_allclose(got["delta"], ref["delta"], atol=1e-4)
+    np.testing.assert_allclose(got["m"], ref["m"], atol=1e-4)
+    np.testing.assert_allclose(got["l"], ref["l"], rtol=1e-4)
+
+
+def test_residuals_m_l_and_delta_bf16():
+    inp = make_case(2, 300, 4, 2, 128, torch.bfloat16, "ranker", True, seed=5)
+    ap = params("tanh", "ranker", 0.0)
+    got = run_gpu(inp, ap, torch.bfloat16, want_ml=True)
+    ref = run_oracle(inp, ap)
+    live = np.isfinite(ref["LSE"])
+    assert np.array_equal(np.isneginf(got["m"]), ~live)
+    np.testing.assert_allclose(got["m"][live], ref["m"][live], atol=1e-3)
+    np.testing.assert_allclose(got["l"][live], ref["l"][live], rtol=5e-3)
+    assert np.all(got["l"][~live] == 0)
+    # LSE = m + log l
+    np.testing.assert_allclose(got["LSE"][live], got["m"][live] + np.log(got["l"][live]), atol=1e-5)
+    assert np.max(np.abs(got["delta"] - ref["delta"])) < 5e-2
+
+
+def test_fully_masked_rows_are_exact():
+    # ranker rows at or past cu see nothing: O = 0, LSE = -inf, no gradient
+    inp = make_case(1, 256, 2, 2, 128, torch.bfloat16, "ranker", False, seed=9)
+    inp["bounds"] = np.array([[0, 100, 100, 120]], np.int32)
+    ap = params("alsc", "ranker", 1e-3)
+    got = run_gpu(inp, ap, torch.bfloat16)
+    assert np.all(got["O"][0, 120:] == 0)
+    assert np.all(np.isneginf(got["LSE"][0, :, 120:]))
+    assert np.all(got["dQ"][0, 120:] == 0)
+    assert np.all(np.isfinite(got["dK"])) and np.all(np.isfinite(got["dV"]))
+    # keys past hu that are not a candidate's own position get no gradient
+    assert np.all(got["dK"][0, 120:] == 0) and np.all(got["dV"][0, 120:] == 0)
+
+
+def test_device_status_reports_bad_segments_and_bounds():
+    inp = make_case(1, 200, 2, 2, 128, torch.bfloat16, "packed", False, seed=3)
+    ap = params("none", "packed", 0.0)
+    q, k, v = (to_dev(inp[n], torch.bfloat16) for n in ("q", "k", "v"))
+    cfg = ca.make_config(ap, 1, 200, 2, 2, 128, torch.bfloat16)
+    ws = ca.new_workspace(cfg, q.device)
+    seg = to_dev(np.ascontiguousarray(inp["seg"][:, ::-1]))  # decreasing ids
+    ca.capattn_fwd(q, k, v, ap, None, seg, None, workspace=ws)
+    st, bits = ca.capattn_device_status(ws)
+    assert st == 6 and bits & 2
+    assert ca.capattn_device_status(ws)[0] == 0  # cleared
+    bounds = to_dev(np.array([[0, 300, 10, 20]], np.int32))
+    ca.capattn_fwd(q, k, v, ap, None, None, bounds, workspace=ws)
+    st, bits = ca.capattn_device_status(ws)
+    assert st == 6 and bits & 4
+
+
+def test_autograd_function_matches_direct_calls():
+    inp = make_case(1, 300, 4, 2, 128, torch.bfloat16, "causal", True, seed=4)
+    ap = params("tanh", "causal", 0.0)
+    q, k, v, do = (to_dev(inp[n], torch.bfloat16) for n in ("q", "k", "v", "do"))
+    temp = to_dev(inp["temp"])
+    qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o = ca.attention(qq, kk, vv, ap, temp)
+    o.backward(do)
+    o2, lse, _, _ = ca.capattn_fwd(q, k, v, ap, temp)
+    dq, dk, dv, _ = ca.capattn_bwd(q, k, v, o2, lse, do, ap, temp)
+    assert torch.equal(o, o2)
+    assert torch.equal(qq.grad, dq) and torch.equal(kk.grad, dk) and torch.equal(vv.grad, dv)
