@@ -189,6 +189,20 @@ capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* 
                                       const int32_t* bounds, int32_t b, uint64_t* bits,
                                       size_t n_words);
 
+/*
+ * Per-kernel timing.  While enabled, every kernel the library launches is
+ * bracketed by CUDA events recorded on the caller's stream (library-owned
+ * events; a small fixed pool).  capattn_profile_read synchronises those events
+ * and returns, per kernel kind (CAPATTN_KERNEL_*), the summed milliseconds and
+ * launch counts since the last reset (reset = nonzero clears after reading).
+ * Not thread-safe; meant for benchmarking.  Disabled by default.
+ */
+enum { CAPATTN_KERNEL_PREPASS = 0, CAPATTN_KERNEL_FWD = 1, CAPATTN_KERNEL_DELTA = 2,
+       CAPATTN_KERNEL_DKV = 3, CAPATTN_KERNEL_DQ = 4, CAPATTN_KERNEL_KINDS = 5 };
+capattn_status capattn_profile_enable(int on);
+capattn_status capattn_profile_read(double* ms, int64_t* launches, int n_kinds, int reset);
+const char* capattn_kernel_name(int kind);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,13 +80,22 @@ def lib() -> ctypes.CDLL:
         h.capattn_visit_map_device.argtypes = [cfgp, vp, vp, ctypes.c_int, vp, sz, vp, sz, vp]
         h.capattn_mask_bits_host.restype = ctypes.c_int
         h.capattn_mask_bits_host.argtypes = [cfgp, vp, vp, i32, vp, sz]
+        h.capattn_profile_enable.restype = ctypes.c_int
+        h.capattn_profile_enable.argtypes = [ctypes.c_int]
+        h.capattn_profile_read.restype = ctypes.c_int
+        h.capattn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int]
+        h.capattn_kernel_name.restype = ctypes.c_char_p
+        h.capattn_kernel_name.argtypes = [ctypes.c_int]
         _lib_handle = h
     return _lib_handle
 
 
 EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn_workspace_bytes",
                     "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_device_status",
-                    "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host")
+                    "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host",
+                    "capattn_profile_enable", "capattn_profile_read", "capattn_kernel_name")
+KERNEL_KINDS = ("prepass", "fwd", "delta", "dkv", "dq")
 
 
 @dataclass(frozen=True)
@@ -255,6 +264,19 @@ def capattn_mask_bits_host(cfg: CapattnConfig, b: int, seg=None, bounds=None):
                                         _np_ptr(bits), bits.size), "capattn_mask_bits_host")
     by = bits.reshape(cfg.L, wpr).view(np.uint8)
     return np.unpackbits(by, axis=1, bitorder="little")[:, :cfg.L].astype(bool)
+
+
+def capattn_profile_enable(on: bool = True):
+    _check(lib().capattn_profile_enable(1 if on else 0), "capattn_profile_enable")
+
+
+def capattn_profile_read(reset: bool = True) -> dict:
+    """{kernel kind: (milliseconds, launches)} since the last reset (synchronises)."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(lib().capattn_profile_read(ms, cnt, n, 1 if reset else 0), "capattn_profile_read")
+    return {KERNEL_KINDS[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
 
 
 class CapAttnFunction(torch.autograd.Function):

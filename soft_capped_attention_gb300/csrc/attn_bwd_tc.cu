@@ -530,13 +530,19 @@ struct BwdTcLaunch {
     auto kdkv = dkv_tc_kernel<METHOD>;
     e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_DKV, s);
+    prof_count(CAPATTN_KERNEL_DKV, 1);
     kdkv<<<dim3(p.Hkv * p.B, p.nk), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, mdo, p);
+    prof_end(CAPATTN_KERNEL_DKV, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kdq = dq_tc_kernel<METHOD>;
     e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_DQ, s);
+    prof_count(CAPATTN_KERNEL_DQ, 1);
     kdq<<<dim3(p.Hq * p.B, p.nq), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, mdo, p);
+    prof_end(CAPATTN_KERNEL_DQ, s);
     return cudaGetLastError();
   }
 };

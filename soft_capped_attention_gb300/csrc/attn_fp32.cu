@@ -322,7 +322,10 @@ struct FwdLaunch {
     auto kern = fwd_fp32_kernel<D, METHOD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fwd_smem<D>());
     if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_FWD, s);
+    prof_count(CAPATTN_KERNEL_FWD, 1);
     kern<<<dim3(p.nq, p.Hq, p.B), NT, fwd_smem<D>(), s>>>(p);
+    prof_end(CAPATTN_KERNEL_FWD, s);
     return cudaGetLastError();
   }
   static cudaError_t run(const Params& p, cudaStream_t s) { return p.D == 64 ? go<64>(p, s) : go<128>(p, s); }
@@ -335,13 +338,19 @@ struct BwdLaunch {
     auto kdkv = dkv_fp32_kernel<D, METHOD>;
     cudaError_t e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkv_smem<D>());
     if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_DKV, s);
+    prof_count(CAPATTN_KERNEL_DKV, 1);
     kdkv<<<dim3(p.nk, p.Hkv, p.B), NT, dkv_smem<D>(), s>>>(p);
+    prof_end(CAPATTN_KERNEL_DKV, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kdq = dq_fp32_kernel<D, METHOD>;
     e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dq_smem<D>());
     if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_DQ, s);
+    prof_count(CAPATTN_KERNEL_DQ, 1);
     kdq<<<dim3(p.nq, p.Hq, p.B), NT, dq_smem<D>(), s>>>(p);
+    prof_end(CAPATTN_KERNEL_DQ, s);
     return cudaGetLastError();
   }
   static cudaError_t run(const Params& p, cudaStream_t s) { return p.D == 64 ? go<64>(p, s) : go<128>(p, s); }

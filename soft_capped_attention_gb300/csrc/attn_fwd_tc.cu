@@ -322,7 +322,10 @@ struct FwdTcLaunch {
     auto kern = fwd_tc_kernel<METHOD>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_FWD, s);
+    prof_count(CAPATTN_KERNEL_FWD, 1);
     kern<<<dim3(p.Hq * p.B, p.nq), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+    prof_end(CAPATTN_KERNEL_FWD, s);
     return cudaGetLastError();
   }
 };

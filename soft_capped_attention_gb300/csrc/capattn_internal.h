@@ -62,6 +62,12 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(const capattn_config& c, int block_q, int block_kv);
 
+// Optional per-kernel event timing around launches (no-ops unless enabled);
+// prof_count adds the number of kernels a launcher issued.
+void prof_begin(int kind, cudaStream_t stream);
+void prof_end(int kind, cudaStream_t stream);
+void prof_count(int kind, int n);
+
 // Launchers.  Each returns cudaGetLastError() after the launch.
 cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s);
 cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s);

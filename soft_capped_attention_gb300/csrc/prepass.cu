@@ -101,6 +101,8 @@ __global__ void kmap_kernel(Params p) {
 }
 
 cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
+  prof_begin(CAPATTN_KERNEL_PREPASS, s);
+  prof_count(CAPATTN_KERNEL_PREPASS, build_kmap ? 3 : 2);
   dim3 g1((p.L + 255) / 256, p.B);
   rowinfo_kernel<<<g1, 256, 0, s>>>(p);
   dim3 g2(p.nq, p.B);
@@ -109,6 +111,7 @@ cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
     dim3 g3(p.nk, p.B);
     kmap_kernel<<<g3, 32, 0, s>>>(p);
   }
+  prof_end(CAPATTN_KERNEL_PREPASS, s);
   return cudaGetLastError();
 }
 
@@ -156,6 +159,8 @@ cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
   const long long nrows = (long long)p.B * p.L * p.Hq;
   const int warps = 8;
   const unsigned grid = (unsigned)((nrows + warps - 1) / warps);
+  prof_begin(CAPATTN_KERNEL_DELTA, s);
+  prof_count(CAPATTN_KERNEL_DELTA, 1);
   if (bf16) {
     delta_kernel<__nv_bfloat16, 128><<<grid, warps * 32, 0, s>>>(p);
   } else if (p.D == 64) {
@@ -163,6 +168,7 @@ cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
   } else {
     delta_kernel<float, 128><<<grid, warps * 32, 0, s>>>(p);
   }
+  prof_end(CAPATTN_KERNEL_DELTA, s);
   return cudaGetLastError();
 }
 
