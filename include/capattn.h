@@ -68,7 +68,8 @@ typedef enum capattn_status {
   CAPATTN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
   CAPATTN_ERR_DEVICE_TIMEOUT = 4,/* a kernel gave up on a bounded wait (device status) */
   CAPATTN_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than capattn_workspace_bytes */
-  CAPATTN_ERR_DEVICE_DATA = 6    /* device status: bad segment ids or ranker bounds */
+  CAPATTN_ERR_DEVICE_DATA = 6,   /* device status: bad segment ids or ranker bounds */
+  CAPATTN_ERR_TOO_LARGE = 7      /* problem needs more scratch than capattn_fwd_noalloc holds */
 } capattn_status;
 
 /* Cap methods (mosaic_backward.py _apply_cap_mosaic).  A cap <= 0 behaves as none. */
@@ -188,6 +189,30 @@ capattn_status capattn_visit_map_device(const capattn_config* cfg, const int32_t
 capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* seg,
                                       const int32_t* bounds, int32_t b, uint64_t* bits,
                                       size_t n_words);
+
+/*
+ * Forward without any allocation or workspace argument (the pages have no
+ * counterpart; this is an addition for callers that cannot allocate, such as
+ * plugins inside a framework that owns all device memory and gives them no
+ * scratch, or services held to a fixed memory budget).  Same inputs, outputs
+ * and results as capattn_fwd, but the scratch lives in a fixed 8 MiB device
+ * array inside the library (held by every GPU that loads it until exit).
+ *  - Returns CAPATTN_ERR_TOO_LARGE, before launching anything, when
+ *    capattn_workspace_bytes(cfg, CAPATTN_PASS_FWD) exceeds 8 MiB (roughly
+ *    B * L above 500,000).
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array: calls that may overlap on the
+ *    GPU (different streams, or concurrent host threads) race on it and must be
+ *    serialised by the caller.  Device-side status bits are not reported; use
+ *    capattn_fwd with a workspace to read them.
+ */
+capattn_status capattn_fwd_noalloc(const capattn_config* cfg, const void* q, const void* k,
+                                   const void* v, const float* temp, const int32_t* seg,
+                                   const int32_t* bounds, void* o, float* lse, float* m, float* l,
+                                   cudaStream_t stream);
 
 /*
  * Per-kernel timing.  While enabled, every kernel the library launches is

@@ -27,7 +27,8 @@ PASS_FWD, PASS_BWD = 0, 1
 VISIT_Q_TILES, VISIT_KV_TILES = 0, 1
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
                 4: "device wait timeout", 5: "workspace missing, misaligned or too small",
-                6: "invalid device data (segment ids or ranker bounds)"}
+                6: "invalid device data (segment ids or ranker bounds)",
+                7: "problem exceeds the fixed scratch of capattn_fwd_noalloc"}
 
 
 class CapattnError(RuntimeError):
@@ -94,7 +95,8 @@ def lib() -> ctypes.CDLL:
 EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn_workspace_bytes",
                     "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_device_status",
                     "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host",
-                    "capattn_profile_enable", "capattn_profile_read", "capattn_kernel_name")
+                    "capattn_profile_enable", "capattn_profile_read", "capattn_kernel_name",
+                    "capattn_fwd_noalloc")
 KERNEL_KINDS = ("prepass", "fwd", "delta", "dkv", "dq")
 
 

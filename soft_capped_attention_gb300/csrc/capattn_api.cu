@@ -142,6 +142,7 @@ const char* capattn_status_string(capattn_status s) {
     case CAPATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
     case CAPATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case CAPATTN_ERR_DEVICE_DATA: return "invalid device data (segment ids or ranker bounds)";
+    case CAPATTN_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of capattn_fwd_noalloc";
   }
   return "unknown status";
 }
