@@ -12,22 +12,26 @@
 // tiles of the tile's visit map, accumulating dK and dV in TMEM (the group sum
 // happens in place, no reduction pass).  Per step:
 //   S^T  = K Q^T, dP^T = V dO^T            (SS MMAs, M = keys, N = queries)
-//   elementwise, in two halves of 64 query columns: P^T and dX^T written back
-//   into TMEM as packed bf16 over the consumed columns
-//   dV += P^T dO, dK += dX^T Q             (TS MMAs, K = 64 per half)
-// so the tensor pipe runs the first half's dV / dK while the second half is
-// computed.  TMEM: S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
+//   elementwise by two warpgroups, each owning 64 query columns in two chunks
+//   of 32; each chunk's P^T and dX^T go back into TMEM as packed bf16 over
+//   already-consumed columns of the warpgroup's own S^T / dP^T region, and the
+//   chunk is handed to the MMA issuer at once:
+//   dV += P^T dO, dK += dX^T Q             (TS MMAs, K = 32 per chunk)
+// so the tensor pipe works on the first chunks while later ones are computed.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
 //
-// dQ: one CTA per (batch, query head, 128-query tile), looping over the KV tiles
-// of its visit map.  S = Q K^T, dP = dO V^T, then dQ += dX K in two halves.
-// TMEM: S [0,128), dP [128,256), dQ [256,384).
+// dQ: one CTA per (batch, query head, 128-query tile), looping over the KV
+// tiles of its visit map: S = Q K^T, dP = dO V^T, then dQ += dX K chunk by
+// chunk.  TMEM: S [0,128), dP [128,256), dQ [256,384).
 //
-// Warp roles in both kernels: warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 2..5 elementwise (one TMEM lane = one tile row each).
+// Warp roles in both kernels (10 warps): warp 0 TMA producer, warp 1 TMEM
+// allocator and MMA issuer, warps 2..5 and 6..9 the two elementwise
+// warpgroups (one TMEM lane = one tile row each).
 #include <math.h>
 
 #include "cap_math.cuh"
 #include "capattn_internal.h"
+#include "softmax_elem.cuh"
 #include "tc_common.cuh"
 #include "tma_maps.h"
 
@@ -40,14 +44,13 @@ constexpr int BT = 128;                       // tile rows (queries and keys)
 constexpr int SLAB = 128 * 64 * 2;
 constexpr int TILE = 2 * SLAB;
 constexpr int NSTAGE = 2;
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;
 constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32], float scale) {
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
   uint32_t pk[16];
 #pragma unroll
-  for (int e = 0; e < 16; ++e)
-    pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * scale, __uint_as_float(v[2 * e + 1]) * scale);
+  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -59,6 +62,24 @@ __device__ __forceinline__ void store_zero_bf16(__nv_bfloat16* dst) {
   for (int e = 0; e < 4; ++e) d4[e] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+__device__ __forceinline__ void issue_ss128(uint32_t d, uint32_t sA, uint32_t sB) {
+  constexpr uint32_t idesc = idesc_bf16(BT, BT, 0, 0);
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
+    mma_ss(d, smem_desc(sA + off, 16, 1024), smem_desc(sB + off, 16, 1024), idesc, ks > 0);
+  }
+}
+
+// D += A[tmem cols a0 .. a0 + 16) x B rows [r0, r0 + 32) (MN-major B, N = 128): one chunk.
+__device__ __forceinline__ void issue_chunk(uint32_t d, uint32_t a0, uint32_t sB, int r0, bool first) {
+  constexpr uint32_t idesc = idesc_bf16(BT, HD, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk)
+    mma_ts(d, a0 + kk * 8, smem_desc(sB + (r0 + 16 * kk) * 128, SLAB, 1024), idesc,
+           (first && kk == 0) ? 0u : 1u);
+}
+
 // ======================================================================= dK / dV
 template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -66,10 +87,10 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
               const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[16];
+  __shared__ __align__(8) uint64_t bars[24];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ __align__(16) float4 colc[2][BT];  // per query column: lse2, rowadd, c1, tl
+  __shared__ __align__(16) float4 colc[2][BT];  // per query column: mul, add - lse2, dscale, radd
   __shared__ __align__(16) int4 coli[2][BT];    // per query column: live span (lo, hi, e)
 
   const int gb = blockIdx.x;
@@ -86,10 +107,10 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const uint32_t bar_full = smem_u32(&bars[1]);    // + s*8 (Q and dO)
   const uint32_t bar_empty = smem_u32(&bars[3]);   // + s*8
   const uint32_t bar_sdp = smem_u32(&bars[5]);
-  const uint32_t bar_ew = smem_u32(&bars[6]);      // + half*8
-  const uint32_t bar_final = smem_u32(&bars[8]);
-  const uint32_t bar_cfull = smem_u32(&bars[9]);   // + cb*8: column constants written
-  const uint32_t bar_cfree = smem_u32(&bars[11]);  // + cb*8: column constants consumed
+  const uint32_t bar_ew = smem_u32(&bars[6]);      // + (2*wg + chunk)*8
+  const uint32_t bar_final = smem_u32(&bars[10]);
+  const uint32_t bar_cfull = smem_u32(&bars[11]);  // + (2*wg + cb)*8: column constants written
+  const uint32_t bar_cfree = smem_u32(&bars[15]);  // + (2*wg + cb)*8: column constants consumed
 
   const uint32_t* map = p.kmap + ((size_t)b * p.nk + kt) * p.wq;
   if (threadIdx.x == 0) {
@@ -100,13 +121,12 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_sdp, 1);
-    mbar_init(bar_ew, 4);
-    mbar_init(bar_ew + 8, 4);
-    mbar_init(bar_final, 1);
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < 4; ++c) {
+      mbar_init(bar_ew + 8 * c, 4);
       mbar_init(bar_cfull + 8 * c, 128);
       mbar_init(bar_cfree + 8 * c, 128);
     }
+    mbar_init(bar_final, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -152,41 +172,28 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(BT, BT, 0, 0);
-      constexpr uint32_t idesc_g = idesc_bf16(BT, HD, 0, 1);
       bool ok = mbar_wait(bar_kv, 0, p.status, &abort_flag);
       for (int j = 0; ok && j < n; ++j) {
         const int s = j % NSTAGE, u = j / NSTAGE;
         if (!mbar_wait(bar_full + 8 * s, u & 1, p.status, &abort_flag)) break;
         tc_fence_after();
         const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-          mma_ss(tmem, smem_desc(sK + off, 16, 1024), smem_desc(sQ + off, 16, 1024), idesc_s, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-          mma_ss(tmem + 128u, smem_desc(sV + off, 16, 1024), smem_desc(sO + off, 16, 1024), idesc_s,
-                 ks > 0);
-        }
+        issue_ss128(tmem, sK, sQ);          // S^T  = K Q^T
+        issue_ss128(tmem + 128u, sV, sO);   // dP^T = V dO^T
         mma_commit(bar_sdp);
-        for (int half = 0; half < 2; ++half) {
-          if (!mbar_wait(bar_ew + 8 * half, j & 1, p.status, &abort_flag)) {
+        // chunk order: (wg0, c0), (wg1, c0), (wg0, c1), (wg1, c1)
+        for (int q = 0; q < 4 && ok; ++q) {
+          const int wg = q & 1, c = q >> 1;
+          if (!mbar_wait(bar_ew + 8 * (2 * wg + c), j & 1, p.status, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int ks = half * 4 + kk;
-            const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-            mma_ts(tmem + 256u, tmem + (uint32_t)(ks * 8), smem_desc(sO + ks * 2048, SLAB, 1024),
-                   idesc_g, acc);
-            mma_ts(tmem + 384u, tmem + 128u + (uint32_t)(ks * 8),
-                   smem_desc(sQ + ks * 2048, SLAB, 1024), idesc_g, acc);
-          }
+          const uint32_t col = (uint32_t)(64 * wg + 16 * c);
+          const int r0 = 64 * wg + 32 * c;
+          const bool first = (j == 0) && (q == 0);
+          issue_chunk(tmem + 256u, tmem + col, sO, r0, first);          // dV += P^T dO
+          issue_chunk(tmem + 384u, tmem + 128u + col, sQ, r0, first);   // dK += dX^T Q
         }
         if (!ok) break;
         mma_commit(bar_empty + 8 * s);
@@ -195,10 +202,13 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       drain_wait(bar_final, 0);
     }
   } else {
+    const int wg = (warp - 2) >> 2;        // query columns [64 wg, 64 wg + 64)
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // key row within the tile (TMEM lane)
+    const int r = quarter * 32 + lane;     // key row within the tile (TMEM lane)
+    const int tid = (warp - 2 - 4 * wg) * 32 + lane;  // 0..127 within the warpgroup
     const int jrow = k0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
     const float zw = p.z_loss_weight;
     bool aborted = false;
     int step = 0;
@@ -208,73 +218,76 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       int qt;
       while (it.next(qt)) {
         const int q0 = qt * BT;
-        const int cb = step & 1;
-        const int cu = step >> 1;
-        {  // column constants of this query tile (thread r loads query row q0 + r)
-          if (step >= 2 && !mbar_wait(bar_cfree + 8 * cb, (cu - 1) & 1, p.status, &abort_flag)) {
-            aborted = true;
-            break;
-          }
-          const int i = q0 + r;
+        const int cb = step & 1, cu = step >> 1;
+        const uint32_t my_cfull = bar_cfull + 8 * (2 * wg + cb);
+        const uint32_t my_cfree = bar_cfree + 8 * (2 * wg + cb);
+        if (step >= 2 && !mbar_wait(my_cfree, (cu - 1) & 1, p.status, &abort_flag)) {
+          aborted = true;
+          break;
+        }
+        if (tid < 64) {  // constants of query column 64 wg + tid
+          const int c = 64 * wg + tid;
+          const int i = q0 + c;
           const bool valid = i < p.L;
           const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
           const float lse = valid ? p.lse[rr] : -INFINITY;
           const float dl = valid ? p.delta[rr] : 0.f;
           const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
           const bool fin = isfinite(lse);
-          colc[cb][r] = make_float4(fin ? lse * kLog2e : 0.f, -dl + (fin ? zw * lse : 0.f),
-                                    p.sm_scale * temp, temp * kLog2e);
-          coli[cb][r] = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
-          mbar_arrive(bar_cfull + 8 * cb);
-          // Every pair of the tile is live when kt lies in the query tile's full range.
-          const int2 fr = p.qfull[(size_t)b * p.nq + qt];
-          const bool tile_full = (kt >= fr.x) && (kt < fr.y);
-          if (!mbar_wait(bar_cfull + 8 * cb, cu & 1, p.status, &abort_flag) ||
-              !mbar_wait(bar_sdp, step & 1, p.status, &abort_flag)) {
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t sv[64], dp[64];
-            tmem_ld32(lane_base + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(lane_base + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-            tmem_ld32(lane_base + 128u + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-            tmem_ld32(lane_base + 128u + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-            tmem_wait_ld();
-            uint32_t pp[32], px[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float pv[2], xv[2];
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                const int c = half * 64 + 2 * e + u;
-                const float4 cc = colc[cb][c];
-                float dc;
-                const float cv = cap_value_grad<METHOD>(__uint_as_float(sv[2 * e + u]) * p.sm_scale,
-                                                        p.cap, &dc);
-                bool lv = true;
-                if (!tile_full) {
-                  const int4 ci = coli[cb][c];
-                  lv = (jrow >= ci.x && jrow < ci.y) || jrow == ci.z;
-                }
-                const float P = lv ? ex2_approx(fmaf(cv, cc.w, -cc.x)) : 0.f;
-                pv[u] = P;
-                xv[u] = cc.z * dc * P * (__uint_as_float(dp[2 * e + u]) + cc.y);
-              }
-              pp[e] = pack_bf16x2(pv[0], pv[1]);
-              px[e] = pack_bf16x2(xv[0], xv[1]);
-            }
-            tmem_st32(lane_base + half * 32, pp);
-            tmem_st32(lane_base + 128u + half * 32, px);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_ew + 8 * half);
-          }
-          mbar_arrive(bar_cfree + 8 * cb);
+          float mul, add;
+          row_consts<METHOD>(p.cap, p.sm_scale, temp, &mul, &add);
+          colc[cb][c] = make_float4(mul, add - (fin ? lse * kL2E : 0.f),
+                                    row_dscale<METHOD>(p.cap, p.sm_scale, temp),
+                                    -dl + (fin ? zw * lse : 0.f));
+          coli[cb][c] = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
         }
+        mbar_arrive(my_cfull);
+        const int2 fr = p.qfull[(size_t)b * p.nq + qt];
+        const bool tile_full = (kt >= fr.x) && (kt < fr.y);
+        if (!mbar_wait(my_cfull, cu & 1, p.status, &abort_flag) ||
+            !mbar_wait(bar_sdp, step & 1, p.status, &abort_flag)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * wg + 32 * c;  // first query column of the chunk
+          uint32_t sv[32], dp[32];
+          tmem_ld32(lane_base + col0, sv);
+          tmem_ld32(lane_base + 128u + col0, dp);
+          tmem_wait_ld();
+          uint32_t pp[16], px[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float pv[2], xv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int cc = col0 + 2 * e + u;
+              const float4 k4 = colc[cb][cc];
+              float d;
+              const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
+              bool lv = true;
+              if (!tile_full) {
+                const int4 ci = coli[cb][cc];
+                lv = (jrow >= ci.x && jrow < ci.y) || jrow == ci.z;
+              }
+              const float P = lv ? ex2_approx(fmaf(k4.x, f, k4.y)) : 0.f;
+              pv[u] = P;
+              xv[u] = (k4.z * d) * (P * (__uint_as_float(dp[2 * e + u]) + k4.w));
+            }
+            pp[e] = pack_bf16x2(pv[0], pv[1]);
+            px[e] = pack_bf16x2(xv[0], xv[1]);
+          }
+          const uint32_t dst = (uint32_t)(64 * wg + 16 * c);
+          tmem_st16(lane_base + dst, pp);
+          tmem_st16(lane_base + 128u + dst, px);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + c));
+        }
+        mbar_arrive(my_cfree);
         ++step;
       }
     }
@@ -284,24 +297,19 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       have = mbar_wait(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
-    if (have || n == 0 || aborted) {
-      __nv_bfloat16* dvg = static_cast<__nv_bfloat16*>(p.dv) + ((size_t)(b * p.L + jrow) * p.Hkv + g) * HD;
-      __nv_bfloat16* dkg = static_cast<__nv_bfloat16*>(p.dk) + ((size_t)(b * p.L + jrow) * p.Hkv + g) * HD;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (have) {
-          uint32_t v[32], k[32];
-          tmem_ld32(lane_base + 256u + c * 32, v);
-          tmem_ld32(lane_base + 384u + c * 32, k);
-          tmem_wait_ld();
-          if (jrow < p.L) {
-            store_row_bf16(dvg + c * 32, v, 1.f);
-            store_row_bf16(dkg + c * 32, k, 1.f);
-          }
-        } else if (jrow < p.L) {
-          store_zero_bf16(dvg + c * 32);
-          store_zero_bf16(dkg + c * 32);
-        }
+    // warpgroup 0 writes dV, warpgroup 1 writes dK
+    void* outp = wg == 0 ? p.dv : p.dk;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(outp) + ((size_t)(b * p.L + jrow) * p.Hkv + g) * HD;
+    const uint32_t acc = lane_base + (wg == 0 ? 256u : 384u);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      if (have) {
+        uint32_t v[32];
+        tmem_ld32(acc + c * 32, v);
+        tmem_wait_ld();
+        if (jrow < p.L) store_row_bf16(dst + c * 32, v);
+      } else if (jrow < p.L) {
+        store_zero_bf16(dst + c * 32);
       }
     }
   }
@@ -339,8 +347,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   const uint32_t bar_full = smem_u32(&bars[1]);    // + s*8
   const uint32_t bar_empty = smem_u32(&bars[3]);   // + s*8
   const uint32_t bar_sdp = smem_u32(&bars[5]);
-  const uint32_t bar_ew = smem_u32(&bars[6]);      // + half*8
-  const uint32_t bar_final = smem_u32(&bars[8]);
+  const uint32_t bar_ew = smem_u32(&bars[6]);      // + (2*wg + chunk)*8
+  const uint32_t bar_final = smem_u32(&bars[10]);
 
   const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
   if (threadIdx.x == 0) {
@@ -351,8 +359,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_sdp, 1);
-    mbar_init(bar_ew, 4);
-    mbar_init(bar_ew + 8, 4);
+    for (int c = 0; c < 4; ++c) mbar_init(bar_ew + 8 * c, 4);
     mbar_init(bar_final, 1);
     fence_mbar_init();
   }
@@ -394,38 +401,24 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(BT, BT, 0, 0);
-      constexpr uint32_t idesc_g = idesc_bf16(BT, HD, 0, 1);
       bool ok = mbar_wait(bar_q, 0, p.status, &abort_flag);
       for (int j = 0; ok && j < n; ++j) {
         const int s = j % NSTAGE, u = j / NSTAGE;
         if (!mbar_wait(bar_full + 8 * s, u & 1, p.status, &abort_flag)) break;
         tc_fence_after();
         const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-          mma_ss(tmem, smem_desc(sQ + off, 16, 1024), smem_desc(sK + off, 16, 1024), idesc_s, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-          mma_ss(tmem + 128u, smem_desc(sO + off, 16, 1024), smem_desc(sV + off, 16, 1024), idesc_s,
-                 ks > 0);
-        }
+        issue_ss128(tmem, sQ, sK);          // S  = Q K^T
+        issue_ss128(tmem + 128u, sO, sV);   // dP = dO V^T
         mma_commit(bar_sdp);
-        for (int half = 0; half < 2; ++half) {
-          if (!mbar_wait(bar_ew + 8 * half, j & 1, p.status, &abort_flag)) {
+        for (int q = 0; q < 4 && ok; ++q) {
+          const int wg = q & 1, c = q >> 1;
+          if (!mbar_wait(bar_ew + 8 * (2 * wg + c), j & 1, p.status, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int ks = half * 4 + kk;
-            mma_ts(tmem + 256u, tmem + (uint32_t)(ks * 8), smem_desc(sK + ks * 2048, SLAB, 1024),
-                   idesc_g, (j > 0 || ks > 0) ? 1u : 0u);
-          }
+          const uint32_t col = (uint32_t)(64 * wg + 16 * c);
+          issue_chunk(tmem + 256u, tmem + col, sK, 64 * wg + 32 * c, (j == 0) && (q == 0));
         }
         if (!ok) break;
         mma_commit(bar_empty + 8 * s);
@@ -434,6 +427,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       drain_wait(bar_final, 0);
     }
   } else {
+    const int wg = (warp - 2) >> 2;        // key columns [64 wg, 64 wg + 64)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int i = q0 + r;
@@ -445,10 +439,12 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const float lse = valid ? p.lse[rr] : -INFINITY;
     const float dl = valid ? p.delta[rr] : 0.f;
     const bool fin = isfinite(lse);
-    const float lse2 = fin ? lse * kLog2e : 0.f;
-    const float rowadd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
-    const float c1 = p.sm_scale * temp;
-    const float tl = temp * kLog2e;
+    const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
+    float mul, add;
+    row_consts<METHOD>(p.cap, p.sm_scale, temp, &mul, &add);
+    const float addl = add - (fin ? lse * kL2E : 0.f);
+    const float dscale = row_dscale<METHOD>(p.cap, p.sm_scale, temp);
+    const float radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
     bool aborted = false;
     TileIter it(map, p.wk);
     for (int j = 0; j < n; ++j) {
@@ -462,34 +458,32 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[64], dp[64];
-        tmem_ld32(lane_base + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(lane_base + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld32(lane_base + 128u + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-        tmem_ld32(lane_base + 128u + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = 64 * wg + 32 * c;
+        uint32_t sv[32], dp[32];
+        tmem_ld32(lane_base + col0, sv);
+        tmem_ld32(lane_base + 128u + col0, dp);
         tmem_wait_ld();
-        uint32_t px[32];
+        uint32_t px[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 16; ++e) {
           float xv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int c = half * 64 + 2 * e + u;
-            float dc;
-            const float cv = cap_value_grad<METHOD>(__uint_as_float(sv[2 * e + u]) * p.sm_scale, p.cap, &dc);
-            const int jj = k0 + c;
+            float d;
+            const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
+            const int jj = k0 + col0 + 2 * e + u;
             const bool lv = full || (jj >= ri.x && jj < ri.y) || jj == ri.z;
-            const float P = lv ? ex2_approx(fmaf(cv, tl, -lse2)) : 0.f;
-            xv[u] = c1 * dc * P * (__uint_as_float(dp[2 * e + u]) + rowadd);
+            const float P = lv ? ex2_approx(fmaf(mul, f, addl)) : 0.f;
+            xv[u] = (dscale * d) * (P * (__uint_as_float(dp[2 * e + u]) + radd));
           }
           px[e] = pack_bf16x2(xv[0], xv[1]);
         }
-        tmem_st32(lane_base + half * 32, px);
+        tmem_st16(lane_base + (uint32_t)(64 * wg + 16 * c), px);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_ew + 8 * half);
+        if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + c));
       }
     }
     bool have = false;
@@ -497,16 +491,18 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       have = mbar_wait(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
+    // warpgroup wg writes dQ columns [64 wg, 64 wg + 64)
     __nv_bfloat16* dqg = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)(b * p.L + i) * p.Hq + h) * HD;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      const int col = 64 * wg + 32 * c;
       if (have) {
         uint32_t v[32];
-        tmem_ld32(lane_base + 256u + c * 32, v);
+        tmem_ld32(lane_base + 256u + col, v);
         tmem_wait_ld();
-        if (valid) store_row_bf16(dqg + c * 32, v, 1.f);
+        if (valid) store_row_bf16(dqg + col, v);
       } else if (valid) {
-        store_zero_bf16(dqg + c * 32);
+        store_zero_bf16(dqg + col);
       }
     }
   }

@@ -6,26 +6,30 @@
 // ranker_mask_mosaic_kv_q (transposed) and an exp2-domain softmax as in the
 // Mosaic kernels.
 //
-// One CTA owns 128 query rows of one (batch, head) and walks the KV tiles of
-// its visit map.  Warp roles:
-//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages;
-//   warp 1      TMEM allocator and MMA issuer (one thread):
-//                 S_j = Q K_j^T      (SS MMA, M=N=128, into a double-buffered
-//                                     128-column TMEM region, so S_{j+1} runs
-//                                     on the tensor pipe while the softmax
-//                                     works on S_j)
-//                 O  += P_j V_j      (TS MMA: P_j read from TMEM as bf16)
-//   warps 2..5  softmax: one thread per query row (TMEM lane).  Loads S_j,
-//               applies sm_scale, cap, temperature and the row's live span,
-//               keeps a running max in the log2 domain, writes P_j = 2^(x - m)
-//               as packed bf16 back over the first 64 columns of S_j, and
-//               rescales O in TMEM when the max grows by more than 2^8
-//               (otherwise the stale max is kept; P stays <= 256).
-// TMEM: S0 [0,128), S1 [128,256), O [256,384) -> 512 columns allocated.
+// One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and walks
+// the union of their KV visit maps.  Warp roles (10 warps):
+//   warp 0      TMA producer: Q0, Q1 once, then K_j / V_j into a 2-stage ring;
+//   warp 1      TMEM allocator and MMA issuer (one thread), ping-ponging the
+//               two tiles so that one tile's softmax overlaps the other tile's
+//               MMAs:  S0_j S1_j | PV0_j S0_{j+1} | PV1_j S1_{j+1} | ...
+//                 S_t = Q_t K_j^T  (SS MMA, M = N = 128)
+//                 O_t += P_t V_j   (TS MMA: P_t read from TMEM as bf16)
+//   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1: one thread
+//               per query row (its TMEM lane).  Pass 1 takes the row maximum of
+//               the raw scores (every cap is increasing, so the logit maximum is
+//               the transformed raw maximum); pass 2 applies sm_scale, cap,
+//               temperature and the row's live span, writes P = 2^(x - m) as
+//               packed bf16 over the first 64 columns of S, and accumulates l.
+//               The running max is only moved (and O rescaled in TMEM) when it
+//               grows by more than 2^8; otherwise P stays <= 256.
+// A tile's S_{j+1} is issued after its PV_j, so when the softmax sees S_{j+1}
+// complete, PV_j is complete too and O may be rescaled in place.
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
 #include <math.h>
 
 #include "cap_math.cuh"
 #include "capattn_internal.h"
+#include "softmax_elem.cuh"
 #include "tc_common.cuh"
 #include "tma_maps.h"
 
@@ -39,10 +43,60 @@ constexpr int HD = 128;
 constexpr int NSTAGE = 2;
 constexpr int SLAB = 128 * 64 * 2;          // one [128][64] bf16 box
 constexpr int TILE = 2 * SLAB;               // 128 x 128 bf16
-constexpr int SMEM_DATA = TILE + NSTAGE * 2 * TILE;
-constexpr int SMEM_BYTES = SMEM_DATA + 1024;  // + alignment slack
-constexpr int NTHREADS = 192;
-constexpr float kRescaleThreshold = 8.0f;     // log2 units
+constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
+constexpr int NTHREADS = 320;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+
+// Iterates the union of two rows of a visit bitmap, reporting per tile which
+// of the two query tiles is live in it.
+struct PairIter {
+  const uint32_t* m0;
+  const uint32_t* m1;  // null when the second tile does not exist
+  int nwords, w;
+  uint32_t b0, b1;
+  __device__ PairIter(const uint32_t* a, const uint32_t* c, int n) : m0(a), m1(c), nwords(n), w(0) {
+    b0 = n > 0 ? a[0] : 0u;
+    b1 = (n > 0 && c) ? c[0] : 0u;
+  }
+  __device__ bool next(int& t, bool& a0, bool& a1) {
+    while ((b0 | b1) == 0u) {
+      if (++w >= nwords) return false;
+      b0 = m0[w];
+      b1 = m1 ? m1[w] : 0u;
+    }
+    const uint32_t u = b0 | b1;
+    const int bit = __ffs(u) - 1;
+    const uint32_t mask = 1u << bit;
+    a0 = (b0 & mask) != 0u;
+    a1 = (b1 & mask) != 0u;
+    b0 &= ~mask;
+    b1 &= ~mask;
+    t = w * 32 + bit;
+    return true;
+  }
+};
+
+__device__ __forceinline__ int count_union(const uint32_t* a, const uint32_t* c, int n) {
+  int s = 0;
+  for (int w = 0; w < n; ++w) s += __popc(a[w] | (c ? c[w] : 0u));
+  return s;
+}
+
+__device__ __forceinline__ void issue_s(uint32_t d, uint32_t sQ, uint32_t sK) {
+  constexpr uint32_t idesc = idesc_bf16(BM, BN, 0, 0);
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
+    mma_ss(d, smem_desc(sQ + off, 16, 1024), smem_desc(sK + off, 16, 1024), idesc, ks > 0);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pt, uint32_t sV, uint32_t acc0) {
+  constexpr uint32_t idesc = idesc_bf16(BM, HD, 0, 1);
+#pragma unroll
+  for (int ks = 0; ks < BN / 16; ++ks)
+    mma_ts(d, pt + ks * 8, smem_desc(sV + ks * 2048, SLAB, 1024), idesc, (acc0 || ks > 0) ? 1u : 0u);
+}
 
 template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -55,25 +109,27 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 
   const int hb = blockIdx.x;
   const int h = hb % p.Hq, b = hb / p.Hq;
-  const int qt = p.nq - 1 - (int)blockIdx.y;  // heaviest (latest) query tiles first
+  const int npair = (p.nq + 1) >> 1;
+  const int pr = npair - 1 - (int)blockIdx.y;  // heaviest (latest) query tiles first
+  const int qt0 = 2 * pr;
+  const bool has1 = qt0 + 1 < p.nq;
   const int g = h / p.G;
-  const int q0 = qt * BM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = base;
-  const uint32_t sKV = base + TILE;  // stage s: K at sKV + s*2*TILE, V at + TILE
+  const uint32_t sQ0 = base, sQ1 = base + TILE;
+  const uint32_t sKV = base + 2 * TILE;  // stage s: K at sKV + s*2*TILE, V at + TILE
 
   const uint32_t bar_q = smem_u32(&bars[0]);
-  const uint32_t bar_kfull = smem_u32(&bars[1]);    // + s*8
-  const uint32_t bar_vfull = smem_u32(&bars[3]);    // + s*8
-  const uint32_t bar_empty = smem_u32(&bars[5]);    // + s*8
-  const uint32_t bar_sfull = smem_u32(&bars[7]);    // + buf*8
-  const uint32_t bar_pfull = smem_u32(&bars[9]);    // + buf*8
-  const uint32_t bar_odone = smem_u32(&bars[11]);
-  const uint32_t bar_final = smem_u32(&bars[12]);
+  const uint32_t bar_kfull = smem_u32(&bars[1]);   // + s*8
+  const uint32_t bar_vfull = smem_u32(&bars[3]);   // + s*8
+  const uint32_t bar_empty = smem_u32(&bars[5]);   // + s*8
+  const uint32_t bar_sfull = smem_u32(&bars[7]);   // + tile*8
+  const uint32_t bar_pfull = smem_u32(&bars[9]);   // + tile*8
+  const uint32_t bar_final = smem_u32(&bars[11]);
 
-  const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
+  const uint32_t* map0 = p.qmap + ((size_t)b * p.nq + qt0) * p.wk;
+  const uint32_t* map1 = has1 ? map0 + p.wk : nullptr;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -83,11 +139,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       mbar_init(bar_vfull + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_sfull + 8 * s, 1);
-      mbar_init(bar_pfull + 8 * s, 4);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_sfull + 8 * t, 1);
+      mbar_init(bar_pfull + 8 * t, 4);
     }
-    mbar_init(bar_odone, 1);
     mbar_init(bar_final, 1);
     fence_mbar_init();
   }
@@ -99,7 +154,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const int n = count_tiles(map, p.wk);
+  const int n = count_union(map0, map1, p.wk);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -107,12 +162,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
       tma_prefetch_desc(&mv);
-      mbar_expect_tx(bar_q, TILE);
-      tma_load_4d(sQ, &mq, bar_q, 0, h, q0, b);
-      tma_load_4d(sQ + SLAB, &mq, bar_q, 64, h, q0, b);
-      TileIter it(map, p.wk);
+      mbar_expect_tx(bar_q, 2 * TILE);
+      tma_load_4d(sQ0, &mq, bar_q, 0, h, qt0 * BM, b);
+      tma_load_4d(sQ0 + SLAB, &mq, bar_q, 64, h, qt0 * BM, b);
+      tma_load_4d(sQ1, &mq, bar_q, 0, h, qt0 * BM + BM, b);
+      tma_load_4d(sQ1 + SLAB, &mq, bar_q, 64, h, qt0 * BM + BM, b);
+      PairIter it(map0, map1, p.wk);
       int t, j = 0;
-      while (it.next(t)) {
+      bool a0, a1;
+      while (it.next(t, a0, a1)) {
         const int s = j % NSTAGE, u = j / NSTAGE;
         if (u > 0 && !mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
         const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
@@ -124,7 +182,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         tma_load_4d(sV + SLAB, &mv, bar_vfull + 8 * s, 64, g, t * BN, b);
         ++j;
       }
-      // Let every issued copy land before the CTA can exit.
       drain_wait(bar_q, 0);
       for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj) {
         drain_wait(bar_kfull + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
@@ -134,160 +191,198 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16(BM, HD, 0, 1);
       bool ok = mbar_wait(bar_q, 0, p.status, &abort_flag);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % NSTAGE, u = j / NSTAGE;
-        if (!mbar_wait(bar_kfull + 8 * s, u & 1, p.status, &abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sK = sKV + s * 2 * TILE;
-        const uint32_t d = tmem + (uint32_t)(j & 1) * 128u;
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-          mma_ss(d, smem_desc(sQ + off, 16, 1024), smem_desc(sK + off, 16, 1024), idesc_s, ks > 0);
-        }
-        mma_commit(bar_sfull + 8 * (j & 1));
-        return true;
-      };
+      tc_fence_after();
+      PairIter it(map0, map1, p.wk);
+      int t;
+      bool c0 = false, c1 = false;  // activity of the current tile
+      bool n0 = false, n1 = false;  // activity of the next tile
+      it.next(t, c0, c1);
+      int pc0 = 0, pc1 = 0;         // p_full phases consumed per query tile
+      uint32_t started0 = 0, started1 = 0;
+      if (ok) ok = mbar_wait(bar_kfull, 0, p.status, &abort_flag);
       if (ok) {
         tc_fence_after();
-        ok = issue_s(0);
+        if (c0) { issue_s(tmem, sQ0, sKV); mma_commit(bar_sfull); }
+        if (c1) { issue_s(tmem + 128u, sQ1, sKV); mma_commit(bar_sfull + 8); }
       }
       for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n && !issue_s(j + 1)) break;
-        if (!mbar_wait(bar_pfull + 8 * (j & 1), (j >> 1) & 1, p.status, &abort_flag)) break;
-        const int s = j % NSTAGE, u = j / NSTAGE;
-        if (!mbar_wait(bar_vfull + 8 * s, u & 1, p.status, &abort_flag)) break;
-        tc_fence_after();
+        const int s = j % NSTAGE;
         const uint32_t sV = sKV + s * 2 * TILE + TILE;
-        const uint32_t pt = tmem + (uint32_t)(j & 1) * 128u;
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ts(tmem + 256u, pt + ks * 8, smem_desc(sV + ks * 2048, SLAB, 1024), idesc_o,
-                 (j > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar_odone);
+        n0 = n1 = false;
+        const bool more = (j + 1 < n) && it.next(t, n0, n1);
+        const int s1 = (j + 1) % NSTAGE;
+        const uint32_t sKn = sKV + s1 * 2 * TILE;
+        if (!mbar_wait(bar_vfull + 8 * s, (j / NSTAGE) & 1, p.status, &abort_flag)) break;
+        if (c0) {
+          if (!mbar_wait(bar_pfull, pc0 & 1, p.status, &abort_flag)) break;
+          ++pc0;
+          tc_fence_after();
+          issue_pv(tmem + 256u, tmem, sV, started0);
+          started0 = 1;
+        }
+        if (more) {
+          if (!mbar_wait(bar_kfull + 8 * s1, ((j + 1) / NSTAGE) & 1, p.status, &abort_flag)) break;
+          tc_fence_after();
+          if (n0) { issue_s(tmem, sQ0, sKn); mma_commit(bar_sfull); }
+        }
+        if (c1) {
+          if (!mbar_wait(bar_pfull + 8, pc1 & 1, p.status, &abort_flag)) break;
+          ++pc1;
+          tc_fence_after();
+          issue_pv(tmem + 384u, tmem + 128u, sV, started1);
+          started1 = 1;
+        }
         mma_commit(bar_empty + 8 * s);
+        if (more && n1) { issue_s(tmem + 128u, sQ1, sKn); mma_commit(bar_sfull + 8); }
+        c0 = n0;
+        c1 = n1;
       }
-      // All issued MMAs complete before TMEM is released.
       mma_commit(bar_final);
       drain_wait(bar_final, 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
+    const int tsel = (warp - 2) >> 2;          // query tile 0 or 1
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const int i = q0 + r;
+    const int i = (qt0 + tsel) * BM + r;
     const bool valid = i < p.L;
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)tsel * 128u;
+    const uint32_t o_base = tmem + ((uint32_t)(quarter * 32) << 16) + 256u + (uint32_t)tsel * 128u;
+    const uint32_t my_sfull = bar_sfull + 8 * tsel, my_pfull = bar_pfull + 8 * tsel;
     const int4 ri = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
-    const float tl = ((p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f) * kLog2e;
-    const float sc = p.sm_scale;
+    const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
+    const bool neg = temp < 0.f;
+    const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
+    float rmul, radd;
+    row_consts<METHOD>(p.cap, p.sm_scale, temp, &rmul, &radd);
     float m_use = -INFINITY, m_true = -INFINITY, lsum = 0.f;
+    int cnt = 0;
     bool aborted = false;
-    TileIter it(map, p.wk);
-    for (int j = 0; j < n; ++j) {
-      int t;
-      it.next(t);
+    PairIter it(map0, map1, p.wk);
+    int t;
+    bool a0, a1;
+    while (it.next(t, a0, a1)) {
+      if (!(tsel == 0 ? a0 : a1)) continue;
       const int k0 = t * BN;
-      const uint32_t buf = (uint32_t)(j & 1);
-      if (!mbar_wait(bar_sfull + 8 * buf, (j >> 1) & 1, p.status, &abort_flag)) {
+      if (!mbar_wait(my_sfull, cnt & 1, p.status, &abort_flag)) {
         aborted = true;
         break;
       }
       tc_fence_after();
-      uint32_t x[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(lane_base + buf * 128u + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
-      tmem_wait_ld();
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BN);
-      float mx = -INFINITY;
-      if (full) {
+      // ---- pass 1: extreme raw score of the live entries
+      float ext = -INFINITY;  // max of (neg ? -X : X)
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(s_base + c * 32, v);
+        tmem_wait_ld();
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float v = cap_value<METHOD>(__uint_as_float(x[c]) * sc, p.cap) * tl;
-          x[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-      } else {
+          for (int e = 0; e < 32; e += 2) {
+            float a = __uint_as_float(v[e]), bb = __uint_as_float(v[e + 1]);
+            if (neg) { a = -a; bb = -bb; }
+            ext = fmaxf(ext, fmaxf(a, bb));
+          }
+        } else {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int jj = k0 + c;
-          const bool lv = (jj >= ri.x && jj < ri.y) || jj == ri.z;
-          const float v = lv ? cap_value<METHOD>(__uint_as_float(x[c]) * sc, p.cap) * tl : -INFINITY;
-          x[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int e = 0; e < 32; ++e) {
+            const int jj = k0 + c * 32 + e;
+            const bool lv = (jj >= ri.x && jj < ri.y) || jj == ri.z;
+            float a = __uint_as_float(v[e]);
+            if (neg) a = -a;
+            ext = fmaxf(ext, lv ? a : -INFINITY);
+          }
         }
       }
-      m_true = fmaxf(m_true, mx);
-      const float m_new = fmaxf(m_use, mx);
+      const float x_max =
+          (ext == -INFINITY) ? -INFINITY : fmaf(rmul, cap_f<METHOD>(neg ? -ext : ext, xf), radd);
+      m_true = fmaxf(m_true, x_max);
+      const float m_new = fmaxf(m_use, x_max);
       const bool resc = m_new > m_use + kRescaleThreshold;
       float alpha = 1.f;
       if (resc) {
         alpha = ex2_approx(m_use - m_new);
         m_use = m_new;
       }
-      float psum = 0.f;
-      const bool any = m_use != -INFINITY;
+      // ---- O rescale (PV of the previous live tile is complete)
+      if (cnt > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_base + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = any ? ex2_approx(__uint_as_float(x[c * 32 + 2 * e]) - m_use) : 0.f;
-          const float p1 = any ? ex2_approx(__uint_as_float(x[c * 32 + 2 * e + 1]) - m_use) : 0.f;
-          psum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(o_base + c * 32, o);
         }
-        tmem_st16(lane_base + buf * 128u + c * 16, pk);
       }
-      lsum = lsum * alpha + psum;
-      if (j > 0) {
-        if (!mbar_wait(bar_odone, (j - 1) & 1, p.status, &abort_flag)) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xFFFFFFFFu, resc)) {
+      // ---- pass 2: P = 2^(x - m_use), packed bf16 over S columns [0, 64)
+      const bool any = m_use != -INFINITY;
+      const float addm = radd - (any ? m_use : 0.f);
+      float psum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(s_base + c * 32, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+        if (full && any) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + 256u + c * 32, o);
-            tmem_wait_ld();
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(rmul, cap_f<METHOD>(__uint_as_float(v[2 * e]), xf), addm));
+            const float p1 = ex2_approx(fmaf(rmul, cap_f<METHOD>(__uint_as_float(v[2 * e + 1]), xf), addm));
+            psum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_base + 256u + c * 32, o);
+          for (int e = 0; e < 16; ++e) {
+            float pp[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int jj = k0 + c * 32 + 2 * e + u;
+              const bool lv = any && ((jj >= ri.x && jj < ri.y) || jj == ri.z);
+              pp[u] = lv ? ex2_approx(fmaf(rmul, cap_f<METHOD>(__uint_as_float(v[2 * e + u]), xf), addm))
+                         : 0.f;
+            }
+            psum += pp[0] + pp[1];
+            pk[e] = pack_bf16x2(pp[0], pp[1]);
           }
         }
+        tmem_st16(s_base + c * 16, pk);
       }
+      lsum = lsum * alpha + psum;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pfull + 8 * buf);
+      if (lane == 0) mbar_arrive(my_pfull);
+      ++cnt;
     }
     // ---------------------------------------------------------- epilogue
     bool have_o = false;
-    if (n > 0 && !aborted) {
-      have_o = mbar_wait(bar_odone, (n - 1) & 1, p.status, &abort_flag);
+    if (cnt > 0 && !aborted) {
+      have_o = mbar_wait(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const bool live = lsum > 0.f;
+    const float inv = live ? 1.f / lsum : 0.f;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.o) + ((size_t)(b * p.L + i) * p.Hq + h) * HD;
-#pragma unroll
+#pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
       if (have_o) {
-        tmem_ld32(lane_base + 256u + c * 32, o);
+        tmem_ld32(o_base + c * 32, o);
         tmem_wait_ld();
       }
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float a = have_o ? __uint_as_float(o[2 * e]) * inv : 0.f;
-        const float bb = have_o ? __uint_as_float(o[2 * e + 1]) * inv : 0.f;
-        pk[e] = pack_bf16x2(lsum > 0.f ? a : 0.f, lsum > 0.f ? bb : 0.f);
+        const float a = (have_o && live) ? __uint_as_float(o[2 * e]) * inv : 0.f;
+        const float bb = (have_o && live) ? __uint_as_float(o[2 * e + 1]) * inv : 0.f;
+        pk[e] = pack_bf16x2(a, bb);
       }
       if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(og + c * 32);
@@ -297,7 +392,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
     if (valid) {
       const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
-      const bool live = lsum > 0.f;
       p.lse[rr] = live ? (m_use + log2f(lsum)) * kLn2 : -INFINITY;
       if (p.m) p.m[rr] = live ? m_true * kLn2 : -INFINITY;
       if (p.l) p.l[rr] = live ? lsum * ex2_approx(m_use - m_true) : 0.f;
@@ -324,7 +418,7 @@ struct FwdTcLaunch {
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_FWD, s);
     prof_count(CAPATTN_KERNEL_FWD, 1);
-    kern<<<dim3(p.Hq * p.B, p.nq), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+    kern<<<dim3(p.Hq * p.B, (p.nq + 1) / 2), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
     prof_end(CAPATTN_KERNEL_FWD, s);
     return cudaGetLastError();
   }

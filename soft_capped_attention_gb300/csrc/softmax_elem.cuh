@@ -1,0 +1,118 @@
+// Per-element score transforms shared by the tcgen05 kernels.
+//
+// The log2-domain logit of a raw score X = <Q_i, K_j> is
+//     x = temp_i * cap(sm_scale * X) * log2(e)  =  mul_i * f(X * in + bias) + add_i
+// with global constants (in, bias) and per-row constants (mul_i, add_i), where
+// f is the shape of the cap (mosaic_backward.py _apply_cap_mosaic):
+//   none      : f(u) = u                   in = 1,                      mul = sm_scale * temp * log2e
+//   tanh      : f(u) = tanh(u)             in = sm_scale / cap,         mul = cap * temp * log2e
+//   soft_sign : f(u) = u / (1 + |u|)       in = sm_scale / cap,         mul = cap * temp * log2e
+//   alsc      : f(u) = 1 / (1 + 2^-u)      in = sm_scale * alpha / cap * log2e, bias = alpha * beta * log2e,
+//                                          mul = temp * log2e * cap / denom, add = -mul * sigma(alpha beta)
+// Every cap is increasing in X, so for temp_i >= 0 the row maximum of x is the
+// transform of the row maximum of X (of the minimum for temp_i < 0): the
+// forward finds the extreme raw score with one max pass.
+//
+// The derivative of the cap with respect to s = sm_scale * X, in terms of the
+// same intermediate: none 1; tanh 1 - tanh^2; soft_sign 1 / (1 + |u|)^2;
+// alsc (alpha / denom) * sigma (1 - sigma).  The backward folds the constant
+// factor (alpha / denom for alsc) into dscale = sm_scale * temp * factor.
+//
+// tanh uses the tanh.approx instruction (max relative error measured ~1e-5 on
+// GB300: an absolute logit error below cap * 1e-5); the others use ex2.approx
+// and rcp.approx.
+#pragma once
+
+#include "capattn_internal.h"
+#include "tc_common.cuh"
+
+namespace capattn {
+
+constexpr float kL2E = 1.4426950408889634f;
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct Xf {  // global part of the transform
+  float in, bias;
+};
+
+template <int METHOD>
+__device__ __forceinline__ Xf make_xf(const CapConsts& k, float sm_scale) {
+  Xf x;
+  x.bias = 0.f;
+  if constexpr (METHOD == CAPATTN_CAP_TANH || METHOD == CAPATTN_CAP_SOFT_SIGN) {
+    x.in = sm_scale * k.inv_cap;
+  } else if constexpr (METHOD == CAPATTN_CAP_ALSC) {
+    x.in = sm_scale * k.alsc_a * kL2E;
+    x.bias = k.alsc_b * kL2E;
+  } else {
+    x.in = 1.f;
+  }
+  return x;
+}
+
+// Per-row multiplier and offset of the transform.
+template <int METHOD>
+__device__ __forceinline__ void row_consts(const CapConsts& k, float sm_scale, float temp,
+                                           float* mul, float* add) {
+  if constexpr (METHOD == CAPATTN_CAP_TANH || METHOD == CAPATTN_CAP_SOFT_SIGN) {
+    *mul = k.cap * temp * kL2E;
+    *add = 0.f;
+  } else if constexpr (METHOD == CAPATTN_CAP_ALSC) {
+    *mul = temp * kL2E * k.alsc_out;
+    *add = -(*mul) * k.alsc_sb;
+  } else {
+    *mul = sm_scale * temp * kL2E;
+    *add = 0.f;
+  }
+}
+
+// sm_scale * temp * (constant factor of the cap derivative).
+template <int METHOD>
+__device__ __forceinline__ float row_dscale(const CapConsts& k, float sm_scale, float temp) {
+  if constexpr (METHOD == CAPATTN_CAP_ALSC) return sm_scale * temp * k.alsc_dout;
+  return sm_scale * temp;
+}
+
+// f(X * in + bias)
+template <int METHOD>
+__device__ __forceinline__ float cap_f(float X, const Xf& xf) {
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    return tanh_approx(X * xf.in);
+  } else if constexpr (METHOD == CAPATTN_CAP_SOFT_SIGN) {
+    const float u = X * xf.in;
+    return u * rcp_approx(1.0f + fabsf(u));
+  } else if constexpr (METHOD == CAPATTN_CAP_ALSC) {
+    return rcp_approx(1.0f + ex2_approx(-fmaf(X, xf.in, xf.bias)));
+  } else {
+    return X;
+  }
+}
+
+// f and the variable part of its derivative.
+template <int METHOD>
+__device__ __forceinline__ float cap_f_d(float X, const Xf& xf, float* d) {
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    const float t = tanh_approx(X * xf.in);
+    *d = fmaf(-t, t, 1.0f);
+    return t;
+  } else if constexpr (METHOD == CAPATTN_CAP_SOFT_SIGN) {
+    const float u = X * xf.in;
+    const float r = rcp_approx(1.0f + fabsf(u));
+    *d = r * r;
+    return u * r;
+  } else if constexpr (METHOD == CAPATTN_CAP_ALSC) {
+    const float sg = rcp_approx(1.0f + ex2_approx(-fmaf(X, xf.in, xf.bias)));
+    *d = sg - sg * sg;
+    return sg;
+  } else {
+    *d = 1.0f;
+    return X;
+  }
+}
+
+}  // namespace capattn
