@@ -80,6 +80,136 @@ __device__ __forceinline__ void issue_chunk(uint32_t d, uint32_t a0, uint32_t sB
            (first && kk == 0) ? 0u : 1u);
 }
 
+// Steps of the dK/dV kernel: (query head of the group) x (visited query tile).
+struct StepIter {
+  const uint32_t* map;
+  int nwords, G, hh;
+  TileIter it;
+  __device__ StepIter(const uint32_t* m, int n, int g) : map(m), nwords(n), G(g), hh(0), it(m, n) {}
+  __device__ bool next(int& h_out, int& qt) {
+    while (hh < G) {
+      if (it.next(qt)) {
+        h_out = hh;
+        return true;
+      }
+      ++hh;
+      it = TileIter(map, nwords);
+    }
+    return false;
+  }
+};
+
+// Raw per-query-column inputs of one step (loaded ahead of use).
+struct ColRaw {
+  float lse2, radd, temp;
+  int4 ri;
+};
+
+__device__ __forceinline__ ColRaw load_col_raw(const Params& p, int b, int h, int qt, int c, bool active) {
+  ColRaw r;
+  r.lse2 = 0.f;
+  r.radd = 0.f;
+  r.temp = 1.f;
+  r.ri = make_int4(0, 0, -1, 0);
+  const int i = qt * BT + c;
+  if (active && i < p.L) {
+    const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
+    const float lse = p.lse[rr];
+    const float dl = p.delta[rr];
+    const bool fin = isfinite(lse);
+    r.lse2 = fin ? lse * kL2E : 0.f;
+    r.radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
+    if (p.temp) r.temp = p.temp[(size_t)b * p.L + i];
+    r.ri = p.rowinfo[(size_t)b * p.L + i];
+  }
+  return r;
+}
+
+// dK/dV elementwise on 16 query columns (col0 .. col0 + 15) of key row jrow:
+// P^T and dX^T packed to bf16 and stored at TMEM columns dst (P) and 128 + dst (dX).
+template <int METHOD, bool MASKED>
+__device__ __forceinline__ void dkv_sub(const uint32_t (&sv)[16], const uint32_t (&dp)[16],
+                                        const float4* colc, const int4* coli, int col0, int jrow,
+                                        const Xf& xf, uint32_t lane_base, int dst) {
+  uint32_t pp[8], px[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float pv[2], xv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int cc = col0 + 2 * e + u;
+      const float4 k4 = colc[cc];
+      float d;
+      const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
+      float P = ex2_approx(fmaf(k4.x, f, k4.y));
+      if constexpr (MASKED) {
+        const int4 ci = coli[cc];
+        if (!((jrow >= ci.x && jrow < ci.y) || jrow == ci.z)) P = 0.f;
+      }
+      pv[u] = P;
+      xv[u] = (k4.z * d) * (P * (__uint_as_float(dp[2 * e + u]) + k4.w));
+    }
+    pp[e] = pack_bf16x2(pv[0], pv[1]);
+    px[e] = pack_bf16x2(xv[0], xv[1]);
+  }
+  tmem_st8(lane_base + dst, pp);
+  tmem_st8(lane_base + 128u + dst, px);
+}
+
+// One warpgroup's 64 query columns of a step, in four sub-chunks of 16 with
+// the next sub-chunk's TMEM loads in flight while one is computed; the MMA
+// issuer is signalled after each half (32 columns).
+template <int METHOD, bool MASKED>
+__device__ __forceinline__ void dkv_step(const float4* colc, const int4* coli, int wg, int jrow,
+                                         const Xf& xf, uint32_t lane_base, uint32_t bar_ew, int lane) {
+  uint32_t sa[16], da[16], sb[16], db[16];
+  const int c0 = 64 * wg;
+  tmem_ld16(lane_base + c0, sa);
+  tmem_ld16(lane_base + 128u + c0, da);
+  tmem_wait_ld();
+#pragma unroll 1
+  for (int k = 0; k < 4; k += 2) {
+    tmem_ld16(lane_base + c0 + 16 * (k + 1), sb);
+    tmem_ld16(lane_base + 128u + c0 + 16 * (k + 1), db);
+    dkv_sub<METHOD, MASKED>(sa, da, colc, coli, c0 + 16 * k, jrow, xf, lane_base, c0 + 8 * k);
+    tmem_wait_ld();
+    if (k + 2 < 4) {
+      tmem_ld16(lane_base + c0 + 16 * (k + 2), sa);
+      tmem_ld16(lane_base + 128u + c0 + 16 * (k + 2), da);
+    }
+    dkv_sub<METHOD, MASKED>(sb, db, colc, coli, c0 + 16 * (k + 1), jrow, xf, lane_base, c0 + 8 * (k + 1));
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + (k >> 1)));
+    tmem_wait_ld();
+  }
+}
+
+// dQ elementwise on 32 key columns (absolute j0 .. j0 + 31) of query row (span
+// ri): dX packed to bf16 into px.  (No TMEM access: callers branch per row.)
+template <int METHOD, bool MASKED>
+__device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_t (&dp)[32], int j0,
+                                         int4 ri, const Xf& xf, float mul, float addl, float dscale,
+                                         float radd, uint32_t (&px)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float xv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float d;
+      const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
+      float P = ex2_approx(fmaf(mul, f, addl));
+      if constexpr (MASKED) {
+        const int jj = j0 + 2 * e + u;
+        if (!((jj >= ri.x && jj < ri.y) || jj == ri.z)) P = 0.f;
+      }
+      xv[u] = (dscale * d) * (P * (__uint_as_float(dp[2 * e + u]) + radd));
+    }
+    px[e] = pack_bf16x2(xv[0], xv[1]);
+  }
+}
+
 // ======================================================================= dK / dV
 template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -211,90 +341,52 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
     const float zw = p.z_loss_weight;
     bool aborted = false;
-    int step = 0;
-    for (int hh = 0; hh < p.G && !aborted; ++hh) {
-      const int h = g * p.G + hh;
-      TileIter it(map, p.wq);
-      int qt;
-      while (it.next(qt)) {
-        const int q0 = qt * BT;
-        const int cb = step & 1, cu = step >> 1;
-        const uint32_t my_cfull = bar_cfull + 8 * (2 * wg + cb);
-        const uint32_t my_cfree = bar_cfree + 8 * (2 * wg + cb);
-        if (step >= 2 && !mbar_wait(my_cfree, (cu - 1) & 1, p.status, &abort_flag)) {
-          aborted = true;
-          break;
-        }
-        if (tid < 64) {  // constants of query column 64 wg + tid
-          const int c = 64 * wg + tid;
-          const int i = q0 + c;
-          const bool valid = i < p.L;
-          const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
-          const float lse = valid ? p.lse[rr] : -INFINITY;
-          const float dl = valid ? p.delta[rr] : 0.f;
-          const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
-          const bool fin = isfinite(lse);
-          float mul, add;
-          row_consts<METHOD>(p.cap, p.sm_scale, temp, &mul, &add);
-          colc[cb][c] = make_float4(mul, add - (fin ? lse * kL2E : 0.f),
-                                    row_dscale<METHOD>(p.cap, p.sm_scale, temp),
-                                    -dl + (fin ? zw * lse : 0.f));
-          coli[cb][c] = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
-        }
-        mbar_arrive(my_cfull);
-        const int2 fr = p.qfull[(size_t)b * p.nq + qt];
-        const bool tile_full = (kt >= fr.x) && (kt < fr.y);
-        if (!mbar_wait(my_cfull, cu & 1, p.status, &abort_flag) ||
-            !mbar_wait(bar_sdp, step & 1, p.status, &abort_flag)) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * wg + 32 * c;  // first query column of the chunk
-          uint32_t sv[32], dp[32];
-          tmem_ld32(lane_base + col0, sv);
-          tmem_ld32(lane_base + 128u + col0, dp);
-          tmem_wait_ld();
-          uint32_t pp[16], px[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pv[2], xv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cc = col0 + 2 * e + u;
-              const float4 k4 = colc[cb][cc];
-              float d;
-              const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
-              bool lv = true;
-              if (!tile_full) {
-                const int4 ci = coli[cb][cc];
-                lv = (jrow >= ci.x && jrow < ci.y) || jrow == ci.z;
-              }
-              const float P = lv ? ex2_approx(fmaf(k4.x, f, k4.y)) : 0.f;
-              pv[u] = P;
-              xv[u] = (k4.z * d) * (P * (__uint_as_float(dp[2 * e + u]) + k4.w));
-            }
-            pp[e] = pack_bf16x2(pv[0], pv[1]);
-            px[e] = pack_bf16x2(xv[0], xv[1]);
-          }
-          const uint32_t dst = (uint32_t)(64 * wg + 16 * c);
-          tmem_st16(lane_base + dst, pp);
-          tmem_st16(lane_base + 128u + dst, px);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + c));
-        }
-        mbar_arrive(my_cfree);
-        ++step;
+    // Raw column constants are loaded one step ahead (their global-load latency
+    // hides behind a whole step of work).
+    StepIter nx(map, p.wq, p.G);
+    int nh = 0, nqt = 0;
+    bool have_next = nx.next(nh, nqt);
+    ColRaw cur = load_col_raw(p, b, g * p.G + nh, nqt, 64 * wg + tid, have_next && tid < 64);
+    int cur_qt = nqt;
+    for (int step = 0; step < n && have_next; ++step) {
+      const int cb = step & 1, cu = step >> 1;
+      const uint32_t my_cfull = bar_cfull + 8 * (2 * wg + cb);
+      const uint32_t my_cfree = bar_cfree + 8 * (2 * wg + cb);
+      if (step >= 2 && !mbar_wait_warp(my_cfree, (cu - 1) & 1, p.status, &abort_flag)) {
+        aborted = true;
+        break;
       }
+      if (tid < 64) {
+        const int c = 64 * wg + tid;
+        float mul, add;
+        row_consts<METHOD>(p.cap, p.sm_scale, cur.temp, &mul, &add);
+        colc[cb][c] = make_float4(mul, add - cur.lse2, row_dscale<METHOD>(p.cap, p.sm_scale, cur.temp),
+                                  cur.radd);
+        coli[cb][c] = cur.ri;
+      }
+      mbar_arrive(my_cfull);
+      const int2 fr = p.qfull[(size_t)b * p.nq + cur_qt];
+      const bool tile_full = (kt >= fr.x) && (kt < fr.y);
+      have_next = nx.next(nh, nqt);
+      const ColRaw nxt = load_col_raw(p, b, g * p.G + nh, nqt, 64 * wg + tid, have_next && tid < 64);
+      if (!mbar_wait_warp(my_cfull, cu & 1, p.status, &abort_flag) ||
+          !mbar_wait_warp(bar_sdp, step & 1, p.status, &abort_flag)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      if (tile_full)
+        dkv_step<METHOD, false>(colc[cb], coli[cb], wg, jrow, xf, lane_base, bar_ew, lane);
+      else
+        dkv_step<METHOD, true>(colc[cb], coli[cb], wg, jrow, xf, lane_base, bar_ew, lane);
+      mbar_arrive(my_cfree);
+      cur = nxt;
+      cur_qt = nqt;
     }
     // ---------------------------------------------------------- epilogue
     bool have = false;
     if (n > 0 && !aborted) {
-      have = mbar_wait(bar_final, 0, p.status, &abort_flag);
+      have = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
     // warpgroup 0 writes dV, warpgroup 1 writes dK
@@ -452,43 +544,44 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       it.next(t);
       const int k0 = t * BT;
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BT);
-      if (!mbar_wait(bar_sdp, j & 1, p.status, &abort_flag)) {
+      if (!mbar_wait_warp(bar_sdp, j & 1, p.status, &abort_flag)) {
         aborted = true;
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = 64 * wg + 32 * c;
-        uint32_t sv[32], dp[32];
-        tmem_ld32(lane_base + col0, sv);
-        tmem_ld32(lane_base + 128u + col0, dp);
-        tmem_wait_ld();
-        uint32_t px[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float xv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float d;
-            const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
-            const int jj = k0 + col0 + 2 * e + u;
-            const bool lv = full || (jj >= ri.x && jj < ri.y) || jj == ri.z;
-            const float P = lv ? ex2_approx(fmaf(mul, f, addl)) : 0.f;
-            xv[u] = (dscale * d) * (P * (__uint_as_float(dp[2 * e + u]) + radd));
-          }
-          px[e] = pack_bf16x2(xv[0], xv[1]);
-        }
-        tmem_st16(lane_base + (uint32_t)(64 * wg + 16 * c), px);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + c));
-      }
+      uint32_t sa[32], da[32], sb[32], db[32];
+      const int colA = 64 * wg, colB = 64 * wg + 32;
+      tmem_ld32(lane_base + colA, sa);
+      tmem_ld32(lane_base + 128u + colA, da);
+      tmem_wait_ld();
+      tmem_ld32(lane_base + colB, sb);
+      tmem_ld32(lane_base + 128u + colB, db);
+      uint32_t px[16];
+      if (full)
+        dq_chunk<METHOD, false>(sa, da, k0 + colA, ri, xf, mul, addl, dscale, radd, px);
+      else
+        dq_chunk<METHOD, true>(sa, da, k0 + colA, ri, xf, mul, addl, dscale, radd, px);
+      __syncwarp();
+      tmem_st16(lane_base + 64 * wg, px);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + 0));
+      tmem_wait_ld();
+      if (full)
+        dq_chunk<METHOD, false>(sb, db, k0 + colB, ri, xf, mul, addl, dscale, radd, px);
+      else
+        dq_chunk<METHOD, true>(sb, db, k0 + colB, ri, xf, mul, addl, dscale, radd, px);
+      __syncwarp();
+      tmem_st16(lane_base + 64 * wg + 16, px);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + 1));
     }
     bool have = false;
     if (n > 0 && !aborted) {
-      have = mbar_wait(bar_final, 0, p.status, &abort_flag);
+      have = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
     // warpgroup wg writes dQ columns [64 wg, 64 wg + 64)

@@ -98,6 +98,49 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pt, uint32_t sV, u
     mma_ts(d, pt + ks * 8, smem_desc(sV + ks * 2048, SLAB, 1024), idesc, (acc0 || ks > 0) ? 1u : 0u);
 }
 
+// Row extreme (max of X, or of -X when the temperature is negative) over live
+// columns k0 .. k0 + 127 of one row.
+template <bool MASKED>
+__device__ __forceinline__ float row_extreme(const uint32_t (&v)[128], bool neg, int k0, int4 ri) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+  const float sg = neg ? -1.f : 1.f;
+#pragma unroll
+  for (int e = 0; e < 128; e += 2) {
+    float a = sg * __uint_as_float(v[e]), b = sg * __uint_as_float(v[e + 1]);
+    if constexpr (MASKED) {
+      const int j0 = k0 + e, j1 = k0 + e + 1;
+      if (!((j0 >= ri.x && j0 < ri.y) || j0 == ri.z)) a = -INFINITY;
+      if (!((j1 >= ri.x && j1 < ri.y) || j1 == ri.z)) b = -INFINITY;
+    }
+    m0 = fmaxf(m0, a);
+    m1 = fmaxf(m1, b);
+  }
+  return fmaxf(m0, m1);
+}
+
+// 32 columns of P = 2^(mul * f(X) + addm), packed to bf16 into pk; returns
+// their sum.  (No TMEM access here: callers branch per row, and the warp-wide
+// tcgen05 store must run after the branch has reconverged.)
+template <int METHOD, bool MASKED>
+__device__ __forceinline__ float p_chunk(const uint32_t (&v)[32], uint32_t (&pk)[16], const Xf& xf,
+                                         float mul, float addm, int j0, int4 ri, bool any) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float p0 = ex2_approx(fmaf(mul, cap_f<METHOD>(__uint_as_float(v[2 * e]), xf), addm));
+    float p1 = ex2_approx(fmaf(mul, cap_f<METHOD>(__uint_as_float(v[2 * e + 1]), xf), addm));
+    if constexpr (MASKED) {
+      const int ja = j0 + 2 * e, jb = ja + 1;
+      if (!(any && ((ja >= ri.x && ja < ri.y) || ja == ri.z))) p0 = 0.f;
+      if (!(any && ((jb >= ri.x && jb < ri.y) || jb == ri.z))) p1 = 0.f;
+    }
+    s0 += p0;
+    s1 += p1;
+    pk[e] = pack_bf16x2(p0, p1);
+  }
+  return s0 + s1;
+}
+
 template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -266,36 +309,21 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     while (it.next(t, a0, a1)) {
       if (!(tsel == 0 ? a0 : a1)) continue;
       const int k0 = t * BN;
-      if (!mbar_wait(my_sfull, cnt & 1, p.status, &abort_flag)) {
+      if (!mbar_wait_warp(my_sfull, cnt & 1, p.status, &abort_flag)) {
         aborted = true;
         break;
       }
       tc_fence_after();
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BN);
-      // ---- pass 1: extreme raw score of the live entries
-      float ext = -INFINITY;  // max of (neg ? -X : X)
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(s_base + c * 32, v);
+      // ---- pass 1: extreme raw score of the live entries (one batched TMEM read)
+      float ext;
+      {
+        uint32_t v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(s_base + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
         tmem_wait_ld();
-        if (full) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float a = __uint_as_float(v[e]), bb = __uint_as_float(v[e + 1]);
-            if (neg) { a = -a; bb = -bb; }
-            ext = fmaxf(ext, fmaxf(a, bb));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int jj = k0 + c * 32 + e;
-            const bool lv = (jj >= ri.x && jj < ri.y) || jj == ri.z;
-            float a = __uint_as_float(v[e]);
-            if (neg) a = -a;
-            ext = fmaxf(ext, lv ? a : -INFINITY);
-          }
-        }
+        ext = full ? row_extreme<false>(v, neg, k0, ri) : row_extreme<true>(v, neg, k0, ri);
       }
       const float x_max =
           (ext == -INFINITY) ? -INFINITY : fmaf(rmul, cap_f<METHOD>(neg ? -ext : ext, xf), radd);
@@ -319,40 +347,35 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           tmem_st32(o_base + c * 32, o);
         }
       }
-      // ---- pass 2: P = 2^(x - m_use), packed bf16 over S columns [0, 64)
+      // ---- pass 2: P = 2^(x - m_use), packed bf16 over S columns [0, 64).
+      // The next chunk's TMEM load is issued before the current chunk is computed.
       const bool any = m_use != -INFINITY;
       const float addm = radd - (any ? m_use : 0.f);
+      const bool fast = full && any;
       float psum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(s_base + c * 32, v);
+      {
+        uint32_t va[32], vb[32], pk[16];
+        tmem_ld32(s_base, va);
         tmem_wait_ld();
-        uint32_t pk[16];
-        if (full && any) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(rmul, cap_f<METHOD>(__uint_as_float(v[2 * e]), xf), addm));
-            const float p1 = ex2_approx(fmaf(rmul, cap_f<METHOD>(__uint_as_float(v[2 * e + 1]), xf), addm));
-            psum += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pp[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int jj = k0 + c * 32 + 2 * e + u;
-              const bool lv = any && ((jj >= ri.x && jj < ri.y) || jj == ri.z);
-              pp[u] = lv ? ex2_approx(fmaf(rmul, cap_f<METHOD>(__uint_as_float(v[2 * e + u]), xf), addm))
-                         : 0.f;
-            }
-            psum += pp[0] + pp[1];
-            pk[e] = pack_bf16x2(pp[0], pp[1]);
-          }
+#pragma unroll 1
+        for (int c = 0; c < 4; c += 2) {
+          tmem_ld32(s_base + (c + 1) * 32, vb);
+          if (fast)
+            psum += p_chunk<METHOD, false>(va, pk, xf, rmul, addm, k0 + c * 32, ri, any);
+          else
+            psum += p_chunk<METHOD, true>(va, pk, xf, rmul, addm, k0 + c * 32, ri, any);
+          __syncwarp();
+          tmem_st16(s_base + c * 16, pk);
+          tmem_wait_ld();
+          if (c + 2 < 4) tmem_ld32(s_base + (c + 2) * 32, va);
+          if (fast)
+            psum += p_chunk<METHOD, false>(vb, pk, xf, rmul, addm, k0 + (c + 1) * 32, ri, any);
+          else
+            psum += p_chunk<METHOD, true>(vb, pk, xf, rmul, addm, k0 + (c + 1) * 32, ri, any);
+          __syncwarp();
+          tmem_st16(s_base + (c + 1) * 16, pk);
+          tmem_wait_ld();
         }
-        tmem_st16(s_base + c * 16, pk);
       }
       lsum = lsum * alpha + psum;
       tmem_wait_st();
@@ -364,7 +387,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     // ---------------------------------------------------------- epilogue
     bool have_o = false;
     if (cnt > 0 && !aborted) {
-      have_o = mbar_wait(bar_final, 0, p.status, &abort_flag);
+      have_o = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
     const bool live = lsum > 0.f;
