@@ -46,6 +46,8 @@ constexpr int TILE = 2 * SLAB;
 constexpr int NSTAGE = 2;
 constexpr int NTHREADS = 320;
 constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
+constexpr int kBwdPolyPairs = 10;  // of 16 column pairs in a dQ chunk: tanh on the FMA pipe
+constexpr int kDkvPolyPairs = 5;   // of 8 column pairs in a dK/dV sub-chunk
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
   uint32_t pk[16];
@@ -125,35 +127,91 @@ __device__ __forceinline__ ColRaw load_col_raw(const Params& p, int b, int h, in
   return r;
 }
 
+// Backward elementwise on a pair of scores: P = 2^(mul * f + add) (0 when
+// masked) and dX = dscale * f' * P * (dP + radd), with packed fp32x2 math.  For
+// the tanh cap with POLY, tanh is evaluated on the FMA pipe (the caller
+// guarantees |X * in| <= 0.5 for the whole warp).
+template <int METHOD, bool POLY>
+__device__ __forceinline__ void bwd_pair(float X0, float X1, float dp0, float dp1, const Xf& xf,
+                                         F2 mul, F2 add, F2 dsc, F2 radd, bool l0, bool l1,
+                                         float& P0, float& P1, float& dX0, float& dX1) {
+  F2 f, d;
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    const F2 u = f2_mul(f2(X0, X1), f2(xf.in, xf.in));
+    if constexpr (POLY) {
+      f = tanh_poly2(u);
+    } else {
+      float a, b;
+      f2_split(u, a, b);
+      f = f2(tanh_approx(a), tanh_approx(b));
+    }
+    d = f2_fma(f2_mul(f, f2(-1.f, -1.f)), f, f2(1.f, 1.f));
+  } else {
+    float d0, d1;
+    const float f0 = cap_f_d<METHOD>(X0, xf, &d0);
+    const float f1 = cap_f_d<METHOD>(X1, xf, &d1);
+    f = f2(f0, f1);
+    d = f2(d0, d1);
+  }
+  float x0, x1;
+  f2_split(f2_fma(mul, f, add), x0, x1);
+  P0 = l0 ? ex2_approx(x0) : 0.f;
+  P1 = l1 ? ex2_approx(x1) : 0.f;
+  const F2 g = f2_mul(f2(P0, P1), f2_add(f2(dp0, dp1), radd));
+  f2_split(f2_mul(f2_mul(dsc, d), g), dX0, dX1);
+}
+
 // dK/dV elementwise on 16 query columns (col0 .. col0 + 15) of key row jrow:
 // P^T and dX^T packed to bf16 and stored at TMEM columns dst (P) and 128 + dst (dX).
+template <int METHOD, bool MASKED, bool POLY>
+__device__ __forceinline__ void dkv_sub_impl(const uint32_t (&sv)[16], const uint32_t (&dp)[16],
+                                             const float4* colc, const int4* coli, int col0,
+                                             int jrow, const Xf& xf, uint32_t lane_base, int dst) {
+  uint32_t pp[8], px[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int cc = col0 + 2 * e;
+    const float4 ka = colc[cc], kb = colc[cc + 1];
+    bool l0 = true, l1 = true;
+    if constexpr (MASKED) {
+      const int4 ca = coli[cc], cb = coli[cc + 1];
+      l0 = (jrow >= ca.x && jrow < ca.y) || jrow == ca.z;
+      l1 = (jrow >= cb.x && jrow < cb.y) || jrow == cb.z;
+    }
+    float P0, P1, x0, x1;
+    const float X0 = __uint_as_float(sv[2 * e]), X1 = __uint_as_float(sv[2 * e + 1]);
+    const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
+    if (POLY && e < kDkvPolyPairs)
+      bwd_pair<METHOD, true>(X0, X1, d0, d1, xf, f2(ka.x, kb.x), f2(ka.y, kb.y), f2(ka.z, kb.z),
+                             f2(ka.w, kb.w), l0, l1, P0, P1, x0, x1);
+    else
+      bwd_pair<METHOD, false>(X0, X1, d0, d1, xf, f2(ka.x, kb.x), f2(ka.y, kb.y), f2(ka.z, kb.z),
+                              f2(ka.w, kb.w), l0, l1, P0, P1, x0, x1);
+    pp[e] = pack_bf16x2(P0, P1);
+    px[e] = pack_bf16x2(x0, x1);
+  }
+  tmem_st8(lane_base + dst, pp);
+  tmem_st8(lane_base + 128u + dst, px);
+}
+
+// dK/dV elementwise on 16 query columns (col0 .. col0 + 15) of key row jrow:
+// P^T and dX^T packed to bf16 and stored at TMEM columns dst (P) and 128 + dst (dX).
+// For the tanh cap the warp votes on whether all its arguments are small enough
+// for the FMA-pipe polynomial.
 template <int METHOD, bool MASKED>
 __device__ __forceinline__ void dkv_sub(const uint32_t (&sv)[16], const uint32_t (&dp)[16],
                                         const float4* colc, const int4* coli, int col0, int jrow,
                                         const Xf& xf, uint32_t lane_base, int dst) {
-  uint32_t pp[8], px[8];
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    float am = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float pv[2], xv[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int cc = col0 + 2 * e + u;
-      const float4 k4 = colc[cc];
-      float d;
-      const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
-      float P = ex2_approx(fmaf(k4.x, f, k4.y));
-      if constexpr (MASKED) {
-        const int4 ci = coli[cc];
-        if (!((jrow >= ci.x && jrow < ci.y) || jrow == ci.z)) P = 0.f;
-      }
-      pv[u] = P;
-      xv[u] = (k4.z * d) * (P * (__uint_as_float(dp[2 * e + u]) + k4.w));
+    for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(__uint_as_float(sv[e])));
+    if (__all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU)) {
+      dkv_sub_impl<METHOD, MASKED, true>(sv, dp, colc, coli, col0, jrow, xf, lane_base, dst);
+      return;
     }
-    pp[e] = pack_bf16x2(pv[0], pv[1]);
-    px[e] = pack_bf16x2(xv[0], xv[1]);
   }
-  tmem_st8(lane_base + dst, pp);
-  tmem_st8(lane_base + 128u + dst, px);
+  dkv_sub_impl<METHOD, MASKED, false>(sv, dp, colc, coli, col0, jrow, xf, lane_base, dst);
 }
 
 // One warpgroup's 64 query columns of a step, in four sub-chunks of 16 with
@@ -188,25 +246,55 @@ __device__ __forceinline__ void dkv_step(const float4* colc, const int4* coli, i
 
 // dQ elementwise on 32 key columns (absolute j0 .. j0 + 31) of query row (span
 // ri): dX packed to bf16 into px.  (No TMEM access: callers branch per row.)
-template <int METHOD, bool MASKED>
+// With POLY (tanh cap), column pairs [0, poly_pairs) use the FMA-pipe tanh.
+template <int METHOD, bool MASKED, bool POLY>
 __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_t (&dp)[32], int j0,
                                          int4 ri, const Xf& xf, float mul, float addl, float dscale,
                                          float radd, uint32_t (&px)[16]) {
+  const F2 mul2 = f2(mul, mul), add2 = f2(addl, addl), dsc2 = f2(dscale, dscale),
+           radd2 = f2(radd, radd);
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    float xv[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float d;
-      const float f = cap_f_d<METHOD>(__uint_as_float(sv[2 * e + u]), xf, &d);
-      float P = ex2_approx(fmaf(mul, f, addl));
-      if constexpr (MASKED) {
-        const int jj = j0 + 2 * e + u;
-        if (!((jj >= ri.x && jj < ri.y) || jj == ri.z)) P = 0.f;
-      }
-      xv[u] = (dscale * d) * (P * (__uint_as_float(dp[2 * e + u]) + radd));
+    bool l0 = true, l1 = true;
+    if constexpr (MASKED) {
+      const int ja = j0 + 2 * e, jb = ja + 1;
+      l0 = (ja >= ri.x && ja < ri.y) || ja == ri.z;
+      l1 = (jb >= ri.x && jb < ri.y) || jb == ri.z;
     }
-    px[e] = pack_bf16x2(xv[0], xv[1]);
+    float P0, P1, x0, x1;
+    const float X0 = __uint_as_float(sv[2 * e]), X1 = __uint_as_float(sv[2 * e + 1]);
+    const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
+    if (POLY && e < kBwdPolyPairs)
+      bwd_pair<METHOD, true>(X0, X1, d0, d1, xf, mul2, add2, dsc2, radd2, l0, l1, P0, P1, x0, x1);
+    else
+      bwd_pair<METHOD, false>(X0, X1, d0, d1, xf, mul2, add2, dsc2, radd2, l0, l1, P0, P1, x0, x1);
+    px[e] = pack_bf16x2(x0, x1);
+  }
+}
+
+// Chooses the dQ chunk variant: masked or not (per row), FMA-pipe tanh when the
+// whole warp's arguments are in range (warp vote).
+template <int METHOD>
+__device__ __forceinline__ void dq_dispatch(bool full, const uint32_t (&sv)[32], const uint32_t (&dp)[32],
+                                            int j0, int4 ri, const Xf& xf, float mul, float addl,
+                                            float dscale, float radd, uint32_t (&px)[16]) {
+  bool poly = false;
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    float am = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(sv[e])));
+    poly = __all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU);
+  }
+  if (poly) {
+    if (full)
+      dq_chunk<METHOD, false, true>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
+    else
+      dq_chunk<METHOD, true, true>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
+  } else {
+    if (full)
+      dq_chunk<METHOD, false, false>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
+    else
+      dq_chunk<METHOD, true, false>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
   }
 }
 
@@ -328,8 +416,9 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (!ok) break;
         mma_commit(bar_empty + 8 * s);
       }
+      // The MMA thread does not wait for its own commit here: the consumer
+      // warps wait for it, and warp 1 re-checks it before freeing TMEM.
       mma_commit(bar_final);
-      drain_wait(bar_final, 0);
     }
   } else {
     const int wg = (warp - 2) >> 2;        // query columns [64 wg, 64 wg + 64)
@@ -405,9 +494,14 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
     }
   }
+  __syncwarp();  // warps 0 and 1 reach the CTA barrier converged
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    // Every MMA has completed before TMEM is released (normally already
+    // observed by the consumer warps; bounded non-suspending poll).
+    if (lane == 0 && n > 0) mbar_poll(bar_final, 0);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -515,8 +609,9 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         if (!ok) break;
         mma_commit(bar_empty + 8 * s);
       }
+      // The MMA thread does not wait for its own commit here: the consumer
+      // warps wait for it, and warp 1 re-checks it before freeing TMEM.
       mma_commit(bar_final);
-      drain_wait(bar_final, 0);
     }
   } else {
     const int wg = (warp - 2) >> 2;        // key columns [64 wg, 64 wg + 64)
@@ -557,10 +652,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       tmem_ld32(lane_base + colB, sb);
       tmem_ld32(lane_base + 128u + colB, db);
       uint32_t px[16];
-      if (full)
-        dq_chunk<METHOD, false>(sa, da, k0 + colA, ri, xf, mul, addl, dscale, radd, px);
-      else
-        dq_chunk<METHOD, true>(sa, da, k0 + colA, ri, xf, mul, addl, dscale, radd, px);
+      dq_dispatch<METHOD>(full, sa, da, k0 + colA, ri, xf, mul, addl, dscale, radd, px);
       __syncwarp();
       tmem_st16(lane_base + 64 * wg, px);
       tmem_wait_st();
@@ -568,10 +660,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + 0));
       tmem_wait_ld();
-      if (full)
-        dq_chunk<METHOD, false>(sb, db, k0 + colB, ri, xf, mul, addl, dscale, radd, px);
-      else
-        dq_chunk<METHOD, true>(sb, db, k0 + colB, ri, xf, mul, addl, dscale, radd, px);
+      dq_dispatch<METHOD>(full, sb, db, k0 + colB, ri, xf, mul, addl, dscale, radd, px);
       __syncwarp();
       tmem_st16(lane_base + 64 * wg + 16, px);
       tmem_wait_st();
@@ -599,9 +688,14 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       }
     }
   }
+  __syncwarp();  // warps 0 and 1 reach the CTA barrier converged
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    // Every MMA has completed before TMEM is released (normally already
+    // observed by the consumer warps; bounded non-suspending poll).
+    if (lane == 0 && n > 0) mbar_poll(bar_final, 0);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

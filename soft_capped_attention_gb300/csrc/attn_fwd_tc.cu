@@ -98,24 +98,67 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pt, uint32_t sV, u
     mma_ts(d, pt + ks * 8, smem_desc(sV + ks * 2048, SLAB, 1024), idesc, (acc0 || ks > 0) ? 1u : 0u);
 }
 
-// Row extreme (max of X, or of -X when the temperature is negative) over live
-// columns k0 .. k0 + 127 of one row.
+// Maximum and minimum raw score over the live columns k0 .. k0 + 127 of one row.
 template <bool MASKED>
-__device__ __forceinline__ float row_extreme(const uint32_t (&v)[128], bool neg, int k0, int4 ri) {
-  float m0 = -INFINITY, m1 = -INFINITY;
-  const float sg = neg ? -1.f : 1.f;
+__device__ __forceinline__ void row_range(const uint32_t (&v)[128], int k0, int4 ri, float& vmax,
+                                          float& vmin) {
+  float a0 = -INFINITY, a1 = -INFINITY, b0 = INFINITY, b1 = INFINITY;
 #pragma unroll
   for (int e = 0; e < 128; e += 2) {
-    float a = sg * __uint_as_float(v[e]), b = sg * __uint_as_float(v[e + 1]);
+    float x = __uint_as_float(v[e]), y = __uint_as_float(v[e + 1]);
+    float xl = x, yl = y;
     if constexpr (MASKED) {
       const int j0 = k0 + e, j1 = k0 + e + 1;
-      if (!((j0 >= ri.x && j0 < ri.y) || j0 == ri.z)) a = -INFINITY;
-      if (!((j1 >= ri.x && j1 < ri.y) || j1 == ri.z)) b = -INFINITY;
+      const bool l0 = (j0 >= ri.x && j0 < ri.y) || j0 == ri.z;
+      const bool l1 = (j1 >= ri.x && j1 < ri.y) || j1 == ri.z;
+      x = l0 ? x : -INFINITY;
+      y = l1 ? y : -INFINITY;
+      xl = l0 ? xl : INFINITY;
+      yl = l1 ? yl : INFINITY;
     }
-    m0 = fmaxf(m0, a);
-    m1 = fmaxf(m1, b);
+    a0 = fmaxf(a0, x);
+    a1 = fmaxf(a1, y);
+    b0 = fminf(b0, xl);
+    b1 = fminf(b1, yl);
   }
-  return fmaxf(m0, m1);
+  vmax = fmaxf(a0, a1);
+  vmin = fminf(b0, b1);
+}
+
+// 32 columns of P for the tanh cap when every |X * in| of the warp is within
+// the polynomial's range: the first POLY_PAIRS column pairs evaluate tanh on the
+// FMA pipe, the rest with tanh.approx; packed fp32x2 arithmetic throughout.
+template <bool MASKED, int POLY_PAIRS>
+__device__ __forceinline__ float p_chunk_tanh_fast(const uint32_t (&v)[32], uint32_t (&pk)[16],
+                                                   const Xf& xf, float mul, float addm, int j0,
+                                                   int4 ri, bool any) {
+  const F2 in2 = f2(xf.in, xf.in), mul2 = f2(mul, mul), add2 = f2(addm, addm);
+  F2 acc = f2(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const F2 u = f2_mul(f2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), in2);
+    F2 t;
+    if (e < POLY_PAIRS) {
+      t = tanh_poly2(u);
+    } else {
+      float a, b;
+      f2_split(u, a, b);
+      t = f2(tanh_approx(a), tanh_approx(b));
+    }
+    float x0, x1;
+    f2_split(f2_fma(t, mul2, add2), x0, x1);
+    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if constexpr (MASKED) {
+      const int ja = j0 + 2 * e, jb = ja + 1;
+      if (!(any && ((ja >= ri.x && ja < ri.y) || ja == ri.z))) p0 = 0.f;
+      if (!(any && ((jb >= ri.x && jb < ri.y) || jb == ri.z))) p1 = 0.f;
+    }
+    acc = f2_add(acc, f2(p0, p1));
+    pk[e] = pack_bf16x2(p0, p1);
+  }
+  float s0, s1;
+  f2_split(acc, s0, s1);
+  return s0 + s1;
 }
 
 // 32 columns of P = 2^(mul * f(X) + addm), packed to bf16 into pk; returns
@@ -139,6 +182,22 @@ __device__ __forceinline__ float p_chunk(const uint32_t (&v)[32], uint32_t (&pk)
     pk[e] = pack_bf16x2(p0, p1);
   }
   return s0 + s1;
+}
+
+constexpr int kPolyPairs = 10;  // of 16 column pairs per chunk: tanh on the FMA pipe
+
+template <int METHOD>
+__device__ __forceinline__ float p_dispatch(bool full_any, bool poly, const uint32_t (&v)[32],
+                                           uint32_t (&pk)[16], const Xf& xf, float mul, float addm,
+                                           int j0, int4 ri, bool any) {
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    if (poly) {
+      return full_any ? p_chunk_tanh_fast<false, kPolyPairs>(v, pk, xf, mul, addm, j0, ri, any)
+                      : p_chunk_tanh_fast<true, kPolyPairs>(v, pk, xf, mul, addm, j0, ri, any);
+    }
+  }
+  return full_any ? p_chunk<METHOD, false>(v, pk, xf, mul, addm, j0, ri, any)
+                  : p_chunk<METHOD, true>(v, pk, xf, mul, addm, j0, ri, any);
 }
 
 template <int METHOD>
@@ -281,8 +340,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         c0 = n0;
         c1 = n1;
       }
+      // The MMA thread does not wait for its own commit here: the consumer
+      // warps wait for it, and warp 1 re-checks it before freeing TMEM.
       mma_commit(bar_final);
-      drain_wait(bar_final, 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -315,18 +375,28 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       tc_fence_after();
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BN);
-      // ---- pass 1: extreme raw score of the live entries (one batched TMEM read)
-      float ext;
+      // ---- pass 1: range of the live raw scores (one batched TMEM read)
+      float vmax, vmin;
       {
         uint32_t v[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           tmem_ld32(s_base + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
         tmem_wait_ld();
-        ext = full ? row_extreme<false>(v, neg, k0, ri) : row_extreme<true>(v, neg, k0, ri);
+        if (full)
+          row_range<false>(v, k0, ri, vmax, vmin);
+        else
+          row_range<true>(v, k0, ri, vmax, vmin);
       }
+      // Every cap is increasing: the logit maximum is the transform of the raw
+      // maximum (of the minimum for a negative temperature).
+      const float xsel = neg ? vmin : vmax;
       const float x_max =
-          (ext == -INFINITY) ? -INFINITY : fmaf(rmul, cap_f<METHOD>(neg ? -ext : ext, xf), radd);
+          (vmax == -INFINITY) ? -INFINITY : fmaf(rmul, cap_f<METHOD>(xsel, xf), radd);
+      // tanh on the FMA pipe when the whole warp's arguments are in range
+      bool poly = false;
+      if constexpr (METHOD == CAPATTN_CAP_TANH)
+        poly = __all_sync(0xFFFFFFFFu, fmaxf(vmax, -vmin) * fabsf(xf.in) <= kTanhPolyMaxU);
       m_true = fmaxf(m_true, x_max);
       const float m_new = fmaxf(m_use, x_max);
       const bool resc = m_new > m_use + kRescaleThreshold;
@@ -360,18 +430,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll 1
         for (int c = 0; c < 4; c += 2) {
           tmem_ld32(s_base + (c + 1) * 32, vb);
-          if (fast)
-            psum += p_chunk<METHOD, false>(va, pk, xf, rmul, addm, k0 + c * 32, ri, any);
-          else
-            psum += p_chunk<METHOD, true>(va, pk, xf, rmul, addm, k0 + c * 32, ri, any);
+          psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, rmul, addm, k0 + c * 32, ri, any);
           __syncwarp();
           tmem_st16(s_base + c * 16, pk);
           tmem_wait_ld();
           if (c + 2 < 4) tmem_ld32(s_base + (c + 2) * 32, va);
-          if (fast)
-            psum += p_chunk<METHOD, false>(vb, pk, xf, rmul, addm, k0 + (c + 1) * 32, ri, any);
-          else
-            psum += p_chunk<METHOD, true>(vb, pk, xf, rmul, addm, k0 + (c + 1) * 32, ri, any);
+          psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, rmul, addm, k0 + (c + 1) * 32, ri, any);
           __syncwarp();
           tmem_st16(s_base + (c + 1) * 16, pk);
           tmem_wait_ld();
@@ -420,9 +484,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (p.l) p.l[rr] = live ? lsum * ex2_approx(m_use - m_true) : 0.f;
     }
   }
+  __syncwarp();  // warps 0 and 1 reach the CTA barrier converged
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    // Every MMA has completed before TMEM is released (normally already
+    // observed by the consumer warps; bounded non-suspending poll).
+    if (lane == 0 && n > 0) mbar_poll(bar_final, 0);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -115,4 +115,53 @@ __device__ __forceinline__ float cap_f_d(float X, const Xf& xf, float* d) {
   }
 }
 
+// ---------------------------------------------------------------- packed fp32
+// Two fp32 lanes in one 64-bit register pair (fma/mul/add .f32x2).
+struct F2 {
+  unsigned long long v;
+};
+__device__ __forceinline__ F2 f2(float a, float b) {
+  F2 r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r.v) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(F2 x, float& a, float& b) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(x.v));
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+
+// ---------------------------------------------------------------- tanh on the FMA pipe
+// tanh(u) = u + u^3 (c0 + w (c1 + w (c2 + w c3))), w = u^2, for |u| <= 0.5:
+// coefficients from csrc/fit_tanh_poly.py (max |error| 2.5e-8 in fp32, below
+// the tanh.approx instruction's error).  Kernels take this path only when a
+// whole warp's arguments are inside the range, and then split each chunk
+// between this FMA-pipe form and the MUFU instruction to balance the pipes.
+constexpr float kTanhPolyMaxU = 0.5f;
+constexpr float kTanhC0 = -0.333330512f;
+constexpr float kTanhC1 = 0.133239388f;
+constexpr float kTanhC2 = -0.0529243536f;
+constexpr float kTanhC3 = 0.0170059651f;
+
+__device__ __forceinline__ F2 tanh_poly2(F2 u) {
+  const F2 w = f2_mul(u, u);
+  F2 p = f2_fma(f2(kTanhC3, kTanhC3), w, f2(kTanhC2, kTanhC2));
+  p = f2_fma(p, w, f2(kTanhC1, kTanhC1));
+  p = f2_fma(p, w, f2(kTanhC0, kTanhC0));
+  return f2_fma(f2_mul(u, w), p, u);
+}
+
 }  // namespace capattn

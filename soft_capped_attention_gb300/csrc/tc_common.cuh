@@ -58,6 +58,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-suspending probe of a phase (mbarrier.test_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded busy poll with test_wait (for a thread that must not sleep inside
+// try_wait, e.g. one waiting for the arrival of its own tcgen05.commit).
+__device__ __forceinline__ void mbar_poll(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // sets the timeout bit in *status and in *abort) when the limit is reached or
 // another thread of the CTA already gave up.
