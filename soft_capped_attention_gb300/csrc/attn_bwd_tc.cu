@@ -7,22 +7,27 @@
 //   P_ij  = 2^(x - LSE_i * log2(e))                       (0 when masked)
 //   dX_ij = sm_scale * temp_i * cap'(s_ij) * P_ij * (dP_ij - delta_i + z * LSE_i)
 //
+// Both kernels cut every 128 x 128 step into two halves of 64 columns ("parts")
+// with their own TMEM buffers, so that one part's score MMAs of the next step
+// run on the tensor pipe while the elementwise warps work on the other part:
+//   MMA order:  ... | acc(j, 0)  S/dP(j+1, 0) | acc(j, 1)  S/dP(j+1, 1) | ...
+//   elementwise:        part 1 of step j       |   part 0 of step j+1
+// TMEM: part 0 scores [0, 64), part 0 dP [64, 128), part 1 scores [128, 192),
+// part 1 dP [192, 256), accumulators from 256.  Each elementwise warpgroup
+// owns 32 columns of a part; its packed bf16 results overwrite score / dP
+// columns it has already read, and the part is handed to the MMA issuer once
+// both warpgroups arrive.
+//
 // dK/dV: one CTA per (batch, KV head, 128-key tile).  K and V stay in shared
 // memory; the CTA loops over the query heads of its GQA group and the query
 // tiles of the tile's visit map, accumulating dK and dV in TMEM (the group sum
-// happens in place, no reduction pass).  Per step:
-//   S^T  = K Q^T, dP^T = V dO^T            (SS MMAs, M = keys, N = queries)
-//   elementwise by two warpgroups, each owning 64 query columns in two chunks
-//   of 32; each chunk's P^T and dX^T go back into TMEM as packed bf16 over
-//   already-consumed columns of the warpgroup's own S^T / dP^T region, and the
-//   chunk is handed to the MMA issuer at once:
-//   dV += P^T dO, dK += dX^T Q             (TS MMAs, K = 32 per chunk)
-// so the tensor pipe works on the first chunks while later ones are computed.
-// TMEM: S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512).
+// happens in place).  Per part: S^T = K Q_part^T, dP^T = V dO_part^T (SS MMAs,
+// M = keys, N = 64 queries); dV += P^T dO_part, dK += dX^T Q_part (TS MMAs,
+// K = 64).  TMEM: dV [256, 384), dK [384, 512).
 //
 // dQ: one CTA per (batch, query head, 128-query tile), looping over the KV
-// tiles of its visit map: S = Q K^T, dP = dO V^T, then dQ += dX K chunk by
-// chunk.  TMEM: S [0,128), dP [128,256), dQ [256,384).
+// tiles of its visit map.  Per part: S = Q K_part^T, dP = dO V_part^T (N = 64
+// keys); dQ += dX K_part (K = 64).  TMEM: dQ [256, 384).
 //
 // Warp roles in both kernels (10 warps): warp 0 TMA producer, warp 1 TMEM
 // allocator and MMA issuer, warps 2..5 and 6..9 the two elementwise
@@ -64,22 +69,30 @@ __device__ __forceinline__ void store_zero_bf16(__nv_bfloat16* dst) {
   for (int e = 0; e < 4; ++e) d4[e] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-__device__ __forceinline__ void issue_ss128(uint32_t d, uint32_t sA, uint32_t sB) {
-  constexpr uint32_t idesc = idesc_bf16(BT, BT, 0, 0);
+// Scores of one part: D[128 x 64] = A[128 x 128] B_part^T, both K-major; the
+// part's 64 rows of B start at row 64 * part of the staged tile.
+__device__ __forceinline__ void issue_scores_part(uint32_t d, uint32_t sA, uint32_t sB, int part) {
+  constexpr uint32_t idesc = idesc_bf16(BT, 64, 0, 0);
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks) {
     const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-    mma_ss(d, smem_desc(sA + off, 16, 1024), smem_desc(sB + off, 16, 1024), idesc, ks > 0);
+    mma_ss(d, smem_desc(sA + off, 16, 1024), smem_desc(sB + off + part * 64 * 128, 16, 1024), idesc,
+           ks > 0);
   }
 }
 
-// D += A[tmem cols a0 .. a0 + 16) x B rows [r0, r0 + 32) (MN-major B, N = 128): one chunk.
-__device__ __forceinline__ void issue_chunk(uint32_t d, uint32_t a0, uint32_t sB, int r0, bool first) {
+// TMEM column (within a part's score or dP buffer) of the packed bf16 values
+// for the part's columns [16 ks, 16 ks + 16): warpgroup ks / 2, sub-chunk ks % 2.
+__device__ __forceinline__ uint32_t packed_col(int ks) { return (uint32_t)(32 * (ks >> 1) + 8 * (ks & 1)); }
+
+// D[128 x 128] += A (packed bf16 in TMEM, 64 columns of the part) x B rows
+// [64 part, 64 part + 64) (MN-major, N = 128).
+__device__ __forceinline__ void issue_acc_part(uint32_t d, uint32_t a_base, uint32_t sB, int part, bool first) {
   constexpr uint32_t idesc = idesc_bf16(BT, HD, 0, 1);
 #pragma unroll
-  for (int kk = 0; kk < 2; ++kk)
-    mma_ts(d, a0 + kk * 8, smem_desc(sB + (r0 + 16 * kk) * 128, SLAB, 1024), idesc,
-           (first && kk == 0) ? 0u : 1u);
+  for (int ks = 0; ks < 4; ++ks)
+    mma_ts(d, a_base + packed_col(ks), smem_desc(sB + (64 * part + 16 * ks) * 128, SLAB, 1024), idesc,
+           (first && ks == 0) ? 0u : 1u);
 }
 
 // Steps of the dK/dV kernel: (query head of the group) x (visited query tile).
@@ -162,11 +175,11 @@ __device__ __forceinline__ void bwd_pair(float X0, float X1, float dp0, float dp
 }
 
 // dK/dV elementwise on 16 query columns (col0 .. col0 + 15) of key row jrow:
-// P^T and dX^T packed to bf16 and stored at TMEM columns dst (P) and 128 + dst (dX).
+// P^T and dX^T packed to bf16 and stored at TMEM addresses p_dst and x_dst.
 template <int METHOD, bool MASKED, bool POLY>
 __device__ __forceinline__ void dkv_sub_impl(const uint32_t (&sv)[16], const uint32_t (&dp)[16],
                                              const float4* colc, const int4* coli, int col0,
-                                             int jrow, const Xf& xf, uint32_t lane_base, int dst) {
+                                             int jrow, const Xf& xf, uint32_t p_dst, uint32_t x_dst) {
   uint32_t pp[8], px[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -190,58 +203,48 @@ __device__ __forceinline__ void dkv_sub_impl(const uint32_t (&sv)[16], const uin
     pp[e] = pack_bf16x2(P0, P1);
     px[e] = pack_bf16x2(x0, x1);
   }
-  tmem_st8(lane_base + dst, pp);
-  tmem_st8(lane_base + 128u + dst, px);
+  tmem_st8(p_dst, pp);
+  tmem_st8(x_dst, px);
 }
 
 // dK/dV elementwise on 16 query columns (col0 .. col0 + 15) of key row jrow:
-// P^T and dX^T packed to bf16 and stored at TMEM columns dst (P) and 128 + dst (dX).
+// P^T and dX^T packed to bf16 and stored at TMEM addresses p_dst and x_dst.
 // For the tanh cap the warp votes on whether all its arguments are small enough
 // for the FMA-pipe polynomial.
 template <int METHOD, bool MASKED>
 __device__ __forceinline__ void dkv_sub(const uint32_t (&sv)[16], const uint32_t (&dp)[16],
                                         const float4* colc, const int4* coli, int col0, int jrow,
-                                        const Xf& xf, uint32_t lane_base, int dst) {
+                                        const Xf& xf, uint32_t p_dst, uint32_t x_dst) {
   if constexpr (METHOD == CAPATTN_CAP_TANH) {
     float am = 0.f;
 #pragma unroll
     for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(__uint_as_float(sv[e])));
     if (__all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU)) {
-      dkv_sub_impl<METHOD, MASKED, true>(sv, dp, colc, coli, col0, jrow, xf, lane_base, dst);
+      dkv_sub_impl<METHOD, MASKED, true>(sv, dp, colc, coli, col0, jrow, xf, p_dst, x_dst);
       return;
     }
   }
-  dkv_sub_impl<METHOD, MASKED, false>(sv, dp, colc, coli, col0, jrow, xf, lane_base, dst);
+  dkv_sub_impl<METHOD, MASKED, false>(sv, dp, colc, coli, col0, jrow, xf, p_dst, x_dst);
 }
 
-// One warpgroup's 64 query columns of a step, in four sub-chunks of 16 with
-// the next sub-chunk's TMEM loads in flight while one is computed; the MMA
-// issuer is signalled after each half (32 columns).
+// One warpgroup's 32 columns of one part: two sub-chunks of 16, the second
+// one's TMEM loads in flight while the first is computed.
 template <int METHOD, bool MASKED>
-__device__ __forceinline__ void dkv_step(const float4* colc, const int4* coli, int wg, int jrow,
-                                         const Xf& xf, uint32_t lane_base, uint32_t bar_ew, int lane) {
+__device__ __forceinline__ void dkv_part(const float4* colc, const int4* coli, int wg, int part,
+                                         int jrow, const Xf& xf, uint32_t lane_base) {
+  const uint32_t sbuf = lane_base + 128u * part, dbuf = sbuf + 64u;
+  const int pc0 = 32 * wg;              // first column within the part
+  const int col0 = 64 * part + pc0;     // first query column within the tile
   uint32_t sa[16], da[16], sb[16], db[16];
-  const int c0 = 64 * wg;
-  tmem_ld16(lane_base + c0, sa);
-  tmem_ld16(lane_base + 128u + c0, da);
+  tmem_ld16(sbuf + pc0, sa);
+  tmem_ld16(dbuf + pc0, da);
   tmem_wait_ld();
-#pragma unroll 1
-  for (int k = 0; k < 4; k += 2) {
-    tmem_ld16(lane_base + c0 + 16 * (k + 1), sb);
-    tmem_ld16(lane_base + 128u + c0 + 16 * (k + 1), db);
-    dkv_sub<METHOD, MASKED>(sa, da, colc, coli, c0 + 16 * k, jrow, xf, lane_base, c0 + 8 * k);
-    tmem_wait_ld();
-    if (k + 2 < 4) {
-      tmem_ld16(lane_base + c0 + 16 * (k + 2), sa);
-      tmem_ld16(lane_base + 128u + c0 + 16 * (k + 2), da);
-    }
-    dkv_sub<METHOD, MASKED>(sb, db, colc, coli, c0 + 16 * (k + 1), jrow, xf, lane_base, c0 + 8 * (k + 1));
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + (k >> 1)));
-    tmem_wait_ld();
-  }
+  tmem_ld16(sbuf + pc0 + 16, sb);
+  tmem_ld16(dbuf + pc0 + 16, db);
+  dkv_sub<METHOD, MASKED>(sa, da, colc, coli, col0, jrow, xf, sbuf + pc0, dbuf + pc0);
+  tmem_wait_ld();
+  dkv_sub<METHOD, MASKED>(sb, db, colc, coli, col0 + 16, jrow, xf, sbuf + pc0 + 8, dbuf + pc0 + 8);
+  tmem_wait_st();
 }
 
 // dQ elementwise on 32 key columns (absolute j0 .. j0 + 31) of query row (span
@@ -324,8 +327,8 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const uint32_t bar_kv = smem_u32(&bars[0]);
   const uint32_t bar_full = smem_u32(&bars[1]);    // + s*8 (Q and dO)
   const uint32_t bar_empty = smem_u32(&bars[3]);   // + s*8
-  const uint32_t bar_sdp = smem_u32(&bars[5]);
-  const uint32_t bar_ew = smem_u32(&bars[6]);      // + (2*wg + chunk)*8
+  const uint32_t bar_sdp = smem_u32(&bars[5]);     // + part*8: scores of the part ready
+  const uint32_t bar_ew = smem_u32(&bars[7]);      // + part*8: part's P / dX written
   const uint32_t bar_final = smem_u32(&bars[10]);
   const uint32_t bar_cfull = smem_u32(&bars[11]);  // + (2*wg + cb)*8: column constants written
   const uint32_t bar_cfree = smem_u32(&bars[15]);  // + (2*wg + cb)*8: column constants consumed
@@ -338,9 +341,11 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_sdp, 1);
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(bar_sdp + 8 * c, 1);
+      mbar_init(bar_ew + 8 * c, 8);
+    }
     for (int c = 0; c < 4; ++c) {
-      mbar_init(bar_ew + 8 * c, 4);
       mbar_init(bar_cfull + 8 * c, 128);
       mbar_init(bar_cfree + 8 * c, 128);
     }
@@ -367,22 +372,19 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       tma_load_4d(sK + SLAB, &mk, bar_kv, 64, g, k0, b);
       tma_load_4d(sV, &mv, bar_kv, 0, g, k0, b);
       tma_load_4d(sV + SLAB, &mv, bar_kv, 64, g, k0, b);
-      int j = 0;
-      for (int hh = 0; hh < p.G && !abort_flag; ++hh) {
+      StepIter st(map, p.wq, p.G);
+      int hh, qt, j = 0;
+      while (!abort_flag && st.next(hh, qt)) {
         const int h = g * p.G + hh;
-        TileIter it(map, p.wq);
-        int qt;
-        while (it.next(qt)) {
-          const int s = j % NSTAGE, u = j / NSTAGE;
-          if (u > 0 && !mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
-          const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
-          mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
-          tma_load_4d(sQ, &mq, bar_full + 8 * s, 0, h, qt * BT, b);
-          tma_load_4d(sQ + SLAB, &mq, bar_full + 8 * s, 64, h, qt * BT, b);
-          tma_load_4d(sO, &mdo, bar_full + 8 * s, 0, h, qt * BT, b);
-          tma_load_4d(sO + SLAB, &mdo, bar_full + 8 * s, 64, h, qt * BT, b);
-          ++j;
-        }
+        const int s = j % NSTAGE, u = j / NSTAGE;
+        if (u > 0 && !mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
+        const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
+        mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
+        tma_load_4d(sQ, &mq, bar_full + 8 * s, 0, h, qt * BT, b);
+        tma_load_4d(sQ + SLAB, &mq, bar_full + 8 * s, 64, h, qt * BT, b);
+        tma_load_4d(sO, &mdo, bar_full + 8 * s, 0, h, qt * BT, b);
+        tma_load_4d(sO + SLAB, &mdo, bar_full + 8 * s, 64, h, qt * BT, b);
+        ++j;
       }
       drain_wait(bar_kv, 0);
       for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj)
@@ -390,52 +392,66 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      bool ok = mbar_wait(bar_kv, 0, p.status, &abort_flag);
-      for (int j = 0; ok && j < n; ++j) {
-        const int s = j % NSTAGE, u = j / NSTAGE;
-        if (!mbar_wait(bar_full + 8 * s, u & 1, p.status, &abort_flag)) break;
+      // scores of part `part` of step j into that part's TMEM buffer
+      auto scores = [&](int j, int part) {
+        const uint32_t sQ = sQD + (j % NSTAGE) * 2 * TILE, sO = sQ + TILE;
+        issue_scores_part(tmem + 128u * part, sK, sQ, part);         // S^T  = K Q^T
+        issue_scores_part(tmem + 128u * part + 64u, sV, sO, part);   // dP^T = V dO^T
+        mma_commit(bar_sdp + 8 * part);
+      };
+      bool ok = mbar_wait(bar_kv, 0, p.status, &abort_flag) &&
+                mbar_wait(bar_full, 0, p.status, &abort_flag);
+      if (ok) {
         tc_fence_after();
+        scores(0, 0);
+        scores(0, 1);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j % NSTAGE;
         const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
-        issue_ss128(tmem, sK, sQ);          // S^T  = K Q^T
-        issue_ss128(tmem + 128u, sV, sO);   // dP^T = V dO^T
-        mma_commit(bar_sdp);
-        // chunk order: (wg0, c0), (wg1, c0), (wg0, c1), (wg1, c1)
-        for (int q = 0; q < 4 && ok; ++q) {
-          const int wg = q & 1, c = q >> 1;
-          if (!mbar_wait(bar_ew + 8 * (2 * wg + c), j & 1, p.status, &abort_flag)) {
+        const bool more = j + 1 < n;
+        for (int part = 0; part < 2; ++part) {
+          if (!mbar_wait(bar_ew + 8 * part, j & 1, p.status, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t col = (uint32_t)(64 * wg + 16 * c);
-          const int r0 = 64 * wg + 32 * c;
-          const bool first = (j == 0) && (q == 0);
-          issue_chunk(tmem + 256u, tmem + col, sO, r0, first);          // dV += P^T dO
-          issue_chunk(tmem + 384u, tmem + 128u + col, sQ, r0, first);   // dK += dX^T Q
+          const bool first = (j == 0) && (part == 0);
+          issue_acc_part(tmem + 256u, tmem + 128u * part, sO, part, first);         // dV += P^T dO
+          issue_acc_part(tmem + 384u, tmem + 128u * part + 64u, sQ, part, first);   // dK += dX^T Q
+          if (part == 1) mma_commit(bar_empty + 8 * s);
+          if (more) {
+            if (part == 0 &&
+                !mbar_wait(bar_full + 8 * ((j + 1) % NSTAGE), ((j + 1) / NSTAGE) & 1, p.status,
+                           &abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            scores(j + 1, part);
+          }
         }
-        if (!ok) break;
-        mma_commit(bar_empty + 8 * s);
       }
-      // The MMA thread does not wait for its own commit here: the consumer
-      // warps wait for it, and warp 1 re-checks it before freeing TMEM.
+      // No wait for this commit here: the consumer warps wait for it, and
+      // warp 1 re-checks it before freeing TMEM.
       mma_commit(bar_final);
     }
   } else {
-    const int wg = (warp - 2) >> 2;        // query columns [64 wg, 64 wg + 64)
+    const int wg = (warp - 2) >> 2;        // 32 columns of each part
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;     // key row within the tile (TMEM lane)
     const int tid = (warp - 2 - 4 * wg) * 32 + lane;  // 0..127 within the warpgroup
     const int jrow = k0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
-    const float zw = p.z_loss_weight;
+    // query column whose constants this thread loads: the warpgroup's 32
+    // columns of part 0 and of part 1
+    const int my_col = (tid < 32) ? 32 * wg + tid : 64 + 32 * wg + (tid - 32);
     bool aborted = false;
-    // Raw column constants are loaded one step ahead (their global-load latency
-    // hides behind a whole step of work).
     StepIter nx(map, p.wq, p.G);
     int nh = 0, nqt = 0;
     bool have_next = nx.next(nh, nqt);
-    ColRaw cur = load_col_raw(p, b, g * p.G + nh, nqt, 64 * wg + tid, have_next && tid < 64);
+    ColRaw cur = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have_next && tid < 64);
     int cur_qt = nqt;
     for (int step = 0; step < n && have_next; ++step) {
       const int cb = step & 1, cu = step >> 1;
@@ -446,28 +462,36 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         break;
       }
       if (tid < 64) {
-        const int c = 64 * wg + tid;
         float mul, add;
         row_consts<METHOD>(p.cap, p.sm_scale, cur.temp, &mul, &add);
-        colc[cb][c] = make_float4(mul, add - cur.lse2, row_dscale<METHOD>(p.cap, p.sm_scale, cur.temp),
-                                  cur.radd);
-        coli[cb][c] = cur.ri;
+        colc[cb][my_col] = make_float4(mul, add - cur.lse2,
+                                       row_dscale<METHOD>(p.cap, p.sm_scale, cur.temp), cur.radd);
+        coli[cb][my_col] = cur.ri;
       }
       mbar_arrive(my_cfull);
       const int2 fr = p.qfull[(size_t)b * p.nq + cur_qt];
       const bool tile_full = (kt >= fr.x) && (kt < fr.y);
       have_next = nx.next(nh, nqt);
-      const ColRaw nxt = load_col_raw(p, b, g * p.G + nh, nqt, 64 * wg + tid, have_next && tid < 64);
-      if (!mbar_wait_warp(my_cfull, cu & 1, p.status, &abort_flag) ||
-          !mbar_wait_warp(bar_sdp, step & 1, p.status, &abort_flag)) {
+      const ColRaw nxt = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have_next && tid < 64);
+      if (!mbar_wait_warp(my_cfull, cu & 1, p.status, &abort_flag)) {
         aborted = true;
         break;
       }
-      tc_fence_after();
-      if (tile_full)
-        dkv_step<METHOD, false>(colc[cb], coli[cb], wg, jrow, xf, lane_base, bar_ew, lane);
-      else
-        dkv_step<METHOD, true>(colc[cb], coli[cb], wg, jrow, xf, lane_base, bar_ew, lane);
+      for (int part = 0; part < 2; ++part) {
+        if (!mbar_wait_warp(bar_sdp + 8 * part, step & 1, p.status, &abort_flag)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        if (tile_full)
+          dkv_part<METHOD, false>(colc[cb], coli[cb], wg, part, jrow, xf, lane_base);
+        else
+          dkv_part<METHOD, true>(colc[cb], coli[cb], wg, part, jrow, xf, lane_base);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ew + 8 * part);
+      }
+      if (aborted) break;
       mbar_arrive(my_cfree);
       cur = nxt;
       cur_qt = nqt;
@@ -532,8 +556,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   const uint32_t bar_q = smem_u32(&bars[0]);
   const uint32_t bar_full = smem_u32(&bars[1]);    // + s*8
   const uint32_t bar_empty = smem_u32(&bars[3]);   // + s*8
-  const uint32_t bar_sdp = smem_u32(&bars[5]);
-  const uint32_t bar_ew = smem_u32(&bars[6]);      // + (2*wg + chunk)*8
+  const uint32_t bar_sdp = smem_u32(&bars[5]);     // + part*8
+  const uint32_t bar_ew = smem_u32(&bars[7]);      // + part*8
   const uint32_t bar_final = smem_u32(&bars[10]);
 
   const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
@@ -544,8 +568,10 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_sdp, 1);
-    for (int c = 0; c < 4; ++c) mbar_init(bar_ew + 8 * c, 4);
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(bar_sdp + 8 * c, 1);
+      mbar_init(bar_ew + 8 * c, 8);
+    }
     mbar_init(bar_final, 1);
     fence_mbar_init();
   }
@@ -587,34 +613,47 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      bool ok = mbar_wait(bar_q, 0, p.status, &abort_flag);
-      for (int j = 0; ok && j < n; ++j) {
-        const int s = j % NSTAGE, u = j / NSTAGE;
-        if (!mbar_wait(bar_full + 8 * s, u & 1, p.status, &abort_flag)) break;
+      auto scores = [&](int j, int part) {
+        const uint32_t sK = sKV + (j % NSTAGE) * 2 * TILE, sV = sK + TILE;
+        issue_scores_part(tmem + 128u * part, sQ, sK, part);         // S  = Q K^T
+        issue_scores_part(tmem + 128u * part + 64u, sO, sV, part);   // dP = dO V^T
+        mma_commit(bar_sdp + 8 * part);
+      };
+      bool ok = mbar_wait(bar_q, 0, p.status, &abort_flag) &&
+                mbar_wait(bar_full, 0, p.status, &abort_flag);
+      if (ok) {
         tc_fence_after();
-        const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
-        issue_ss128(tmem, sQ, sK);          // S  = Q K^T
-        issue_ss128(tmem + 128u, sO, sV);   // dP = dO V^T
-        mma_commit(bar_sdp);
-        for (int q = 0; q < 4 && ok; ++q) {
-          const int wg = q & 1, c = q >> 1;
-          if (!mbar_wait(bar_ew + 8 * (2 * wg + c), j & 1, p.status, &abort_flag)) {
+        scores(0, 0);
+        scores(0, 1);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j % NSTAGE;
+        const uint32_t sK = sKV + s * 2 * TILE;
+        const bool more = j + 1 < n;
+        for (int part = 0; part < 2; ++part) {
+          if (!mbar_wait(bar_ew + 8 * part, j & 1, p.status, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t col = (uint32_t)(64 * wg + 16 * c);
-          issue_chunk(tmem + 256u, tmem + col, sK, 64 * wg + 32 * c, (j == 0) && (q == 0));
+          issue_acc_part(tmem + 256u, tmem + 128u * part + 64u, sK, part, (j == 0) && (part == 0));
+          if (part == 1) mma_commit(bar_empty + 8 * s);
+          if (more) {
+            if (part == 0 &&
+                !mbar_wait(bar_full + 8 * ((j + 1) % NSTAGE), ((j + 1) / NSTAGE) & 1, p.status,
+                           &abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            scores(j + 1, part);
+          }
         }
-        if (!ok) break;
-        mma_commit(bar_empty + 8 * s);
       }
-      // The MMA thread does not wait for its own commit here: the consumer
-      // warps wait for it, and warp 1 re-checks it before freeing TMEM.
       mma_commit(bar_final);
     }
   } else {
-    const int wg = (warp - 2) >> 2;        // key columns [64 wg, 64 wg + 64)
+    const int wg = (warp - 2) >> 2;        // 32 key columns of each part
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int i = q0 + r;
@@ -634,39 +673,32 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const float radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
     bool aborted = false;
     TileIter it(map, p.wk);
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < n && !aborted; ++j) {
       int t;
       it.next(t);
       const int k0 = t * BT;
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BT);
-      if (!mbar_wait_warp(bar_sdp, j & 1, p.status, &abort_flag)) {
-        aborted = true;
-        break;
+      for (int part = 0; part < 2; ++part) {
+        if (!mbar_wait_warp(bar_sdp + 8 * part, j & 1, p.status, &abort_flag)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sbuf = lane_base + 128u * part, dbuf = sbuf + 64u;
+        const int pc0 = 32 * wg;
+        uint32_t sv[32], dp[32], px[16];
+        tmem_ld32(sbuf + pc0, sv);
+        tmem_ld32(dbuf + pc0, dp);
+        tmem_wait_ld();
+        dq_dispatch<METHOD>(full, sv, dp, k0 + 64 * part + pc0, ri, xf, mul, addl, dscale, radd, px);
+        __syncwarp();
+        // packed dX of columns [pc0, pc0 + 32): 16 columns at dbuf + pc0
+        tmem_st16(dbuf + pc0, px);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ew + 8 * part);
       }
-      tc_fence_after();
-      uint32_t sa[32], da[32], sb[32], db[32];
-      const int colA = 64 * wg, colB = 64 * wg + 32;
-      tmem_ld32(lane_base + colA, sa);
-      tmem_ld32(lane_base + 128u + colA, da);
-      tmem_wait_ld();
-      tmem_ld32(lane_base + colB, sb);
-      tmem_ld32(lane_base + 128u + colB, db);
-      uint32_t px[16];
-      dq_dispatch<METHOD>(full, sa, da, k0 + colA, ri, xf, mul, addl, dscale, radd, px);
-      __syncwarp();
-      tmem_st16(lane_base + 64 * wg, px);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + 0));
-      tmem_wait_ld();
-      dq_dispatch<METHOD>(full, sb, db, k0 + colB, ri, xf, mul, addl, dscale, radd, px);
-      __syncwarp();
-      tmem_st16(lane_base + 64 * wg + 16, px);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ew + 8 * (2 * wg + 1));
     }
     bool have = false;
     if (n > 0 && !aborted) {
@@ -692,8 +724,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    // Every MMA has completed before TMEM is released (normally already
-    // observed by the consumer warps; bounded non-suspending poll).
     if (lane == 0 && n > 0) mbar_poll(bar_final, 0);
     __syncwarp();
     tc_fence_after();
