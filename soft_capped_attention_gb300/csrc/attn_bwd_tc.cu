@@ -7,31 +7,29 @@
 //   P_ij  = 2^(x - LSE_i * log2(e))                       (0 when masked)
 //   dX_ij = sm_scale * temp_i * cap'(s_ij) * P_ij * (dP_ij - delta_i + z * LSE_i)
 //
-// Both kernels cut every 128 x 128 step into two halves of 64 columns ("parts")
-// with their own TMEM buffers, so that one part's score MMAs of the next step
-// run on the tensor pipe while the elementwise warps work on the other part:
-//   MMA order:  ... | acc(j, 0)  S/dP(j+1, 0) | acc(j, 1)  S/dP(j+1, 1) | ...
-//   elementwise:        part 1 of step j       |   part 0 of step j+1
-// TMEM: part 0 scores [0, 64), part 0 dP [64, 128), part 1 scores [128, 192),
-// part 1 dP [192, 256), accumulators from 256.  Each elementwise warpgroup
-// owns 32 columns of a part; its packed bf16 results overwrite score / dP
-// columns it has already read, and the part is handed to the MMA issuer once
-// both warpgroups arrive.
+// Both kernels work in 128 x 128 steps with four tcgen05 phases per step:
+// score MMAs (S and dP, N = 128, separately committed), the elementwise pass,
+// and the accumulation MMAs, handed over in 16-column chunks as the
+// elementwise warps finish them.  The elementwise warps copy their S columns
+// to registers first and release them, so the next step's S MMAs run during
+// this step's elementwise pass; P / dX are packed to bf16 over the dP columns
+// already read, and the next step's dP MMAs follow the last chunk.
 //
 // dK/dV: one CTA per (batch, KV head, 128-key tile).  K and V stay in shared
 // memory; the CTA loops over the query heads of its GQA group and the query
 // tiles of the tile's visit map, accumulating dK and dV in TMEM (the group sum
-// happens in place).  Per part: S^T = K Q_part^T, dP^T = V dO_part^T (SS MMAs,
-// M = keys, N = 64 queries); dV += P^T dO_part, dK += dX^T Q_part (TS MMAs,
-// K = 64).  TMEM: dV [256, 384), dK [384, 512).
+// happens in place): S^T = K Q^T, dP^T = V dO^T (SS MMAs, M = keys); dV += P^T
+// dO, dK += dX^T Q (TS MMAs).  TMEM: S^T [0, 128), dP^T [128, 256), dV
+// [256, 384), dK [384, 512).
 //
 // dQ: one CTA per (batch, query head, 128-query tile), looping over the KV
-// tiles of its visit map.  Per part: S = Q K_part^T, dP = dO V_part^T (N = 64
-// keys); dQ += dX K_part (K = 64).  TMEM: dQ [256, 384).
+// tiles of its visit map: S = Q K^T, dP = dO V^T; dQ += dX K (TS MMAs).  TMEM:
+// S [0, 128), dP [128, 256), dQ [256, 384).
 //
 // Warp roles in both kernels (10 warps): warp 0 TMA producer, warp 1 TMEM
-// allocator and MMA issuer, warps 2..5 and 6..9 the two elementwise
-// warpgroups (one TMEM lane = one tile row each).
+// allocator and MMA issuer (both run their loops warp-wide; one elected lane
+// issues), warps 2..5 and 6..9 the two elementwise warpgroups (one TMEM lane =
+// one tile row each; each warpgroup owns 64 columns).
 #include <math.h>
 
 #include "cap_math.cuh"
@@ -51,8 +49,6 @@ constexpr int TILE = 2 * SLAB;
 constexpr int NSTAGE = 2;
 constexpr int NTHREADS = 320;
 constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
-constexpr int kBwdPolyPairs = 10;  // of 16 column pairs in a dQ chunk: tanh on the FMA pipe
-constexpr int kDkvPolyPairs = 5;   // of 8 column pairs in a dK/dV sub-chunk
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
   uint32_t pk[16];
@@ -67,32 +63,6 @@ __device__ __forceinline__ void store_zero_bf16(__nv_bfloat16* dst) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int e = 0; e < 4; ++e) d4[e] = make_uint4(0u, 0u, 0u, 0u);
-}
-
-// Scores of one part: D[128 x 64] = A[128 x 128] B_part^T, both K-major; the
-// part's 64 rows of B start at row 64 * part of the staged tile.
-__device__ __forceinline__ void issue_scores_part(uint32_t d, uint32_t sA, uint32_t sB, int part) {
-  constexpr uint32_t idesc = idesc_bf16(BT, 64, 0, 0);
-#pragma unroll
-  for (int ks = 0; ks < HD / 16; ++ks) {
-    const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-    mma_ss(d, smem_desc(sA + off, 16, 1024), smem_desc(sB + off + part * 64 * 128, 16, 1024), idesc,
-           ks > 0);
-  }
-}
-
-// TMEM column (within a part's score or dP buffer) of the packed bf16 values
-// for the part's columns [16 ks, 16 ks + 16): warpgroup ks / 2, sub-chunk ks % 2.
-__device__ __forceinline__ uint32_t packed_col(int ks) { return (uint32_t)(32 * (ks >> 1) + 8 * (ks & 1)); }
-
-// D[128 x 128] += A (packed bf16 in TMEM, 64 columns of the part) x B rows
-// [64 part, 64 part + 64) (MN-major, N = 128).
-__device__ __forceinline__ void issue_acc_part(uint32_t d, uint32_t a_base, uint32_t sB, int part, bool first) {
-  constexpr uint32_t idesc = idesc_bf16(BT, HD, 0, 1);
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks)
-    mma_ts(d, a_base + packed_col(ks), smem_desc(sB + (64 * part + 16 * ks) * 128, SLAB, 1024), idesc,
-           (first && ks == 0) ? 0u : 1u);
 }
 
 // Steps of the dK/dV kernel: (query head of the group) x (visited query tile).
@@ -114,41 +84,60 @@ struct StepIter {
   }
 };
 
-// Raw per-query-column inputs of one step (loaded ahead of use).
+// Raw per-query-column inputs of one step, loaded ahead of use and left
+// untouched until then (arithmetic on them here would stall on the loads).
 struct ColRaw {
-  float lse2, radd, temp;
+  float lse, dl, temp;
   int4 ri;
 };
 
 __device__ __forceinline__ ColRaw load_col_raw(const Params& p, int b, int h, int qt, int c, bool active) {
   ColRaw r;
-  r.lse2 = 0.f;
-  r.radd = 0.f;
+  r.lse = -INFINITY;
+  r.dl = 0.f;
   r.temp = 1.f;
   r.ri = make_int4(0, 0, -1, 0);
   const int i = qt * BT + c;
   if (active && i < p.L) {
     const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
-    const float lse = p.lse[rr];
-    const float dl = p.delta[rr];
-    const bool fin = isfinite(lse);
-    r.lse2 = fin ? lse * kL2E : 0.f;
-    r.radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
+    r.lse = p.lse[rr];
+    r.dl = p.delta[rr];
     if (p.temp) r.temp = p.temp[(size_t)b * p.L + i];
     r.ri = p.rowinfo[(size_t)b * p.L + i];
   }
   return r;
 }
 
-// Backward elementwise on a pair of scores: P = 2^(mul * f + add) (0 when
-// masked) and dX = dscale * f' * P * (dP + radd), with packed fp32x2 math.  For
-// the tanh cap with POLY, tanh is evaluated on the FMA pipe (the caller
-// guarantees |X * in| <= 0.5 for the whole warp).
+// ======================================================================= dK / dV
+// Score MMAs of a whole step: D[128 x 128] = A[128 x 128] B^T, both K-major,
+// from the tiles' descriptors.
+__device__ __forceinline__ void issue_scores(uint32_t d, uint64_t dA, uint64_t dB) {
+  constexpr uint32_t idesc = idesc_bf16(BT, BT, 0, 0);
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
+    mma_ss(d, desc_add(dA, off), desc_add(dB, off), idesc, ks > 0 ? 1u : 0u);
+  }
+}
+
+// Per-step constants of a pair of query columns (c, c + 1), each half of a float4
+// being one packed f32x2 operand:
+//   a = (mul_c, mul_c+1, addl_c, addl_c+1)         x = mul * f + addl  (log2 domain, LSE folded in)
+//   b = (ndsc_c, ndsc_c+1, ndr_c, ndr_c+1)         ndsc = -dscale, ndr = -dscale * radd
+struct ColPair {
+  float4 a, b;
+};
+
+// P and dX of one pair of scores of a key row, packed to bf16:
+//   P  = 2^(mul f(X) + addl)                        (0 where masked)
+//   dX = dscale f'(X) P (dP + radd) = (-f') P (ndsc dP + ndr)
+// For the tanh cap, -f' = f^2 - 1; with POLY, tanh runs on the FMA pipe (the
+// caller guarantees |X in| <= 0.5 for the whole warp).
 template <int METHOD, bool POLY>
-__device__ __forceinline__ void bwd_pair(float X0, float X1, float dp0, float dp1, const Xf& xf,
-                                         F2 mul, F2 add, F2 dsc, F2 radd, bool l0, bool l1,
-                                         float& P0, float& P1, float& dX0, float& dX1) {
-  F2 f, d;
+__device__ __forceinline__ void dkv_pair(float X0, float X1, float dp0, float dp1, const Xf& xf,
+                                         const ColPair& c, bool l0, bool l1, uint32_t& pk,
+                                         uint32_t& xk) {
+  F2 f, e;
   if constexpr (METHOD == CAPATTN_CAP_TANH) {
     const F2 u = f2_mul(f2(X0, X1), f2(xf.in, xf.in));
     if constexpr (POLY) {
@@ -158,161 +147,105 @@ __device__ __forceinline__ void bwd_pair(float X0, float X1, float dp0, float dp
       f2_split(u, a, b);
       f = f2(tanh_approx(a), tanh_approx(b));
     }
-    d = f2_fma(f2_mul(f, f2(-1.f, -1.f)), f, f2(1.f, 1.f));
+    e = f2_fma(f, f, f2(-1.f, -1.f));
   } else {
     float d0, d1;
     const float f0 = cap_f_d<METHOD>(X0, xf, &d0);
     const float f1 = cap_f_d<METHOD>(X1, xf, &d1);
     f = f2(f0, f1);
-    d = f2(d0, d1);
+    e = f2(-d0, -d1);
   }
   float x0, x1;
-  f2_split(f2_fma(mul, f, add), x0, x1);
-  P0 = l0 ? ex2_approx(x0) : 0.f;
-  P1 = l1 ? ex2_approx(x1) : 0.f;
-  const F2 g = f2_mul(f2(P0, P1), f2_add(f2(dp0, dp1), radd));
-  f2_split(f2_mul(f2_mul(dsc, d), g), dX0, dX1);
+  f2_split(f2_fma(f2(c.a.x, c.a.y), f, f2(c.a.z, c.a.w)), x0, x1);
+  const float P0 = l0 ? ex2_approx(x0) : 0.f;
+  const float P1 = l1 ? ex2_approx(x1) : 0.f;
+  const F2 h = f2_fma(f2(dp0, dp1), f2(c.b.x, c.b.y), f2(c.b.z, c.b.w));
+  float g0, g1;
+  f2_split(f2_mul(e, f2_mul(f2(P0, P1), h)), g0, g1);
+  pk = pack_bf16x2(P0, P1);
+  xk = pack_bf16x2(g0, g1);
 }
 
-// dK/dV elementwise on 16 query columns (col0 .. col0 + 15) of key row jrow:
-// P^T and dX^T packed to bf16 and stored at TMEM addresses p_dst and x_dst.
-template <int METHOD, bool MASKED, bool POLY>
-__device__ __forceinline__ void dkv_sub_impl(const uint32_t (&sv)[16], const uint32_t (&dp)[16],
-                                             const float4* colc, const int4* coli, int col0,
-                                             int jrow, const Xf& xf, uint32_t p_dst, uint32_t x_dst) {
-  uint32_t pp[8], px[8];
+constexpr int kDkvPolyPairs = 5;  // of the 8 column pairs of a chunk: tanh on the FMA pipe
+
+// One 16-column chunk (columns 16 C .. 16 C + 15 of the warpgroup's 64) of a key
+// row: S values from the row's register copy, dP from dp.
+template <int METHOD, bool MASKED, bool POLY, int C>
+__device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_t (&dp)[16],
+                                          const ColPair* cp, const int4* ci, int jrow, const Xf& xf,
+                                          uint32_t (&pk)[8], uint32_t (&xk)[8]) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const int cc = col0 + 2 * e;
-    const float4 ka = colc[cc], kb = colc[cc + 1];
+    const ColPair c = cp[8 * C + e];
     bool l0 = true, l1 = true;
     if constexpr (MASKED) {
-      const int4 ca = coli[cc], cb = coli[cc + 1];
-      l0 = (jrow >= ca.x && jrow < ca.y) || jrow == ca.z;
-      l1 = (jrow >= cb.x && jrow < cb.y) || jrow == cb.z;
+      const int4 a = ci[16 * C + 2 * e], b = ci[16 * C + 2 * e + 1];
+      l0 = (jrow >= a.x && jrow < a.y) || jrow == a.z;
+      l1 = (jrow >= b.x && jrow < b.y) || jrow == b.z;
     }
-    float P0, P1, x0, x1;
-    const float X0 = __uint_as_float(sv[2 * e]), X1 = __uint_as_float(sv[2 * e + 1]);
+    const float X0 = __uint_as_float(s[16 * C + 2 * e]), X1 = __uint_as_float(s[16 * C + 2 * e + 1]);
     const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
     if (POLY && e < kDkvPolyPairs)
-      bwd_pair<METHOD, true>(X0, X1, d0, d1, xf, f2(ka.x, kb.x), f2(ka.y, kb.y), f2(ka.z, kb.z),
-                             f2(ka.w, kb.w), l0, l1, P0, P1, x0, x1);
+      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, c, l0, l1, pk[e], xk[e]);
     else
-      bwd_pair<METHOD, false>(X0, X1, d0, d1, xf, f2(ka.x, kb.x), f2(ka.y, kb.y), f2(ka.z, kb.z),
-                              f2(ka.w, kb.w), l0, l1, P0, P1, x0, x1);
-    pp[e] = pack_bf16x2(P0, P1);
-    px[e] = pack_bf16x2(x0, x1);
+      dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, c, l0, l1, pk[e], xk[e]);
   }
-  tmem_st8(p_dst, pp);
-  tmem_st8(x_dst, px);
 }
 
-// dK/dV elementwise on 16 query columns (col0 .. col0 + 15) of key row jrow:
-// P^T and dX^T packed to bf16 and stored at TMEM addresses p_dst and x_dst.
-// For the tanh cap the warp votes on whether all its arguments are small enough
-// for the FMA-pipe polynomial.
-template <int METHOD, bool MASKED>
-__device__ __forceinline__ void dkv_sub(const uint32_t (&sv)[16], const uint32_t (&dp)[16],
-                                        const float4* colc, const int4* coli, int col0, int jrow,
-                                        const Xf& xf, uint32_t p_dst, uint32_t x_dst) {
-  if constexpr (METHOD == CAPATTN_CAP_TANH) {
-    float am = 0.f;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(__uint_as_float(sv[e])));
-    if (__all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU)) {
-      dkv_sub_impl<METHOD, MASKED, true>(sv, dp, colc, coli, col0, jrow, xf, p_dst, x_dst);
-      return;
-    }
-  }
-  dkv_sub_impl<METHOD, MASKED, false>(sv, dp, colc, coli, col0, jrow, xf, p_dst, x_dst);
-}
-
-// One warpgroup's 32 columns of one part: two sub-chunks of 16, the second
-// one's TMEM loads in flight while the first is computed.
-template <int METHOD, bool MASKED>
-__device__ __forceinline__ void dkv_part(const float4* colc, const int4* coli, int wg, int part,
-                                         int jrow, const Xf& xf, uint32_t lane_base) {
-  const uint32_t sbuf = lane_base + 128u * part, dbuf = sbuf + 64u;
-  const int pc0 = 32 * wg;              // first column within the part
-  const int col0 = 64 * part + pc0;     // first query column within the tile
-  uint32_t sa[16], da[16], sb[16], db[16];
-  tmem_ld16(sbuf + pc0, sa);
-  tmem_ld16(dbuf + pc0, da);
-  tmem_wait_ld();
-  tmem_ld16(sbuf + pc0 + 16, sb);
-  tmem_ld16(dbuf + pc0 + 16, db);
-  dkv_sub<METHOD, MASKED>(sa, da, colc, coli, col0, jrow, xf, sbuf + pc0, dbuf + pc0);
-  tmem_wait_ld();
-  dkv_sub<METHOD, MASKED>(sb, db, colc, coli, col0 + 16, jrow, xf, sbuf + pc0 + 8, dbuf + pc0 + 8);
-  tmem_wait_st();
-}
-
-// dQ elementwise on 32 key columns (absolute j0 .. j0 + 31) of query row (span
-// ri): dX packed to bf16 into px.  (No TMEM access: callers branch per row.)
-// With POLY (tanh cap), column pairs [0, poly_pairs) use the FMA-pipe tanh.
+// The warpgroup's 64 columns of one step, chunk by chunk: dP of chunk C + 1 is
+// loaded while chunk C is computed; the packed P^T and dX^T of chunk C overwrite
+// its dP columns ([16 C, 16 C + 8) and [16 C + 8, 16 C + 16) of the warpgroup's
+// range) and the chunk is handed to the MMA issuer.
 template <int METHOD, bool MASKED, bool POLY>
-__device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_t (&dp)[32], int j0,
-                                         int4 ri, const Xf& xf, float mul, float addl, float dscale,
-                                         float radd, uint32_t (&px)[16]) {
-  const F2 mul2 = f2(mul, mul), add2 = f2(addl, addl), dsc2 = f2(dscale, dscale),
-           radd2 = f2(radd, radd);
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    bool l0 = true, l1 = true;
-    if constexpr (MASKED) {
-      const int ja = j0 + 2 * e, jb = ja + 1;
-      l0 = (ja >= ri.x && ja < ri.y) || ja == ri.z;
-      l1 = (jb >= ri.x && jb < ri.y) || jb == ri.z;
-    }
-    float P0, P1, x0, x1;
-    const float X0 = __uint_as_float(sv[2 * e]), X1 = __uint_as_float(sv[2 * e + 1]);
-    const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
-    if (POLY && e < kBwdPolyPairs)
-      bwd_pair<METHOD, true>(X0, X1, d0, d1, xf, mul2, add2, dsc2, radd2, l0, l1, P0, P1, x0, x1);
-    else
-      bwd_pair<METHOD, false>(X0, X1, d0, d1, xf, mul2, add2, dsc2, radd2, l0, l1, P0, P1, x0, x1);
-    px[e] = pack_bf16x2(x0, x1);
+__device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair* cp,
+                                         const int4* ci, int jrow, const Xf& xf, uint32_t bar_chunk0,
+                                         int lane) {
+  uint32_t da[16], db[16], pk[8], xk[8];
+  tmem_ld16(dp_base, da);
+  tmem_wait_ld();
+#define CAPATTN_DKV_CHUNK(C, CUR, NXT)                                                     \
+  {                                                                                       \
+    if (C < 3) tmem_ld16(dp_base + 16 * (C + 1), NXT);                                    \
+    dkv_chunk<METHOD, MASKED, POLY, C>(s, CUR, cp, ci, jrow, xf, pk, xk);                 \
+    __syncwarp();                                                                         \
+    tmem_st8(dp_base + 16 * C, pk);                                                       \
+    tmem_st8(dp_base + 16 * C + 8, xk);                                                   \
+    tmem_wait_st();                                                                       \
+    if (C < 3) tmem_wait_ld();                                                            \
+    tc_fence_before();                                                                    \
+    __syncwarp();                                                                         \
+    if (lane == 0) mbar_arrive(bar_chunk0 + 8 * C);                                       \
   }
+  CAPATTN_DKV_CHUNK(0, da, db)
+  CAPATTN_DKV_CHUNK(1, db, da)
+  CAPATTN_DKV_CHUNK(2, da, db)
+  CAPATTN_DKV_CHUNK(3, db, da)
+#undef CAPATTN_DKV_CHUNK
 }
 
-// Chooses the dQ chunk variant: masked or not (per row), FMA-pipe tanh when the
-// whole warp's arguments are in range (warp vote).
-template <int METHOD>
-__device__ __forceinline__ void dq_dispatch(bool full, const uint32_t (&sv)[32], const uint32_t (&dp)[32],
-                                            int j0, int4 ri, const Xf& xf, float mul, float addl,
-                                            float dscale, float radd, uint32_t (&px)[16]) {
-  bool poly = false;
-  if constexpr (METHOD == CAPATTN_CAP_TANH) {
-    float am = 0.f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(__uint_as_float(sv[e])));
-    poly = __all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU);
-  }
-  if (poly) {
-    if (full)
-      dq_chunk<METHOD, false, true>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
-    else
-      dq_chunk<METHOD, true, true>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
-  } else {
-    if (full)
-      dq_chunk<METHOD, false, false>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
-    else
-      dq_chunk<METHOD, true, false>(sv, dp, j0, ri, xf, mul, addl, dscale, radd, px);
-  }
-}
-
-// ======================================================================= dK / dV
+// dK/dV: one CTA per (batch, KV head, 128-key tile).  K and V stay in shared
+// memory; the CTA loops over the query heads of its GQA group and the query tiles
+// of the tile's visit map ("steps"), accumulating dK and dV in TMEM (the group
+// sum happens in place).  Per step j (M = keys, N = queries, K-dim = head dim):
+//   S^T = K Q_j^T and dP^T = V dO_j^T   (SS MMAs, N = 128, separate commits)
+//   dV += P^T dO_j, dK += dX^T Q_j      (TS MMAs, 16 query rows per chunk)
+// TMEM: S^T [0, 128), dP^T [128, 256), dV [256, 384), dK [384, 512).  Each
+// elementwise warpgroup owns 64 query columns: it copies its S^T columns to
+// registers and releases them at once (the MMA issuer then computes S^T of step
+// j + 1 while step j's elementwise work runs), and packs P^T / dX^T over its dP^T
+// columns chunk by chunk; dP^T of step j + 1 is issued once every chunk's MMAs
+// are.
 template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
               const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[24];
+  __shared__ __align__(8) uint64_t bars[26];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ __align__(16) float4 colc[2][BT];  // per query column: mul, add - lse2, dscale, radd
-  __shared__ __align__(16) int4 coli[2][BT];    // per query column: live span (lo, hi, e)
+  __shared__ __align__(16) ColPair colc[2][BT / 2];  // per query column pair (double-buffered)
+  __shared__ __align__(16) int4 coli[2][BT];         // per query column: live span (lo, hi, e)
 
   const int gb = blockIdx.x;
   const int g = gb % p.Hkv, b = gb / p.Hkv;
@@ -327,11 +260,13 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const uint32_t bar_kv = smem_u32(&bars[0]);
   const uint32_t bar_full = smem_u32(&bars[1]);    // + s*8 (Q and dO)
   const uint32_t bar_empty = smem_u32(&bars[3]);   // + s*8
-  const uint32_t bar_sdp = smem_u32(&bars[5]);     // + part*8: scores of the part ready
-  const uint32_t bar_ew = smem_u32(&bars[7]);      // + part*8: part's P / dX written
-  const uint32_t bar_final = smem_u32(&bars[10]);
-  const uint32_t bar_cfull = smem_u32(&bars[11]);  // + (2*wg + cb)*8: column constants written
-  const uint32_t bar_cfree = smem_u32(&bars[15]);  // + (2*wg + cb)*8: column constants consumed
+  const uint32_t bar_s = smem_u32(&bars[5]);       // S^T of the step complete
+  const uint32_t bar_dp = smem_u32(&bars[6]);      // dP^T of the step complete
+  const uint32_t bar_sfree = smem_u32(&bars[7]);   // S^T copied to registers (8 warps)
+  const uint32_t bar_chunk = smem_u32(&bars[8]);   // + c*8: chunk c packed by both warpgroups (8 warps)
+  const uint32_t bar_final = smem_u32(&bars[16]);
+  const uint32_t bar_cfull = smem_u32(&bars[17]);  // + (2*wg + cb)*8: column constants written
+  const uint32_t bar_cfree = smem_u32(&bars[21]);  // + (2*wg + cb)*8: column constants consumed
 
   const uint32_t* map = p.kmap + ((size_t)b * p.nk + kt) * p.wq;
   if (threadIdx.x == 0) {
@@ -341,15 +276,15 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int c = 0; c < 2; ++c) {
-      mbar_init(bar_sdp + 8 * c, 1);
-      mbar_init(bar_ew + 8 * c, 8);
-    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_sfree, 8);
+    for (int c = 0; c < 4; ++c) mbar_init(bar_chunk + 8 * c, 8);
+    mbar_init(bar_final, 1);
     for (int c = 0; c < 4; ++c) {
       mbar_init(bar_cfull + 8 * c, 128);
       mbar_init(bar_cfree + 8 * c, 128);
     }
-    mbar_init(bar_final, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -364,137 +299,225 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const int n = ntiles * p.G;  // steps: (query head of the group) x (visited query tile)
 
   if (warp == 0) {
-    if (lane == 0 && n > 0) {
-      tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mdo);
-      mbar_expect_tx(bar_kv, 2 * TILE);
-      tma_load_4d(sK, &mk, bar_kv, 0, g, k0, b);
-      tma_load_4d(sK + SLAB, &mk, bar_kv, 64, g, k0, b);
-      tma_load_4d(sV, &mv, bar_kv, 0, g, k0, b);
-      tma_load_4d(sV + SLAB, &mv, bar_kv, 64, g, k0, b);
+    // ------------------------------------------------------------ TMA producer
+    if (n > 0) {
+      const bool leader = elect_one_sync();
+      if (leader) {
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mdo);
+        mbar_expect_tx(bar_kv, 2 * TILE);
+        tma_load_4d(sK, &mk, bar_kv, 0, g, k0, b);
+        tma_load_4d(sK + SLAB, &mk, bar_kv, 64, g, k0, b);
+        tma_load_4d(sV, &mv, bar_kv, 0, g, k0, b);
+        tma_load_4d(sV + SLAB, &mv, bar_kv, 64, g, k0, b);
+      }
+      __syncwarp();
       StepIter st(map, p.wq, p.G);
       int hh, qt, j = 0;
-      while (!abort_flag && st.next(hh, qt)) {
+      while (!__any_sync(0xFFFFFFFFu, abort_flag != 0) && st.next(hh, qt)) {
         const int h = g * p.G + hh;
         const int s = j % NSTAGE, u = j / NSTAGE;
-        if (u > 0 && !mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
-        const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
-        mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
-        tma_load_4d(sQ, &mq, bar_full + 8 * s, 0, h, qt * BT, b);
-        tma_load_4d(sQ + SLAB, &mq, bar_full + 8 * s, 64, h, qt * BT, b);
-        tma_load_4d(sO, &mdo, bar_full + 8 * s, 0, h, qt * BT, b);
-        tma_load_4d(sO + SLAB, &mdo, bar_full + 8 * s, 64, h, qt * BT, b);
+        if (u > 0 && !mbar_wait_warp(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
+        if (leader) {
+          const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
+          mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
+          tma_load_4d(sQ, &mq, bar_full + 8 * s, 0, h, qt * BT, b);
+          tma_load_4d(sQ + SLAB, &mq, bar_full + 8 * s, 64, h, qt * BT, b);
+          tma_load_4d(sO, &mdo, bar_full + 8 * s, 0, h, qt * BT, b);
+          tma_load_4d(sO + SLAB, &mdo, bar_full + 8 * s, 64, h, qt * BT, b);
+        }
+        __syncwarp();
         ++j;
       }
-      drain_wait(bar_kv, 0);
-      for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj)
-        drain_wait(bar_full + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+      if (leader) {
+        drain_wait(bar_kv, 0);
+        for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj)
+          drain_wait(bar_full + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+      }
+      __syncwarp();
     }
   } else if (warp == 1) {
-    if (lane == 0 && n > 0) {
-      // scores of part `part` of step j into that part's TMEM buffer
-      auto scores = [&](int j, int part) {
-        const uint32_t sQ = sQD + (j % NSTAGE) * 2 * TILE, sO = sQ + TILE;
-        issue_scores_part(tmem + 128u * part, sK, sQ, part);         // S^T  = K Q^T
-        issue_scores_part(tmem + 128u * part + 64u, sV, sO, part);   // dP^T = V dO^T
-        mma_commit(bar_sdp + 8 * part);
-      };
-      bool ok = mbar_wait(bar_kv, 0, p.status, &abort_flag) &&
-                mbar_wait(bar_full, 0, p.status, &abort_flag);
+    // ------------------------------------------------------------ MMA issuer
+    if (n > 0) {
+      const bool leader = elect_one_sync();
+      constexpr uint32_t idesc_acc = idesc_bf16(BT, HD, 0, 1);
+      const uint64_t dK = smem_desc(sK, 16, 1024), dV = smem_desc(sV, 16, 1024);
+      const uint64_t dQD = smem_desc(sQD, 16, 1024);        // Q / dO stages, K-major
+      const uint64_t dQDmn = smem_desc(sQD, SLAB, 1024);    // the same, MN-major
+      bool ok = mbar_wait_warp(bar_kv, 0, p.status, &abort_flag) &&
+                mbar_wait_warp(bar_full, 0, p.status, &abort_flag);
       if (ok) {
         tc_fence_after();
-        scores(0, 0);
-        scores(0, 1);
+        if (leader) {
+          issue_scores(tmem, dK, dQD);                          // S^T  = K Q^T
+          mma_commit(bar_s);
+          issue_scores(tmem + 128u, dV, desc_add(dQD, TILE));   // dP^T = V dO^T
+          mma_commit(bar_dp);
+        }
+        __syncwarp();
       }
       for (int j = 0; ok && j < n; ++j) {
-        const int s = j % NSTAGE;
-        const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
+        const uint32_t so = (uint32_t)((j % NSTAGE) * 2 * TILE);
+        const uint32_t son = (uint32_t)(((j + 1) % NSTAGE) * 2 * TILE);
         const bool more = j + 1 < n;
-        for (int part = 0; part < 2; ++part) {
-          if (!mbar_wait(bar_ew + 8 * part, j & 1, p.status, &abort_flag)) {
-            ok = false;
+        if (!mbar_wait_warp(bar_sfree, j & 1, p.status, &abort_flag)) break;
+        if (more) {
+          if (!mbar_wait_warp(bar_full + 8 * ((j + 1) % NSTAGE), ((j + 1) / NSTAGE) & 1, p.status,
+                              &abort_flag))
             break;
-          }
           tc_fence_after();
-          const bool first = (j == 0) && (part == 0);
-          issue_acc_part(tmem + 256u, tmem + 128u * part, sO, part, first);         // dV += P^T dO
-          issue_acc_part(tmem + 384u, tmem + 128u * part + 64u, sQ, part, first);   // dK += dX^T Q
-          if (part == 1) mma_commit(bar_empty + 8 * s);
-          if (more) {
-            if (part == 0 &&
-                !mbar_wait(bar_full + 8 * ((j + 1) % NSTAGE), ((j + 1) / NSTAGE) & 1, p.status,
-                           &abort_flag)) {
-              ok = false;
-              break;
-            }
+          if (leader) {
+            issue_scores(tmem, dK, desc_add(dQD, son));
+            mma_commit(bar_s);
+          }
+          __syncwarp();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (ok && !mbar_wait_warp(bar_chunk + 8 * c, j & 1, p.status, &abort_flag)) ok = false;
+          if (ok) {
             tc_fence_after();
-            scores(j + 1, part);
+            if (leader) {
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                const uint32_t q0 = (uint32_t)(64 * w + 16 * c);
+                const uint32_t acc = (j == 0 && c == 0 && w == 0) ? 0u : 1u;
+                mma_ts(tmem + 256u, tmem + 128u + q0, desc_add(dQDmn, so + TILE + q0 * 128), idesc_acc,
+                       acc);                                                 // dV += P^T dO
+                mma_ts(tmem + 384u, tmem + 128u + q0 + 8, desc_add(dQDmn, so + q0 * 128), idesc_acc,
+                       acc);                                                 // dK += dX^T Q
+              }
+            }
+            __syncwarp();
           }
         }
+        if (!ok) break;
+        if (leader) {
+          mma_commit(bar_empty + 8 * (j % NSTAGE));
+          if (more) {
+            issue_scores(tmem + 128u, dV, desc_add(dQD, son + TILE));
+            mma_commit(bar_dp);
+          }
+        }
+        __syncwarp();
       }
       // No wait for this commit here: the consumer warps wait for it, and
       // warp 1 re-checks it before freeing TMEM.
-      mma_commit(bar_final);
+      if (leader) mma_commit(bar_final);
+      __syncwarp();
     }
   } else {
-    const int wg = (warp - 2) >> 2;        // 32 columns of each part
+    const int wg = (warp - 2) >> 2;        // query columns [64 wg, 64 wg + 64)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;     // key row within the tile (TMEM lane)
     const int tid = (warp - 2 - 4 * wg) * 32 + lane;  // 0..127 within the warpgroup
     const int jrow = k0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_cols = lane_base + 64u * wg, dp_cols = lane_base + 128u + 64u * wg;
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
-    // query column whose constants this thread loads: the warpgroup's 32
-    // columns of part 0 and of part 1
-    const int my_col = (tid < 32) ? 32 * wg + tid : 64 + 32 * wg + (tid - 32);
+    const int my_col = 64 * wg + tid;      // query column whose constants this thread loads
     bool aborted = false;
+    // Per-step column constants go through a double buffer one step ahead of
+    // use, and their global inputs (and the tile's fully-live flag) are loaded
+    // two steps ahead, so that no global load sits between two steps.
+    auto put = [&](int buf, const ColRaw& r) {
+      if (tid < 64) {
+        const bool fin = isfinite(r.lse);
+        const float lse2 = fin ? r.lse * kL2E : 0.f;
+        const float radd = -r.dl + (fin ? p.z_loss_weight * r.lse : 0.f);
+        float mul, add;
+        row_consts<METHOD>(p.cap, p.sm_scale, r.temp, &mul, &add);
+        const float dsc = row_dscale<METHOD>(p.cap, p.sm_scale, r.temp);
+        float* cf = reinterpret_cast<float*>(&colc[buf][my_col >> 1]);
+        const int o = my_col & 1;
+        cf[0 + o] = mul;
+        cf[2 + o] = add - lse2;
+        cf[4 + o] = -dsc;
+        cf[6 + o] = -dsc * radd;
+        coli[buf][my_col] = r.ri;
+      }
+    };
+    // fully-live query-tile range of a step's query tile (raw; compared at use)
+    auto qfull_of = [&](bool have, int qt) {
+      return have ? p.qfull[(size_t)b * p.nq + qt] : make_int2(0, 0x7fffffff);
+    };
     StepIter nx(map, p.wq, p.G);
     int nh = 0, nqt = 0;
-    bool have_next = nx.next(nh, nqt);
-    ColRaw cur = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have_next && tid < 64);
-    int cur_qt = nqt;
-    for (int step = 0; step < n && have_next; ++step) {
+    const bool have0 = nx.next(nh, nqt);
+    const ColRaw r0 = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have0 && tid < 64);
+    int2 fr_cur = qfull_of(have0, nqt);
+    const bool have1 = nx.next(nh, nqt);
+    ColRaw r1 = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have1 && tid < 64);
+    int2 fr_nxt = qfull_of(have1, nqt);
+    put(0, r0);
+    mbar_arrive(bar_cfull + 8 * (2 * wg));
+    for (int step = 0; step < n; ++step) {
       const int cb = step & 1, cu = step >> 1;
       const uint32_t my_cfull = bar_cfull + 8 * (2 * wg + cb);
       const uint32_t my_cfree = bar_cfree + 8 * (2 * wg + cb);
-      if (step >= 2 && !mbar_wait_warp(my_cfree, (cu - 1) & 1, p.status, &abort_flag)) {
-        aborted = true;
-        break;
+      if (step + 1 < n) {
+        // constants of step + 1 into the other buffer (last used by step - 1)
+        const int nb = cb ^ 1, nu = (step + 1) >> 1;
+        if (step >= 1 &&
+            !mbar_wait_warp(bar_cfree + 8 * (2 * wg + nb), (nu - 1) & 1, p.status, &abort_flag)) {
+          aborted = true;
+          break;
+        }
+        put(nb, r1);
+        mbar_arrive(bar_cfull + 8 * (2 * wg + nb));
       }
-      if (tid < 64) {
-        float mul, add;
-        row_consts<METHOD>(p.cap, p.sm_scale, cur.temp, &mul, &add);
-        colc[cb][my_col] = make_float4(mul, add - cur.lse2,
-                                       row_dscale<METHOD>(p.cap, p.sm_scale, cur.temp), cur.radd);
-        coli[cb][my_col] = cur.ri;
-      }
-      mbar_arrive(my_cfull);
-      const int2 fr = p.qfull[(size_t)b * p.nq + cur_qt];
-      const bool tile_full = (kt >= fr.x) && (kt < fr.y);
-      have_next = nx.next(nh, nqt);
-      const ColRaw nxt = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have_next && tid < 64);
+      const bool have2 = nx.next(nh, nqt);
+      const ColRaw r2 = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have2 && tid < 64);
+      const int2 fr2 = qfull_of(have2, nqt);
+      const bool tile_full = (kt >= fr_cur.x) && (kt < fr_cur.y);
       if (!mbar_wait_warp(my_cfull, cu & 1, p.status, &abort_flag)) {
         aborted = true;
         break;
       }
-      for (int part = 0; part < 2; ++part) {
-        if (!mbar_wait_warp(bar_sdp + 8 * part, step & 1, p.status, &abort_flag)) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-        if (tile_full)
-          dkv_part<METHOD, false>(colc[cb], coli[cb], wg, part, jrow, xf, lane_base);
-        else
-          dkv_part<METHOD, true>(colc[cb], coli[cb], wg, part, jrow, xf, lane_base);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_ew + 8 * part);
+      // S^T of this warpgroup's columns to registers; the columns are then free
+      if (!mbar_wait_warp(bar_s, step & 1, p.status, &abort_flag)) {
+        aborted = true;
+        break;
       }
-      if (aborted) break;
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld16(s_cols, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+      tmem_ld16(s_cols + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+      tmem_ld16(s_cols + 32, *reinterpret_cast<uint32_t(*)[16]>(&sv[32]));
+      tmem_ld16(s_cols + 48, *reinterpret_cast<uint32_t(*)[16]>(&sv[48]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sfree);
+      bool poly = false;
+      if constexpr (METHOD == CAPATTN_CAP_TANH) {
+        float am = 0.f;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) am = fmax3_abs(am, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+        poly = __all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU);
+      }
+      if (!mbar_wait_warp(bar_dp, step & 1, p.status, &abort_flag)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const ColPair* cp = &colc[cb][32 * wg];
+      const int4* ci = &coli[cb][64 * wg];
+      if (tile_full) {
+        if (poly)
+          dkv_step<METHOD, false, true>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+        else
+          dkv_step<METHOD, false, false>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+      } else {
+        if (poly)
+          dkv_step<METHOD, true, true>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+        else
+          dkv_step<METHOD, true, false>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+      }
       mbar_arrive(my_cfree);
-      cur = nxt;
-      cur_qt = nqt;
+      r1 = r2;
+      fr_cur = fr_nxt;
+      fr_nxt = fr2;
     }
     // ---------------------------------------------------------- epilogue
     bool have = false;
@@ -532,13 +555,72 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 }
 
 // ======================================================================= dQ
+// One 16-column chunk (key columns 16 C .. 16 C + 15 of the warpgroup's 64) of a
+// query row: dX packed to bf16.  Row constants in rc (both halves equal).
+template <int METHOD, bool MASKED, bool POLY, int C>
+__device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t (&dp)[16],
+                                         const ColPair& rc, int4 ri, int j0, const Xf& xf,
+                                         uint32_t (&xk)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    bool l0 = true, l1 = true;
+    if constexpr (MASKED) {
+      const int ja = j0 + 16 * C + 2 * e, jb = ja + 1;
+      l0 = (ja >= ri.x && ja < ri.y) || ja == ri.z;
+      l1 = (jb >= ri.x && jb < ri.y) || jb == ri.z;
+    }
+    const float X0 = __uint_as_float(s[16 * C + 2 * e]), X1 = __uint_as_float(s[16 * C + 2 * e + 1]);
+    const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
+    uint32_t pk;
+    if (POLY && e < kDkvPolyPairs)
+      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, rc, l0, l1, pk, xk[e]);
+    else
+      dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, rc, l0, l1, pk, xk[e]);
+  }
+}
+
+// The warpgroup's 64 key columns of one step: dX of chunk C is packed over the
+// first 8 of its 16 dP columns and handed to the MMA issuer.
+template <int METHOD, bool MASKED, bool POLY>
+__device__ __forceinline__ void dq_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair& rc,
+                                        int4 ri, int j0, const Xf& xf, uint32_t bar_chunk0, int lane) {
+  uint32_t da[16], db[16], xk[8];
+  tmem_ld16(dp_base, da);
+  tmem_wait_ld();
+#define CAPATTN_DQ_CHUNK(C, CUR, NXT)                                                      \
+  {                                                                                       \
+    if (C < 3) tmem_ld16(dp_base + 16 * (C + 1), NXT);                                    \
+    dq_chunk<METHOD, MASKED, POLY, C>(s, CUR, rc, ri, j0, xf, xk);                        \
+    __syncwarp();                                                                         \
+    tmem_st8(dp_base + 16 * C, xk);                                                       \
+    tmem_wait_st();                                                                       \
+    if (C < 3) tmem_wait_ld();                                                            \
+    tc_fence_before();                                                                    \
+    __syncwarp();                                                                         \
+    if (lane == 0) mbar_arrive(bar_chunk0 + 8 * C);                                       \
+  }
+  CAPATTN_DQ_CHUNK(0, da, db)
+  CAPATTN_DQ_CHUNK(1, db, da)
+  CAPATTN_DQ_CHUNK(2, da, db)
+  CAPATTN_DQ_CHUNK(3, db, da)
+#undef CAPATTN_DQ_CHUNK
+}
+
+// dQ: one CTA per (batch, query head, 128-query tile), looping over the KV tiles
+// of its visit map.  Per step j (M = queries, N = keys, K-dim = head dim):
+//   S = Q K_j^T and dP = dO V_j^T   (SS MMAs, N = 128, separate commits)
+//   dQ += dX K_j                    (TS MMAs, 16 keys per chunk)
+// TMEM: S [0, 128), dP [128, 256), dQ [256, 384).  The elementwise warpgroups
+// own 64 key columns each, copy their S columns to registers and release them
+// (S of step j + 1 then runs during step j's elementwise work), and pack dX over
+// their dP columns chunk by chunk.
 template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
              const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[16];
+  __shared__ __align__(8) uint64_t bars[20];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -556,9 +638,11 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   const uint32_t bar_q = smem_u32(&bars[0]);
   const uint32_t bar_full = smem_u32(&bars[1]);    // + s*8
   const uint32_t bar_empty = smem_u32(&bars[3]);   // + s*8
-  const uint32_t bar_sdp = smem_u32(&bars[5]);     // + part*8
-  const uint32_t bar_ew = smem_u32(&bars[7]);      // + part*8
-  const uint32_t bar_final = smem_u32(&bars[10]);
+  const uint32_t bar_s = smem_u32(&bars[5]);
+  const uint32_t bar_dp = smem_u32(&bars[6]);
+  const uint32_t bar_sfree = smem_u32(&bars[7]);
+  const uint32_t bar_chunk = smem_u32(&bars[8]);   // + c*8: chunk c packed by both warpgroups
+  const uint32_t bar_final = smem_u32(&bars[16]);
 
   const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
   if (threadIdx.x == 0) {
@@ -568,10 +652,10 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int c = 0; c < 2; ++c) {
-      mbar_init(bar_sdp + 8 * c, 1);
-      mbar_init(bar_ew + 8 * c, 8);
-    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_sfree, 8);
+    for (int c = 0; c < 4; ++c) mbar_init(bar_chunk + 8 * c, 8);
     mbar_init(bar_final, 1);
     fence_mbar_init();
   }
@@ -586,79 +670,115 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   const int n = count_tiles(map, p.wk);
 
   if (warp == 0) {
-    if (lane == 0 && n > 0) {
-      tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
-      mbar_expect_tx(bar_q, 2 * TILE);
-      tma_load_4d(sQ, &mq, bar_q, 0, h, q0, b);
-      tma_load_4d(sQ + SLAB, &mq, bar_q, 64, h, q0, b);
-      tma_load_4d(sO, &mdo, bar_q, 0, h, q0, b);
-      tma_load_4d(sO + SLAB, &mdo, bar_q, 64, h, q0, b);
+    // ------------------------------------------------------------ TMA producer
+    if (n > 0) {
+      const bool leader = elect_one_sync();
+      if (leader) {
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+        mbar_expect_tx(bar_q, 2 * TILE);
+        tma_load_4d(sQ, &mq, bar_q, 0, h, q0, b);
+        tma_load_4d(sQ + SLAB, &mq, bar_q, 64, h, q0, b);
+        tma_load_4d(sO, &mdo, bar_q, 0, h, q0, b);
+        tma_load_4d(sO + SLAB, &mdo, bar_q, 64, h, q0, b);
+      }
+      __syncwarp();
       TileIter it(map, p.wk);
       int t, j = 0;
-      while (it.next(t)) {
+      while (!__any_sync(0xFFFFFFFFu, abort_flag != 0) && it.next(t)) {
         const int s = j % NSTAGE, u = j / NSTAGE;
-        if (u > 0 && !mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
-        const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
-        mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
-        tma_load_4d(sK, &mk, bar_full + 8 * s, 0, g, t * BT, b);
-        tma_load_4d(sK + SLAB, &mk, bar_full + 8 * s, 64, g, t * BT, b);
-        tma_load_4d(sV, &mv, bar_full + 8 * s, 0, g, t * BT, b);
-        tma_load_4d(sV + SLAB, &mv, bar_full + 8 * s, 64, g, t * BT, b);
+        if (u > 0 && !mbar_wait_warp(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
+        if (leader) {
+          const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
+          mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
+          tma_load_4d(sK, &mk, bar_full + 8 * s, 0, g, t * BT, b);
+          tma_load_4d(sK + SLAB, &mk, bar_full + 8 * s, 64, g, t * BT, b);
+          tma_load_4d(sV, &mv, bar_full + 8 * s, 0, g, t * BT, b);
+          tma_load_4d(sV + SLAB, &mv, bar_full + 8 * s, 64, g, t * BT, b);
+        }
+        __syncwarp();
         ++j;
       }
-      drain_wait(bar_q, 0);
-      for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj)
-        drain_wait(bar_full + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+      if (leader) {
+        drain_wait(bar_q, 0);
+        for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj)
+          drain_wait(bar_full + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+      }
+      __syncwarp();
     }
   } else if (warp == 1) {
-    if (lane == 0 && n > 0) {
-      auto scores = [&](int j, int part) {
-        const uint32_t sK = sKV + (j % NSTAGE) * 2 * TILE, sV = sK + TILE;
-        issue_scores_part(tmem + 128u * part, sQ, sK, part);         // S  = Q K^T
-        issue_scores_part(tmem + 128u * part + 64u, sO, sV, part);   // dP = dO V^T
-        mma_commit(bar_sdp + 8 * part);
-      };
-      bool ok = mbar_wait(bar_q, 0, p.status, &abort_flag) &&
-                mbar_wait(bar_full, 0, p.status, &abort_flag);
+    // ------------------------------------------------------------ MMA issuer
+    if (n > 0) {
+      const bool leader = elect_one_sync();
+      constexpr uint32_t idesc_acc = idesc_bf16(BT, HD, 0, 1);
+      const uint64_t dQ = smem_desc(sQ, 16, 1024), dO = smem_desc(sO, 16, 1024);
+      const uint64_t dKV = smem_desc(sKV, 16, 1024);        // K / V stages, K-major
+      const uint64_t dKVmn = smem_desc(sKV, SLAB, 1024);    // the same, MN-major
+      bool ok = mbar_wait_warp(bar_q, 0, p.status, &abort_flag) &&
+                mbar_wait_warp(bar_full, 0, p.status, &abort_flag);
       if (ok) {
         tc_fence_after();
-        scores(0, 0);
-        scores(0, 1);
+        if (leader) {
+          issue_scores(tmem, dQ, dKV);                          // S  = Q K^T
+          mma_commit(bar_s);
+          issue_scores(tmem + 128u, dO, desc_add(dKV, TILE));   // dP = dO V^T
+          mma_commit(bar_dp);
+        }
+        __syncwarp();
       }
       for (int j = 0; ok && j < n; ++j) {
-        const int s = j % NSTAGE;
-        const uint32_t sK = sKV + s * 2 * TILE;
+        const uint32_t so = (uint32_t)((j % NSTAGE) * 2 * TILE);
+        const uint32_t son = (uint32_t)(((j + 1) % NSTAGE) * 2 * TILE);
         const bool more = j + 1 < n;
-        for (int part = 0; part < 2; ++part) {
-          if (!mbar_wait(bar_ew + 8 * part, j & 1, p.status, &abort_flag)) {
-            ok = false;
+        if (!mbar_wait_warp(bar_sfree, j & 1, p.status, &abort_flag)) break;
+        if (more) {
+          if (!mbar_wait_warp(bar_full + 8 * ((j + 1) % NSTAGE), ((j + 1) / NSTAGE) & 1, p.status,
+                              &abort_flag))
             break;
-          }
           tc_fence_after();
-          issue_acc_part(tmem + 256u, tmem + 128u * part + 64u, sK, part, (j == 0) && (part == 0));
-          if (part == 1) mma_commit(bar_empty + 8 * s);
-          if (more) {
-            if (part == 0 &&
-                !mbar_wait(bar_full + 8 * ((j + 1) % NSTAGE), ((j + 1) / NSTAGE) & 1, p.status,
-                           &abort_flag)) {
-              ok = false;
-              break;
-            }
+          if (leader) {
+            issue_scores(tmem, dQ, desc_add(dKV, son));
+            mma_commit(bar_s);
+          }
+          __syncwarp();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (ok && !mbar_wait_warp(bar_chunk + 8 * c, j & 1, p.status, &abort_flag)) ok = false;
+          if (ok) {
             tc_fence_after();
-            scores(j + 1, part);
+            if (leader) {
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                const uint32_t k0c = (uint32_t)(64 * w + 16 * c);
+                mma_ts(tmem + 256u, tmem + 128u + k0c, desc_add(dKVmn, so + k0c * 128), idesc_acc,
+                       (j == 0 && c == 0 && w == 0) ? 0u : 1u);     // dQ += dX K
+              }
+            }
+            __syncwarp();
           }
         }
+        if (!ok) break;
+        if (leader) {
+          mma_commit(bar_empty + 8 * (j % NSTAGE));
+          if (more) {
+            issue_scores(tmem + 128u, dO, desc_add(dKV, son + TILE));
+            mma_commit(bar_dp);
+          }
+        }
+        __syncwarp();
       }
-      mma_commit(bar_final);
+      if (leader) mma_commit(bar_final);
+      __syncwarp();
     }
   } else {
-    const int wg = (warp - 2) >> 2;        // 32 key columns of each part
+    const int wg = (warp - 2) >> 2;        // key columns [64 wg, 64 wg + 64)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int i = q0 + r;
     const bool valid = i < p.L;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_cols = lane_base + 64u * wg, dp_cols = lane_base + 128u + 64u * wg;
     const int4 ri = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
     const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
     const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
@@ -666,38 +786,60 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const float dl = valid ? p.delta[rr] : 0.f;
     const bool fin = isfinite(lse);
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
-    float mul, add;
-    row_consts<METHOD>(p.cap, p.sm_scale, temp, &mul, &add);
-    const float addl = add - (fin ? lse * kL2E : 0.f);
-    const float dscale = row_dscale<METHOD>(p.cap, p.sm_scale, temp);
-    const float radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
+    ColPair rc;
+    {
+      float mul, add;
+      row_consts<METHOD>(p.cap, p.sm_scale, temp, &mul, &add);
+      const float addl = add - (fin ? lse * kL2E : 0.f);
+      const float dsc = row_dscale<METHOD>(p.cap, p.sm_scale, temp);
+      const float radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
+      rc.a = make_float4(mul, mul, addl, addl);
+      rc.b = make_float4(-dsc, -dsc, -dsc * radd, -dsc * radd);
+    }
     bool aborted = false;
     TileIter it(map, p.wk);
-    for (int j = 0; j < n && !aborted; ++j) {
+    for (int j = 0; j < n; ++j) {
       int t;
       it.next(t);
       const int k0 = t * BT;
-      const bool full = (ri.x <= k0) && (ri.y >= k0 + BT);
-      for (int part = 0; part < 2; ++part) {
-        if (!mbar_wait_warp(bar_sdp + 8 * part, j & 1, p.status, &abort_flag)) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sbuf = lane_base + 128u * part, dbuf = sbuf + 64u;
-        const int pc0 = 32 * wg;
-        uint32_t sv[32], dp[32], px[16];
-        tmem_ld32(sbuf + pc0, sv);
-        tmem_ld32(dbuf + pc0, dp);
-        tmem_wait_ld();
-        dq_dispatch<METHOD>(full, sv, dp, k0 + 64 * part + pc0, ri, xf, mul, addl, dscale, radd, px);
-        __syncwarp();
-        // packed dX of columns [pc0, pc0 + 32): 16 columns at dbuf + pc0
-        tmem_st16(dbuf + pc0, px);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_ew + 8 * part);
+      const bool full = __all_sync(0xFFFFFFFFu, (ri.x <= k0) && (ri.y >= k0 + BT));
+      if (!mbar_wait_warp(bar_s, j & 1, p.status, &abort_flag)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld16(s_cols, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+      tmem_ld16(s_cols + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+      tmem_ld16(s_cols + 32, *reinterpret_cast<uint32_t(*)[16]>(&sv[32]));
+      tmem_ld16(s_cols + 48, *reinterpret_cast<uint32_t(*)[16]>(&sv[48]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sfree);
+      bool poly = false;
+      if constexpr (METHOD == CAPATTN_CAP_TANH) {
+        float am = 0.f;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) am = fmax3_abs(am, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+        poly = __all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU);
+      }
+      if (!mbar_wait_warp(bar_dp, j & 1, p.status, &abort_flag)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const int j0 = k0 + 64 * wg;
+      if (full) {
+        if (poly)
+          dq_step<METHOD, false, true>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
+        else
+          dq_step<METHOD, false, false>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
+      } else {
+        if (poly)
+          dq_step<METHOD, true, true>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
+        else
+          dq_step<METHOD, true, false>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
       }
     }
     bool have = false;

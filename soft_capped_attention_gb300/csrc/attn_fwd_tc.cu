@@ -82,20 +82,22 @@ __device__ __forceinline__ int count_union(const uint32_t* a, const uint32_t* c,
   return s;
 }
 
-__device__ __forceinline__ void issue_s(uint32_t d, uint32_t sQ, uint32_t sK) {
+// S = Q K^T from the tiles' K-major descriptors.
+__device__ __forceinline__ void issue_s(uint32_t d, uint64_t dQ, uint64_t dK) {
   constexpr uint32_t idesc = idesc_bf16(BM, BN, 0, 0);
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks) {
     const uint32_t off = (ks >> 2) * SLAB + (ks & 3) * 32;
-    mma_ss(d, smem_desc(sQ + off, 16, 1024), smem_desc(sK + off, 16, 1024), idesc, ks > 0);
+    mma_ss(d, desc_add(dQ, off), desc_add(dK, off), idesc, ks > 0 ? 1u : 0u);
   }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pt, uint32_t sV, uint32_t acc0) {
+// O += P V with P (bf16) in TMEM and V's MN-major descriptor.
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pt, uint64_t dV, uint32_t acc0) {
   constexpr uint32_t idesc = idesc_bf16(BM, HD, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < BN / 16; ++ks)
-    mma_ts(d, pt + ks * 8, smem_desc(sV + ks * 2048, SLAB, 1024), idesc, (acc0 || ks > 0) ? 1u : 0u);
+    mma_ts(d, pt + ks * 8, desc_add(dV, ks * 2048), idesc, (acc0 || ks > 0) ? 1u : 0u);
 }
 
 // Maximum and minimum raw score over the live columns k0 .. k0 + 127 of one row.
@@ -260,40 +262,54 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n > 0) {
-      tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
-      mbar_expect_tx(bar_q, 2 * TILE);
-      tma_load_4d(sQ0, &mq, bar_q, 0, h, qt0 * BM, b);
-      tma_load_4d(sQ0 + SLAB, &mq, bar_q, 64, h, qt0 * BM, b);
-      tma_load_4d(sQ1, &mq, bar_q, 0, h, qt0 * BM + BM, b);
-      tma_load_4d(sQ1 + SLAB, &mq, bar_q, 64, h, qt0 * BM + BM, b);
+    if (n > 0) {
+      const bool leader = elect_one_sync();
+      if (leader) {
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+        mbar_expect_tx(bar_q, 2 * TILE);
+        tma_load_4d(sQ0, &mq, bar_q, 0, h, qt0 * BM, b);
+        tma_load_4d(sQ0 + SLAB, &mq, bar_q, 64, h, qt0 * BM, b);
+        tma_load_4d(sQ1, &mq, bar_q, 0, h, qt0 * BM + BM, b);
+        tma_load_4d(sQ1 + SLAB, &mq, bar_q, 64, h, qt0 * BM + BM, b);
+      }
+      __syncwarp();
       PairIter it(map0, map1, p.wk);
       int t, j = 0;
       bool a0, a1;
       while (it.next(t, a0, a1)) {
         const int s = j % NSTAGE, u = j / NSTAGE;
-        if (u > 0 && !mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
-        const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
-        mbar_expect_tx(bar_kfull + 8 * s, TILE);
-        tma_load_4d(sK, &mk, bar_kfull + 8 * s, 0, g, t * BN, b);
-        tma_load_4d(sK + SLAB, &mk, bar_kfull + 8 * s, 64, g, t * BN, b);
-        mbar_expect_tx(bar_vfull + 8 * s, TILE);
-        tma_load_4d(sV, &mv, bar_vfull + 8 * s, 0, g, t * BN, b);
-        tma_load_4d(sV + SLAB, &mv, bar_vfull + 8 * s, 64, g, t * BN, b);
+        if (u > 0 && !mbar_wait_warp(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
+        if (leader) {
+          const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
+          mbar_expect_tx(bar_kfull + 8 * s, TILE);
+          tma_load_4d(sK, &mk, bar_kfull + 8 * s, 0, g, t * BN, b);
+          tma_load_4d(sK + SLAB, &mk, bar_kfull + 8 * s, 64, g, t * BN, b);
+          mbar_expect_tx(bar_vfull + 8 * s, TILE);
+          tma_load_4d(sV, &mv, bar_vfull + 8 * s, 0, g, t * BN, b);
+          tma_load_4d(sV + SLAB, &mv, bar_vfull + 8 * s, 64, g, t * BN, b);
+        }
+        __syncwarp();
         ++j;
       }
-      drain_wait(bar_q, 0);
-      for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj) {
-        drain_wait(bar_kfull + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
-        drain_wait(bar_vfull + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+      if (leader) {
+        drain_wait(bar_q, 0);
+        for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj) {
+          drain_wait(bar_kfull + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+          drain_wait(bar_vfull + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+        }
       }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
-      bool ok = mbar_wait(bar_q, 0, p.status, &abort_flag);
+    if (n > 0) {
+      const bool leader = elect_one_sync();
+      const uint64_t dQ0 = smem_desc(sQ0, 16, 1024), dQ1 = smem_desc(sQ1, 16, 1024);
+      const uint64_t dKV = smem_desc(sKV, 16, 1024);      // K / V stages, K-major
+      const uint64_t dKVmn = smem_desc(sKV, SLAB, 1024);  // the same, MN-major
+      bool ok = mbar_wait_warp(bar_q, 0, p.status, &abort_flag);
       tc_fence_after();
       PairIter it(map0, map1, p.wk);
       int t;
@@ -302,47 +318,57 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       it.next(t, c0, c1);
       int pc0 = 0, pc1 = 0;         // p_full phases consumed per query tile
       uint32_t started0 = 0, started1 = 0;
-      if (ok) ok = mbar_wait(bar_kfull, 0, p.status, &abort_flag);
+      if (ok) ok = mbar_wait_warp(bar_kfull, 0, p.status, &abort_flag);
       if (ok) {
         tc_fence_after();
-        if (c0) { issue_s(tmem, sQ0, sKV); mma_commit(bar_sfull); }
-        if (c1) { issue_s(tmem + 128u, sQ1, sKV); mma_commit(bar_sfull + 8); }
+        if (leader) {
+          if (c0) { issue_s(tmem, dQ0, dKV); mma_commit(bar_sfull); }
+          if (c1) { issue_s(tmem + 128u, dQ1, dKV); mma_commit(bar_sfull + 8); }
+        }
+        __syncwarp();
       }
       for (int j = 0; ok && j < n; ++j) {
         const int s = j % NSTAGE;
-        const uint32_t sV = sKV + s * 2 * TILE + TILE;
+        const uint32_t vo = (uint32_t)(s * 2 * TILE + TILE);
         n0 = n1 = false;
         const bool more = (j + 1 < n) && it.next(t, n0, n1);
         const int s1 = (j + 1) % NSTAGE;
-        const uint32_t sKn = sKV + s1 * 2 * TILE;
-        if (!mbar_wait(bar_vfull + 8 * s, (j / NSTAGE) & 1, p.status, &abort_flag)) break;
+        const uint32_t ko = (uint32_t)(s1 * 2 * TILE);
+        if (!mbar_wait_warp(bar_vfull + 8 * s, (j / NSTAGE) & 1, p.status, &abort_flag)) break;
         if (c0) {
-          if (!mbar_wait(bar_pfull, pc0 & 1, p.status, &abort_flag)) break;
+          if (!mbar_wait_warp(bar_pfull, pc0 & 1, p.status, &abort_flag)) break;
           ++pc0;
           tc_fence_after();
-          issue_pv(tmem + 256u, tmem, sV, started0);
+          if (leader) issue_pv(tmem + 256u, tmem, desc_add(dKVmn, vo), started0);
+          __syncwarp();
           started0 = 1;
         }
         if (more) {
-          if (!mbar_wait(bar_kfull + 8 * s1, ((j + 1) / NSTAGE) & 1, p.status, &abort_flag)) break;
+          if (!mbar_wait_warp(bar_kfull + 8 * s1, ((j + 1) / NSTAGE) & 1, p.status, &abort_flag)) break;
           tc_fence_after();
-          if (n0) { issue_s(tmem, sQ0, sKn); mma_commit(bar_sfull); }
+          if (n0 && leader) { issue_s(tmem, dQ0, desc_add(dKV, ko)); mma_commit(bar_sfull); }
+          __syncwarp();
         }
         if (c1) {
-          if (!mbar_wait(bar_pfull + 8, pc1 & 1, p.status, &abort_flag)) break;
+          if (!mbar_wait_warp(bar_pfull + 8, pc1 & 1, p.status, &abort_flag)) break;
           ++pc1;
           tc_fence_after();
-          issue_pv(tmem + 384u, tmem + 128u, sV, started1);
+          if (leader) issue_pv(tmem + 384u, tmem + 128u, desc_add(dKVmn, vo), started1);
+          __syncwarp();
           started1 = 1;
         }
-        mma_commit(bar_empty + 8 * s);
-        if (more && n1) { issue_s(tmem + 128u, sQ1, sKn); mma_commit(bar_sfull + 8); }
+        if (leader) {
+          mma_commit(bar_empty + 8 * s);
+          if (more && n1) { issue_s(tmem + 128u, dQ1, desc_add(dKV, ko)); mma_commit(bar_sfull + 8); }
+        }
+        __syncwarp();
         c0 = n0;
         c1 = n1;
       }
       // The MMA thread does not wait for its own commit here: the consumer
       // warps wait for it, and warp 1 re-checks it before freeing TMEM.
-      mma_commit(bar_final);
+      if (leader) mma_commit(bar_final);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax

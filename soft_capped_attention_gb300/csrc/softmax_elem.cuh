@@ -115,6 +115,13 @@ __device__ __forceinline__ float cap_f_d(float X, const Xf& xf, float* d) {
   }
 }
 
+// max(acc, |a|, |b|) with the three-input max instruction.
+__device__ __forceinline__ float fmax3_abs(float acc, float a, float b) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(acc), "f"(fabsf(a)), "f"(fabsf(b)));
+  return r;
+}
+
 // ---------------------------------------------------------------- packed fp32
 // Two fp32 lanes in one 64-bit register pair (fma/mul/add .f32x2).
 struct F2 {

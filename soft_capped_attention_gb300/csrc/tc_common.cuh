@@ -258,6 +258,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, 
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Adds a byte offset to the start-address field of a shared-memory descriptor
+// (the field holds address >> 4; tiles stay below 256 KB so it never carries).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+// One lane of a converged warp (elect.sync).  Role warps run their loops
+// warp-wide, so that descriptors and addresses stay warp-uniform, and only the
+// elected lane issues the single-thread tcgen05.mma / tcgen05.commit / TMA
+// instructions; commits track the MMAs of the issuing thread, so one lane is
+// elected once and keeps the role.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile("{ .reg .pred P; elect.sync _|P, 0xffffffff; selp.u32 %0, 1, 0, P; }" : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
