@@ -215,16 +215,22 @@ capattn_status capattn_fwd_noalloc(const capattn_config* cfg, const void* q, con
                                    cudaStream_t stream);
 
 /*
- * Per-kernel timing.  While enabled, every kernel the library launches is
- * bracketed by CUDA events recorded on the caller's stream (library-owned
- * events; a small fixed pool).  capattn_profile_read synchronises those events
- * and returns, per kernel kind (CAPATTN_KERNEL_*), the summed milliseconds and
- * launch counts since the last reset (reset = nonzero clears after reading).
+ * Per-kernel timing.  While enabled, every kernel the library launches whose
+ * kind is selected (all kinds by default) is bracketed by CUDA events recorded
+ * on the caller's stream (library-owned events; a small fixed pool), and the
+ * launches of every kind are counted.  capattn_profile_read synchronises those
+ * events and returns, per kernel kind (CAPATTN_KERNEL_*), the summed
+ * milliseconds (0 for unselected kinds) and launch counts since the last reset
+ * (reset = nonzero clears after reading).  Each recorded event costs the stream
+ * a few microseconds, so a timing run selects only the kernel it times.
+ * capattn_profile_select takes a bit mask of kinds (bit k = kind k; 0 selects
+ * none) and returns CAPATTN_ERR_INVALID_ARG for bits beyond the known kinds.
  * Not thread-safe; meant for benchmarking.  Disabled by default.
  */
 enum { CAPATTN_KERNEL_PREPASS = 0, CAPATTN_KERNEL_FWD = 1, CAPATTN_KERNEL_DELTA = 2,
        CAPATTN_KERNEL_DKV = 3, CAPATTN_KERNEL_DQ = 4, CAPATTN_KERNEL_KINDS = 5 };
 capattn_status capattn_profile_enable(int on);
+capattn_status capattn_profile_select(unsigned int kind_mask);
 capattn_status capattn_profile_read(double* ms, int64_t* launches, int n_kinds, int reset);
 const char* capattn_kernel_name(int kind);
 

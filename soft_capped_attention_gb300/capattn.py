@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         h.capattn_mask_bits_host.argtypes = [cfgp, vp, vp, i32, vp, sz]
         h.capattn_profile_enable.restype = ctypes.c_int
         h.capattn_profile_enable.argtypes = [ctypes.c_int]
+        h.capattn_profile_select.restype = ctypes.c_int
+        h.capattn_profile_select.argtypes = [ctypes.c_uint]
         h.capattn_profile_read.restype = ctypes.c_int
         h.capattn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                            ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int]
@@ -95,7 +97,7 @@ def lib() -> ctypes.CDLL:
 EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn_workspace_bytes",
                     "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_device_status",
                     "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host",
-                    "capattn_profile_enable", "capattn_profile_read", "capattn_kernel_name",
+                    "capattn_profile_enable", "capattn_profile_select", "capattn_profile_read", "capattn_kernel_name",
                     "capattn_fwd_noalloc")
 KERNEL_KINDS = ("prepass", "fwd", "delta", "dkv", "dq")
 
@@ -270,6 +272,17 @@ def capattn_mask_bits_host(cfg: CapattnConfig, b: int, seg=None, bounds=None):
 
 def capattn_profile_enable(on: bool = True):
     _check(lib().capattn_profile_enable(1 if on else 0), "capattn_profile_enable")
+
+
+def capattn_profile_select(kinds=None):
+    """Time only the given kernel kinds (names from KERNEL_KINDS; None = all)."""
+    if kinds is None:
+        mask = (1 << len(KERNEL_KINDS)) - 1
+    else:
+        mask = 0
+        for k in kinds:
+            mask |= 1 << KERNEL_KINDS.index(k)
+    _check(lib().capattn_profile_select(mask), "capattn_profile_select")
 
 
 def capattn_profile_read(reset: bool = True) -> dict:

@@ -127,6 +127,26 @@ __device__ __forceinline__ void row_range(const uint32_t (&v)[128], int k0, int4
   vmin = fminf(b0, b1);
 }
 
+// Maximum (and, with NEED_MIN, minimum) raw score of a fully live row of 128
+// columns, with three-input max / min in two independent chains each.
+template <bool NEED_MIN>
+__device__ __forceinline__ void row_range_full(const uint32_t (&v)[128], float& vmax, float& vmin) {
+  float a0 = -INFINITY, a1 = -INFINITY, b0 = INFINITY, b1 = INFINITY;
+#pragma unroll
+  for (int e = 0; e < 128; e += 4) {
+    const float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
+    const float x2 = __uint_as_float(v[e + 2]), x3 = __uint_as_float(v[e + 3]);
+    a0 = fmax3(a0, x0, x1);
+    a1 = fmax3(a1, x2, x3);
+    if constexpr (NEED_MIN) {
+      b0 = fmin3(b0, x0, x1);
+      b1 = fmin3(b1, x2, x3);
+    }
+  }
+  vmax = fmaxf(a0, a1);
+  vmin = NEED_MIN ? fminf(b0, b1) : vmax;
+}
+
 // 32 columns of P for the tanh cap when every |X * in| of the warp is within
 // the polynomial's range: the first POLY_PAIRS column pairs evaluate tanh on the
 // FMA pipe, the rest with tanh.approx; packed fp32x2 arithmetic throughout.
@@ -383,6 +403,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int4 ri = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
     const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
     const bool neg = temp < 0.f;
+    // the row minimum is needed for a negative temperature and for the range
+    // check of the tanh polynomial
+    const bool need_min = (METHOD == CAPATTN_CAP_TANH) || __any_sync(0xFFFFFFFFu, neg);
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
     float rmul, radd;
     row_consts<METHOD>(p.cap, p.sm_scale, temp, &rmul, &radd);
@@ -409,10 +432,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         for (int c = 0; c < 4; ++c)
           tmem_ld32(s_base + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
         tmem_wait_ld();
-        if (full)
-          row_range<false>(v, k0, ri, vmax, vmin);
-        else
+        if (!full)
           row_range<true>(v, k0, ri, vmax, vmin);
+        else if (need_min)
+          row_range_full<true>(v, vmax, vmin);
+        else
+          row_range_full<false>(v, vmax, vmin);
       }
       // Every cap is increasing: the logit maximum is the transform of the raw
       // maximum (of the minimum for a negative temperature).

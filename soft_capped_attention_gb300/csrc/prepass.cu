@@ -155,6 +155,53 @@ __global__ void delta_kernel(Params p) {
   }
 }
 
+// bf16, D = 128: 16 lanes per row with 16-byte loads; each warp takes 8 rows
+// (4 per half-warp) and issues all of its loads before reducing, to keep
+// enough bytes in flight to stream O and dO at HBM speed.
+constexpr int kDeltaRowsPerWarp = 8;
+
+__global__ void delta_bf16_kernel(Params p) {
+  const long long nrows = (long long)p.B * p.L * p.Hq;
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4, sub = lane & 15;
+  const long long row0 = ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kDeltaRowsPerWarp;
+  uint4 a[kDeltaRowsPerWarp / 2], c[kDeltaRowsPerWarp / 2];
+#pragma unroll
+  for (int t = 0; t < kDeltaRowsPerWarp / 2; ++t) {
+    const long long row = row0 + 2 * t + half;
+    if (row < nrows) {
+      a[t] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + row * 128)[sub];
+      c[t] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dO) + row * 128)[sub];
+    } else {
+      a[t] = make_uint4(0u, 0u, 0u, 0u);
+      c[t] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kDeltaRowsPerWarp / 2; ++t) {
+    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&a[t]);
+    const __nv_bfloat162* y2 = reinterpret_cast<const __nv_bfloat162*>(&c[t]);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(x2[e]);
+      const float2 y = __bfloat1622float2(y2[e]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    const long long row = row0 + 2 * t + half;
+    if (sub == 0 && row < nrows) {
+      const int h = (int)(row % p.Hq);
+      const long long bi = row / p.Hq;
+      const int i = (int)(bi % p.L);
+      const int b = (int)(bi / p.L);
+      p.delta[((size_t)b * p.Hq + h) * p.L + i] = acc;
+    }
+  }
+}
+
 cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
   const long long nrows = (long long)p.B * p.L * p.Hq;
   const int warps = 8;
@@ -162,7 +209,8 @@ cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
   prof_begin(CAPATTN_KERNEL_DELTA, s);
   prof_count(CAPATTN_KERNEL_DELTA, 1);
   if (bf16) {
-    delta_kernel<__nv_bfloat16, 128><<<grid, warps * 32, 0, s>>>(p);
+    const long long per_block = (long long)warps * kDeltaRowsPerWarp;
+    delta_bf16_kernel<<<(unsigned)((nrows + per_block - 1) / per_block), warps * 32, 0, s>>>(p);
   } else if (p.D == 64) {
     delta_kernel<float, 64><<<grid, warps * 32, 0, s>>>(p);
   } else {

@@ -16,6 +16,7 @@ struct Pending {
 struct ProfState {
   std::mutex mu;
   bool on = false;
+  unsigned mask = (1u << CAPATTN_KERNEL_KINDS) - 1u;
   std::vector<cudaEvent_t> pool;
   std::vector<Pending> pending;
   Pending open[CAPATTN_KERNEL_KINDS];
@@ -45,7 +46,7 @@ cudaEvent_t take_event(ProfState& s) {
 void prof_begin(int kind, cudaStream_t stream) {
   ProfState& s = state();
   std::lock_guard<std::mutex> g(s.mu);
-  if (!s.on || kind < 0 || kind >= CAPATTN_KERNEL_KINDS) return;
+  if (!s.on || kind < 0 || kind >= CAPATTN_KERNEL_KINDS || !((s.mask >> kind) & 1u)) return;
   Pending p;
   p.kind = kind;
   p.start = take_event(s);
@@ -82,6 +83,14 @@ capattn_status capattn_profile_enable(int on) {
   ProfState& s = state();
   std::lock_guard<std::mutex> g(s.mu);
   s.on = on != 0;
+  return CAPATTN_OK;
+}
+
+capattn_status capattn_profile_select(unsigned int kind_mask) {
+  if (kind_mask >> CAPATTN_KERNEL_KINDS) return CAPATTN_ERR_INVALID_ARG;
+  ProfState& s = state();
+  std::lock_guard<std::mutex> g(s.mu);
+  s.mask = kind_mask;
   return CAPATTN_OK;
 }
 

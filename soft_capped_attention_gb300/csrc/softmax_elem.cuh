@@ -122,6 +122,18 @@ __device__ __forceinline__ float fmax3_abs(float acc, float a, float b) {
   return r;
 }
 
+// Three-input max / min.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // ---------------------------------------------------------------- packed fp32
 // Two fp32 lanes in one 64-bit register pair (fma/mul/add .f32x2).
 struct F2 {
