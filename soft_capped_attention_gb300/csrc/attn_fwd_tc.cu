@@ -7,24 +7,30 @@
 // Mosaic kernels.
 //
 // One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and walks
-// the union of their KV visit maps.  Warp roles (10 warps):
-//   warp 0      TMA producer: Q0, Q1 once, then K_j / V_j into a 2-stage ring;
-//   warp 1      TMEM allocator and MMA issuer (one thread), ping-ponging the
-//               two tiles so that one tile's softmax overlaps the other tile's
-//               MMAs:  S0_j S1_j | PV0_j S0_{j+1} | PV1_j S1_{j+1} | ...
-//                 S_t = Q_t K_j^T  (SS MMA, M = N = 128)
-//                 O_t += P_t V_j   (TS MMA: P_t read from TMEM as bf16)
-//   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1: one thread
-//               per query row (its TMEM lane).  Pass 1 takes the row maximum of
-//               the raw scores (every cap is increasing, so the logit maximum is
-//               the transformed raw maximum); pass 2 applies sm_scale, cap,
-//               temperature and the row's live span, writes P = 2^(x - m) as
-//               packed bf16 over the first 64 columns of S, and accumulates l.
-//               The running max is only moved (and O rescaled in TMEM) when it
-//               grows by more than 2^8; otherwise P stays <= 256.
+// the union of their KV visit maps.  Warp roles (18 warps):
+//   warp 0       TMA producer: Q0, Q1 once, then K_j / V_j into a 2-stage ring;
+//   warp 1       TMEM allocator and MMA issuer (warp-wide loop, one elected
+//                lane issues), ping-ponging the two tiles so that one tile's
+//                softmax overlaps the other tile's MMAs:
+//                  S0_j S1_j | PV0_j S0_{j+1} | PV1_j S1_{j+1} | ...
+//                  S_t = Q_t K_j^T  (SS MMA, M = N = 128)
+//                  O_t += P_t V_j   (TS MMA: P_t read from TMEM as bf16)
+//   warps 2..9   softmax of tile 0, warps 10..17 softmax of tile 1.  Each row
+//                (TMEM lane) is shared by two threads, one per half of the
+//                step's 128 key columns (warps 2..5 / 10..13 the first half).
+//                Pass 1 takes the range of the half-row's raw scores; the two
+//                halves exchange it through shared memory (every cap is
+//                increasing, so the logit maximum is the transformed raw
+//                maximum); pass 2 applies sm_scale, cap, temperature and the
+//                row's live span and writes P = 2^(x - m) as packed bf16 over
+//                the first 32 columns of the half; each half keeps its part of
+//                l.  The running max is only moved (and O rescaled in TMEM, each
+//                half its 64 columns of O) when it grows by more than 2^8;
+//                otherwise P stays <= 256.
 // A tile's S_{j+1} is issued after its PV_j, so when the softmax sees S_{j+1}
 // complete, PV_j is complete too and O may be rescaled in place.
-// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); packed P of a
+// tile's key columns [0, 64) at S [0, 32), of [64, 128) at S [64, 96).
 #include <math.h>
 
 #include "cap_math.cuh"
@@ -44,8 +50,16 @@ constexpr int NSTAGE = 2;
 constexpr int SLAB = 128 * 64 * 2;          // one [128][64] bf16 box
 constexpr int TILE = 2 * SLAB;               // 128 x 128 bf16
 constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 576;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+// Capped logits of a row lie in a window [x_hi - W, x_hi] (log2 units) known
+// before any score is seen: W = 2 |mul| for tanh and soft_sign (|f| < 1), |mul|
+// for ALSC (0 < f < 1).  With the fixed reference m = x_hi - max(0, W - kSpanLo)
+// every exponent x - m lies in [-kSpanLo, W - kSpanLo]: no term underflows
+// ex2's normal range and, while W <= kSpanMax, none overflows fp32 even summed
+// over a row of 2^20 keys.
+constexpr float kSpanLo = 120.0f;
+constexpr float kSpanMax = 220.0f;
 
 // Iterates the union of two rows of a visit bitmap, reporting per tile which
 // of the two query tiles is live in it.
@@ -92,21 +106,23 @@ __device__ __forceinline__ void issue_s(uint32_t d, uint64_t dQ, uint64_t dK) {
   }
 }
 
-// O += P V with P (bf16) in TMEM and V's MN-major descriptor.
+// O += P V with P (bf16) in TMEM (key columns [0, 64) packed at pt + [0, 32),
+// [64, 128) at pt + [64, 96)) and V's MN-major descriptor.
 __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pt, uint64_t dV, uint32_t acc0) {
   constexpr uint32_t idesc = idesc_bf16(BM, HD, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < BN / 16; ++ks)
-    mma_ts(d, pt + ks * 8, desc_add(dV, ks * 2048), idesc, (acc0 || ks > 0) ? 1u : 0u);
+    mma_ts(d, pt + (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4)), desc_add(dV, ks * 2048), idesc,
+           (acc0 || ks > 0) ? 1u : 0u);
 }
 
-// Maximum and minimum raw score over the live columns k0 .. k0 + 127 of one row.
-template <bool MASKED>
-__device__ __forceinline__ void row_range(const uint32_t (&v)[128], int k0, int4 ri, float& vmax,
+// Maximum and minimum raw score over the live columns k0 .. k0 + NC - 1 of one row.
+template <bool MASKED, int NC>
+__device__ __forceinline__ void row_range(const uint32_t (&v)[NC], int k0, int4 ri, float& vmax,
                                           float& vmin) {
   float a0 = -INFINITY, a1 = -INFINITY, b0 = INFINITY, b1 = INFINITY;
 #pragma unroll
-  for (int e = 0; e < 128; e += 2) {
+  for (int e = 0; e < NC; e += 2) {
     float x = __uint_as_float(v[e]), y = __uint_as_float(v[e + 1]);
     float xl = x, yl = y;
     if constexpr (MASKED) {
@@ -127,13 +143,12 @@ __device__ __forceinline__ void row_range(const uint32_t (&v)[128], int k0, int4
   vmin = fminf(b0, b1);
 }
 
-// Maximum (and, with NEED_MIN, minimum) raw score of a fully live row of 128
-// columns, with three-input max / min in two independent chains each.
-template <bool NEED_MIN>
-__device__ __forceinline__ void row_range_full(const uint32_t (&v)[128], float& vmax, float& vmin) {
+// Maximum (and, with NEED_MIN, minimum) raw score of NC fully live columns, with three-input max / min in two independent chains each.
+template <bool NEED_MIN, int NC>
+__device__ __forceinline__ void row_range_full(const uint32_t (&v)[NC], float& vmax, float& vmin) {
   float a0 = -INFINITY, a1 = -INFINITY, b0 = INFINITY, b1 = INFINITY;
 #pragma unroll
-  for (int e = 0; e < 128; e += 4) {
+  for (int e = 0; e < NC; e += 4) {
     const float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
     const float x2 = __uint_as_float(v[e + 2]), x3 = __uint_as_float(v[e + 3]);
     a0 = fmax3(a0, x0, x1);
@@ -147,28 +162,20 @@ __device__ __forceinline__ void row_range_full(const uint32_t (&v)[128], float& 
   vmin = NEED_MIN ? fminf(b0, b1) : vmax;
 }
 
-// 32 columns of P for the tanh cap when every |X * in| of the warp is within
-// the polynomial's range: the first POLY_PAIRS column pairs evaluate tanh on the
-// FMA pipe, the rest with tanh.approx; packed fp32x2 arithmetic throughout.
-template <bool MASKED, int POLY_PAIRS>
-__device__ __forceinline__ float p_chunk_tanh_fast(const uint32_t (&v)[32], uint32_t (&pk)[16],
-                                                   const Xf& xf, float mul, float addm, int j0,
-                                                   int4 ri, bool any) {
-  const F2 in2 = f2(xf.in, xf.in), mul2 = f2(mul, mul), add2 = f2(addm, addm);
+// NP column pairs of P for the tanh cap with the folded polynomial (every
+// |X * in| of the warp within the polynomial's range): x = X Q(X^2) + addm on
+// the FMA pipe, 2^x on MUFU.
+template <bool MASKED, int NP>
+__device__ __forceinline__ float p_chunk_tanh_fold(const uint32_t (&v)[2 * NP], uint32_t (&pk)[NP],
+                                                   const TanhFold& tf, float addm, int j0, int4 ri,
+                                                   bool any) {
+  const F2 add2 = f2(addm, addm);
   F2 acc = f2(0.f, 0.f);
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const F2 u = f2_mul(f2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), in2);
-    F2 t;
-    if (e < POLY_PAIRS) {
-      t = tanh_poly2(u);
-    } else {
-      float a, b;
-      f2_split(u, a, b);
-      t = f2(tanh_approx(a), tanh_approx(b));
-    }
+  for (int e = 0; e < NP; ++e) {
     float x0, x1;
-    f2_split(f2_fma(t, mul2, add2), x0, x1);
+    f2_split(tanh_fold_eval(f2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), tf, add2),
+             x0, x1);
     float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
     if constexpr (MASKED) {
       const int ja = j0 + 2 * e, jb = ja + 1;
@@ -183,15 +190,15 @@ __device__ __forceinline__ float p_chunk_tanh_fast(const uint32_t (&v)[32], uint
   return s0 + s1;
 }
 
-// 32 columns of P = 2^(mul * f(X) + addm), packed to bf16 into pk; returns
+// NP column pairs of P = 2^(mul * f(X) + addm), packed to bf16 into pk; returns
 // their sum.  (No TMEM access here: callers branch per row, and the warp-wide
 // tcgen05 store must run after the branch has reconverged.)
-template <int METHOD, bool MASKED>
-__device__ __forceinline__ float p_chunk(const uint32_t (&v)[32], uint32_t (&pk)[16], const Xf& xf,
+template <int METHOD, bool MASKED, int NP>
+__device__ __forceinline__ float p_chunk(const uint32_t (&v)[2 * NP], uint32_t (&pk)[NP], const Xf& xf,
                                          float mul, float addm, int j0, int4 ri, bool any) {
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
+  for (int e = 0; e < NP; ++e) {
     float p0 = ex2_approx(fmaf(mul, cap_f<METHOD>(__uint_as_float(v[2 * e]), xf), addm));
     float p1 = ex2_approx(fmaf(mul, cap_f<METHOD>(__uint_as_float(v[2 * e + 1]), xf), addm));
     if constexpr (MASKED) {
@@ -206,20 +213,32 @@ __device__ __forceinline__ float p_chunk(const uint32_t (&v)[32], uint32_t (&pk)
   return s0 + s1;
 }
 
-constexpr int kPolyPairs = 10;  // of 16 column pairs per chunk: tanh on the FMA pipe
-
+// Whether the warp may take the folded tanh polynomial for 16 raw scores
+// (every |X * in| within its range); always false for the other caps.
 template <int METHOD>
-__device__ __forceinline__ float p_dispatch(bool full_any, bool poly, const uint32_t (&v)[32],
-                                           uint32_t (&pk)[16], const Xf& xf, float mul, float addm,
-                                           int j0, int4 ri, bool any) {
+__device__ __forceinline__ bool sub_poly(const uint32_t (&v)[16], const TanhFold& tf, const Xf& xf) {
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    float am = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) am = fmax3_abs(am, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+    return __all_sync(0xFFFFFFFFu, tf.ok && am * fabsf(xf.in) <= kTanhPolyMaxU);
+  }
+  return false;
+}
+
+// 16 columns of P (8 packed pairs): masked or not, FMA-pipe tanh or not.
+template <int METHOD>
+__device__ __forceinline__ float p_dispatch(bool full_any, bool poly, const uint32_t (&v)[16],
+                                           uint32_t (&pk)[8], const Xf& xf, const TanhFold& tf,
+                                           float mul, float addm, int j0, int4 ri, bool any) {
   if constexpr (METHOD == CAPATTN_CAP_TANH) {
     if (poly) {
-      return full_any ? p_chunk_tanh_fast<false, kPolyPairs>(v, pk, xf, mul, addm, j0, ri, any)
-                      : p_chunk_tanh_fast<true, kPolyPairs>(v, pk, xf, mul, addm, j0, ri, any);
+      return full_any ? p_chunk_tanh_fold<false, 8>(v, pk, tf, addm, j0, ri, any)
+                      : p_chunk_tanh_fold<true, 8>(v, pk, tf, addm, j0, ri, any);
     }
   }
-  return full_any ? p_chunk<METHOD, false>(v, pk, xf, mul, addm, j0, ri, any)
-                  : p_chunk<METHOD, true>(v, pk, xf, mul, addm, j0, ri, any);
+  return full_any ? p_chunk<METHOD, false, 8>(v, pk, xf, mul, addm, j0, ri, any)
+                  : p_chunk<METHOD, true, 8>(v, pk, xf, mul, addm, j0, ri, any);
 }
 
 template <int METHOD>
@@ -230,6 +249,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   __shared__ __align__(8) uint64_t bars[16];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  // half-row partial results exchanged between the two halves of a row:
+  // [step parity][tile][half][row] = (max, min) of the half's raw scores,
+  // and at the end (l of the half, unused)
+  __shared__ float2 xch[2][2][2][BM];
 
   const int hb = blockIdx.x;
   const int h = hb % p.Hq, b = hb / p.Hq;
@@ -251,6 +274,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const uint32_t bar_sfull = smem_u32(&bars[7]);   // + tile*8
   const uint32_t bar_pfull = smem_u32(&bars[9]);   // + tile*8
   const uint32_t bar_final = smem_u32(&bars[11]);
+  const uint32_t bar_xch = smem_u32(&bars[12]);    // + tile*8: both halves of the rows wrote xch
 
   const uint32_t* map0 = p.qmap + ((size_t)b * p.nq + qt0) * p.wk;
   const uint32_t* map1 = has1 ? map0 + p.wk : nullptr;
@@ -265,7 +289,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_sfull + 8 * t, 1);
-      mbar_init(bar_pfull + 8 * t, 4);
+      mbar_init(bar_pfull + 8 * t, 8);
+      mbar_init(bar_xch + 8 * t, 8);
     }
     mbar_init(bar_final, 1);
     fence_mbar_init();
@@ -279,6 +304,30 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int n = count_union(map0, map1, p.wk);
+
+  // Softmax rows (warps 2..17): per-row constants, and whether every row of the
+  // CTA can use a fixed reference instead of the running max (capped method,
+  // logit window <= kSpanMax, and the running max m / sum l not requested).
+  const int sw = warp - 2;                     // 0..15 for softmax warps
+  const int tsel = (sw >> 3) & 1;              // query tile 0 or 1
+  const int half = (sw >> 2) & 1;              // key columns [64 half, 64 half + 64) of each step
+  const int r = (warp & 3) * 32 + lane;
+  const int i = (qt0 + tsel) * BM + r;
+  const bool valid = warp >= 2 && i < p.L;
+  const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
+  float rmul, radd;
+  row_consts<METHOD>(p.cap, p.sm_scale, temp, &rmul, &radd);
+  float x_hi = 0.f, span = 0.f;
+  if constexpr (METHOD == CAPATTN_CAP_TANH || METHOD == CAPATTN_CAP_SOFT_SIGN) {
+    x_hi = fabsf(rmul);
+    span = 2.f * fabsf(rmul);
+  } else if constexpr (METHOD == CAPATTN_CAP_ALSC) {
+    x_hi = fmaxf(radd, rmul + radd);
+    span = fabsf(rmul);
+  }
+  const bool fixed_ref = (METHOD != CAPATTN_CAP_NONE) && p.m == nullptr && p.l == nullptr &&
+                         __syncthreads_and(warp < 2 || span <= kSpanMax);
+  const float m_fixed = x_hi - fmaxf(0.f, span - kSpanLo);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -392,24 +441,21 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int tsel = (warp - 2) >> 2;          // query tile 0 or 1
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const int i = (qt0 + tsel) * BM + r;
-    const bool valid = i < p.L;
-    const uint32_t s_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)tsel * 128u;
-    const uint32_t o_base = tmem + ((uint32_t)(quarter * 32) << 16) + 256u + (uint32_t)tsel * 128u;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_base = tmem + lane_off + (uint32_t)tsel * 128u + 64u * (uint32_t)half;
+    const uint32_t o_base = tmem + lane_off + 256u + (uint32_t)tsel * 128u + 64u * (uint32_t)half;
     const uint32_t my_sfull = bar_sfull + 8 * tsel, my_pfull = bar_pfull + 8 * tsel;
+    const uint32_t my_xch = bar_xch + 8 * tsel;
     const int4 ri = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
-    const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
     const bool neg = temp < 0.f;
     // the row minimum is needed for a negative temperature and for the range
     // check of the tanh polynomial
     const bool need_min = (METHOD == CAPATTN_CAP_TANH) || __any_sync(0xFFFFFFFFu, neg);
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
-    float rmul, radd;
-    row_consts<METHOD>(p.cap, p.sm_scale, temp, &rmul, &radd);
-    float m_use = -INFINITY, m_true = -INFINITY, lsum = 0.f;
+    TanhFold tf{};
+    if constexpr (METHOD == CAPATTN_CAP_TANH) tf = tanh_fold(xf.in, rmul);
+    float m_use = fixed_ref ? m_fixed : -INFINITY, m_true = -INFINITY, lsum = 0.f;
     int cnt = 0;
     bool aborted = false;
     PairIter it(map0, map1, p.wk);
@@ -418,48 +464,61 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     while (it.next(t, a0, a1)) {
       if (!(tsel == 0 ? a0 : a1)) continue;
       const int k0 = t * BN;
+      const int c0 = k0 + 64 * half;           // first key column of this half
       if (!mbar_wait_warp(my_sfull, cnt & 1, p.status, &abort_flag)) {
         aborted = true;
         break;
       }
       tc_fence_after();
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BN);
-      // ---- pass 1: range of the live raw scores (one batched TMEM read)
+      float alpha = 1.f;
+      bool poly = false;
+      if (!fixed_ref) {
+      // ---- pass 1: range of the half-row's live raw scores, kept in registers
+      uint32_t v[64];
+      tmem_ld32(s_base, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(s_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_wait_ld();
       float vmax, vmin;
+      if (!full)
+        row_range<true, 64>(v, c0, ri, vmax, vmin);
+      else if (need_min)
+        row_range_full<true, 64>(v, vmax, vmin);
+      else
+        row_range_full<false, 64>(v, vmax, vmin);
+      // ---- combine with the other half of the row
+      xch[cnt & 1][tsel][half][r] = make_float2(vmax, vmin);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(my_xch);
+      if (!mbar_wait_warp(my_xch, cnt & 1, p.status, &abort_flag)) {
+        aborted = true;
+        break;
+      }
       {
-        uint32_t v[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(s_base + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-        tmem_wait_ld();
-        if (!full)
-          row_range<true>(v, k0, ri, vmax, vmin);
-        else if (need_min)
-          row_range_full<true>(v, vmax, vmin);
-        else
-          row_range_full<false>(v, vmax, vmin);
+        const float2 other = xch[cnt & 1][tsel][half ^ 1][r];
+        vmax = fmaxf(vmax, other.x);
+        vmin = fminf(vmin, other.y);
       }
       // Every cap is increasing: the logit maximum is the transform of the raw
       // maximum (of the minimum for a negative temperature).
       const float xsel = neg ? vmin : vmax;
       const float x_max =
           (vmax == -INFINITY) ? -INFINITY : fmaf(rmul, cap_f<METHOD>(xsel, xf), radd);
-      // tanh on the FMA pipe when the whole warp's arguments are in range
-      bool poly = false;
+      // tanh on the FMA pipe when the whole warp's arguments are in range (the
+      // two halves of a row see the same range, so they decide alike)
       if constexpr (METHOD == CAPATTN_CAP_TANH)
-        poly = __all_sync(0xFFFFFFFFu, fmaxf(vmax, -vmin) * fabsf(xf.in) <= kTanhPolyMaxU);
+        poly = __all_sync(0xFFFFFFFFu, tf.ok && fmaxf(vmax, -vmin) * fabsf(xf.in) <= kTanhPolyMaxU);
       m_true = fmaxf(m_true, x_max);
       const float m_new = fmaxf(m_use, x_max);
       const bool resc = m_new > m_use + kRescaleThreshold;
-      float alpha = 1.f;
       if (resc) {
         alpha = ex2_approx(m_use - m_new);
         m_use = m_new;
       }
-      // ---- O rescale (PV of the previous live tile is complete)
+      // ---- O rescale of this half's 64 columns (PV of the previous live tile is complete)
       if (cnt > 0 && __any_sync(0xFFFFFFFFu, resc)) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
           tmem_ld32(o_base + c * 32, o);
           tmem_wait_ld();
@@ -468,28 +527,32 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           tmem_st32(o_base + c * 32, o);
         }
       }
-      // ---- pass 2: P = 2^(x - m_use), packed bf16 over S columns [0, 64).
-      // The next chunk's TMEM load is issued before the current chunk is computed.
+      }  // !fixed_ref
+      // ---- pass 2: P = 2^(x - m_use), packed bf16 over this half's columns [0, 32)
       const bool any = m_use != -INFINITY;
       const float addm = radd - (any ? m_use : 0.f);
       const bool fast = full && any;
+      // Sub-chunk c (16 columns) is reloaded from TMEM (the next one's load in
+      // flight while it is computed) and packed over columns [8 c, 8 c + 8).
       float psum = 0.f;
       {
-        uint32_t va[32], vb[32], pk[16];
-        tmem_ld32(s_base, va);
+        uint32_t va[16], vb[16], pk[8];
+        tmem_ld16(s_base, va);
         tmem_wait_ld();
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < 4; c += 2) {
-          tmem_ld32(s_base + (c + 1) * 32, vb);
-          psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, rmul, addm, k0 + c * 32, ri, any);
+          tmem_ld16(s_base + 16 * (c + 1), vb);
+          if (fixed_ref) poly = sub_poly<METHOD>(va, tf, xf);
+          psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, tf, rmul, addm, c0 + 16 * c, ri, any);
           __syncwarp();
-          tmem_st16(s_base + c * 16, pk);
+          tmem_st8(s_base + 8 * c, pk);
           tmem_wait_ld();
-          if (c + 2 < 4) tmem_ld32(s_base + (c + 2) * 32, va);
-          psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, rmul, addm, k0 + (c + 1) * 32, ri, any);
+          if (c + 2 < 4) tmem_ld16(s_base + 16 * (c + 2), va);
+          if (fixed_ref) poly = sub_poly<METHOD>(vb, tf, xf);
+          psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, tf, rmul, addm, c0 + 16 * (c + 1), ri, any);
           __syncwarp();
-          tmem_st16(s_base + (c + 1) * 16, pk);
-          tmem_wait_ld();
+          tmem_st8(s_base + 8 * (c + 1), pk);
+          if (c + 2 < 4) tmem_wait_ld();
         }
       }
       lsum = lsum * alpha + psum;
@@ -500,16 +563,31 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       ++cnt;
     }
     // ---------------------------------------------------------- epilogue
+    // l of the whole row: the two halves add their parts (one more exchange;
+    // with the running max every step used one exchange phase, with the fixed
+    // reference none did)
+    float l_row = lsum;
+    if (cnt > 0 && !aborted) {
+      const int xp = fixed_ref ? 0 : (cnt & 1);
+      xch[xp][tsel][half][r] = make_float2(lsum, 0.f);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(my_xch);
+      if (mbar_wait_warp(my_xch, xp, p.status, &abort_flag))
+        l_row = lsum + xch[xp][tsel][half ^ 1][r].x;
+      else
+        aborted = true;
+    }
     bool have_o = false;
     if (cnt > 0 && !aborted) {
       have_o = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
-    const bool live = lsum > 0.f;
-    const float inv = live ? 1.f / lsum : 0.f;
-    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.o) + ((size_t)(b * p.L + i) * p.Hq + h) * HD;
+    const bool live = l_row > 0.f;
+    const float inv = live ? 1.f / l_row : 0.f;
+    __nv_bfloat16* og =
+        static_cast<__nv_bfloat16*>(p.o) + ((size_t)(b * p.L + i) * p.Hq + h) * HD + 64 * half;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t o[32];
       if (have_o) {
         tmem_ld32(o_base + c * 32, o);
@@ -528,11 +606,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
       }
     }
-    if (valid) {
+    if (valid && half == 0) {
       const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
-      p.lse[rr] = live ? (m_use + log2f(lsum)) * kLn2 : -INFINITY;
+      p.lse[rr] = live ? (m_use + log2f(l_row)) * kLn2 : -INFINITY;
       if (p.m) p.m[rr] = live ? m_true * kLn2 : -INFINITY;
-      if (p.l) p.l[rr] = live ? lsum * ex2_approx(m_use - m_true) : 0.f;
+      if (p.l) p.l[rr] = live ? l_row * ex2_approx(m_use - m_true) : 0.f;
     }
   }
   __syncwarp();  // warps 0 and 1 reach the CTA barrier converged

@@ -175,6 +175,42 @@ constexpr float kTanhC1 = 0.133239388f;
 constexpr float kTanhC2 = -0.0529243536f;
 constexpr float kTanhC3 = 0.0170059651f;
 
+// The same polynomial with the argument scale `in` and an output scale `mul`
+// folded into its coefficients: mul * tanh(in * X) = X * Q(X^2), Q(z) = K0 + z (K1 + z (K2 + z (K3 + z K4))),
+// K0 = mul in, K(k+1) = mul c_k in^(2k+3).  Evaluating Q in fp32 keeps the
+// result within 2e-7 * mul of mul * tanh (tests/test_tanh_poly.py bounds
+// it); the coefficients stay normal floats while |K4| >= 1e-30, which callers
+// check before taking this form.
+struct TanhFold {
+  F2 k0, k1, k2, k3, k4;
+  bool ok;  // coefficients usable (no underflow)
+};
+__device__ __forceinline__ TanhFold tanh_fold(float in, float mul) {
+  const float w = in * in;
+  const float a0 = mul * in;
+  const float a1 = a0 * w * kTanhC0;
+  const float a2 = a0 * w * w * kTanhC1;
+  const float a3 = a0 * w * w * w * kTanhC2;
+  const float a4 = a0 * w * w * w * w * kTanhC3;
+  TanhFold t;
+  t.k0 = f2(a0, a0);
+  t.k1 = f2(a1, a1);
+  t.k2 = f2(a2, a2);
+  t.k3 = f2(a3, a3);
+  t.k4 = f2(a4, a4);
+  t.ok = (mul == 0.f) || (fabsf(a4) >= 1e-30f);
+  return t;
+}
+// x = X * Q(X^2) + add for a pair of raw scores.
+__device__ __forceinline__ F2 tanh_fold_eval(F2 X, const TanhFold& t, F2 add) {
+  const F2 z = f2_mul(X, X);
+  F2 q = f2_fma(t.k4, z, t.k3);
+  q = f2_fma(q, z, t.k2);
+  q = f2_fma(q, z, t.k1);
+  q = f2_fma(q, z, t.k0);
+  return f2_fma(X, q, add);
+}
+
 __device__ __forceinline__ F2 tanh_poly2(F2 u) {
   const F2 w = f2_mul(u, u);
   F2 p = f2_fma(f2(kTanhC3, kTanhC3), w, f2(kTanhC2, kTanhC2));

@@ -176,3 +176,44 @@ def test_autograd_function_matches_direct_calls():
     dq, dk, dv, _ = ca.capattn_bwd(q, k, v, o2, lse, do, ap, temp)
     assert torch.equal(o, o2)
     assert torch.equal(qq.grad, dq) and torch.equal(kk.grad, dk) and torch.equal(vv.grad, dv)
+
+
+def test_fixed_reference_and_running_max_agree_bf16():
+    # Capped rows without m / l requested take the fixed reference; asking for
+    # m / l switches to the running max.  Both must match the oracle.
+    inp = make_case(2, 333, 4, 2, 128, torch.bfloat16, "causal", True, seed=21)
+    ap = params("tanh", "causal", 0.0)
+    ref = run_oracle(inp, ap)
+    a = run_gpu(inp, ap, torch.bfloat16, want_ml=False)
+    b = run_gpu(inp, ap, torch.bfloat16, want_ml=True)
+    compare(a, ref, torch.bfloat16)
+    compare(b, ref, torch.bfloat16)
+
+
+def test_scores_at_the_bottom_of_the_cap_window():
+    # Every score far below -cap: all capped logits sit near the low end of the
+    # tanh window, where the fixed reference puts exponents near -120.  The
+    # softmax is then nearly uniform and must still match the oracle.
+    B, L, H, D = 1, 256, 2, 128
+    rng = np.random.default_rng(31)
+    base = np.abs(rng.standard_normal((B, L, H, D))).astype(np.float32) + 0.5
+    inp = {"q": round_to_bf16(base * 4.0), "k": round_to_bf16(-base * 4.0),
+           "v": round_to_bf16(rng.standard_normal((B, L, H, D)).astype(np.float32)),
+           "do": round_to_bf16(rng.standard_normal((B, L, H, D)).astype(np.float32)),
+           "temp": None, "seg": None, "bounds": None}
+    ap = params("tanh", "full", 0.0)
+    got, ref = run_gpu(inp, ap, torch.bfloat16), run_oracle(inp, ap)
+    # the forward is what the fixed reference changes (the saturated cap leaves
+    # the score gradients near zero, where a relative comparison says little)
+    assert np.max(np.abs(got["O"] - ref["O"])) <= 2e-2
+    assert np.all(np.isfinite(got["LSE"]))
+    assert np.max(np.abs(got["LSE"] - ref["LSE"])) <= 1e-3
+
+
+def test_wide_cap_window_uses_running_max():
+    # tanh cap 200: the logit window (2 * 200 * log2 e) is wider than the fixed
+    # reference allows, so the forward keeps the running max.
+    inp = make_case(1, 300, 2, 2, 128, torch.bfloat16, "causal", False, seed=41, scale=3.0)
+    ap = ca.AttnParams(sm_scale=float(1.0 / np.sqrt(128.0)), cap_method="tanh", cap=200.0, alpha=0.0,
+                       beta=0.0, causal=True, window_len=0, z_loss_weight=0.0)
+    compare(run_gpu(inp, ap, torch.bfloat16), run_oracle(inp, ap), torch.bfloat16)
