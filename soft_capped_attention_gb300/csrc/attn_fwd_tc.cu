@@ -213,6 +213,14 @@ __device__ __forceinline__ float p_chunk(const uint32_t (&v)[2 * NP], uint32_t (
   return s0 + s1;
 }
 
+// Whether no row of the warp has a live key among the 16 columns j0 .. j0 + 15
+// (live span [ri.x, ri.y) plus the extra column ri.z).  A warp-wide vote: every
+// lane of the warp must call it.
+__device__ __forceinline__ bool sub_dead(int4 ri, int j0) {
+  const bool live = (ri.x < j0 + 16 && ri.y > j0 && ri.x < ri.y) || (ri.z >= j0 && ri.z < j0 + 16);
+  return __all_sync(0xFFFFFFFFu, !live);
+}
+
 // Whether the warp may take the folded tanh polynomial for 16 raw scores
 // (every |X * in| within its range); always false for the other caps.
 template <int METHOD>
@@ -471,6 +479,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       tc_fence_after();
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BN);
+      const bool warp_partial = __any_sync(0xFFFFFFFFu, !full);
       float alpha = 1.f;
       bool poly = false;
       if (!fixed_ref) {
@@ -542,14 +551,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
         for (int c = 0; c < 4; c += 2) {
           tmem_ld16(s_base + 16 * (c + 1), vb);
-          if (fixed_ref) poly = sub_poly<METHOD>(va, tf, xf);
-          psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, tf, rmul, addm, c0 + 16 * c, ri, any);
+          // (warp-wide vote, taken only in steps with partially masked rows)
+          if (warp_partial && sub_dead(ri, c0 + 16 * c)) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = 0u;
+          } else {
+            if (fixed_ref) poly = sub_poly<METHOD>(va, tf, xf);
+            psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, tf, rmul, addm, c0 + 16 * c, ri, any);
+          }
           __syncwarp();
           tmem_st8(s_base + 8 * c, pk);
           tmem_wait_ld();
           if (c + 2 < 4) tmem_ld16(s_base + 16 * (c + 2), va);
-          if (fixed_ref) poly = sub_poly<METHOD>(vb, tf, xf);
-          psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, tf, rmul, addm, c0 + 16 * (c + 1), ri, any);
+          // (warp-wide vote, taken only in steps with partially masked rows)
+          if (warp_partial && sub_dead(ri, c0 + 16 * (c + 1))) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = 0u;
+          } else {
+            if (fixed_ref) poly = sub_poly<METHOD>(vb, tf, xf);
+            psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, tf, rmul, addm, c0 + 16 * (c + 1), ri, any);
+          }
           __syncwarp();
           tmem_st8(s_base + 8 * (c + 1), pk);
           if (c + 2 < 4) tmem_wait_ld();
