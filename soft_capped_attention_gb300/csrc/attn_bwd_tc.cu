@@ -623,6 +623,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   __shared__ __align__(8) uint64_t bars[20];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ float dxch[2][BT];   // half-row sums of O * dO (delta), one per warpgroup
 
   const int hb = blockIdx.x;
   const int h = hb % p.Hq, b = hb / p.Hq;
@@ -643,6 +644,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   const uint32_t bar_sfree = smem_u32(&bars[7]);
   const uint32_t bar_chunk = smem_u32(&bars[8]);   // + c*8: chunk c packed by both warpgroups
   const uint32_t bar_final = smem_u32(&bars[16]);
+  const uint32_t bar_dx = smem_u32(&bars[17]);     // both warpgroups wrote their delta halves
 
   const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
   if (threadIdx.x == 0) {
@@ -657,6 +659,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     mbar_init(bar_sfree, 8);
     for (int c = 0; c < 4; ++c) mbar_init(bar_chunk + 8 * c, 8);
     mbar_init(bar_final, 1);
+    mbar_init(bar_dx, 8);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -783,7 +786,50 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
     const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
     const float lse = valid ? p.lse[rr] : -INFINITY;
-    const float dl = valid ? p.delta[rr] : 0.f;
+    bool aborted = false;
+    // delta_i = rowsum(O * dO) (the pre-pass of the backward), computed here for
+    // the tile's rows: each warpgroup sums its 64 dims, O from global memory and
+    // dO from the tile staged for the dP MMAs (128-byte swizzle: the 16-byte
+    // chunk c of row r sits at chunk c ^ (r % 8)); the halves add through shared
+    // memory.  A tile with no visited KV tile has only fully masked rows, whose
+    // O and delta are 0.
+    float dl = 0.f;
+    {
+      float dpart = 0.f;
+      if (n > 0) {
+        // O is loaded first, so that its latency overlaps the wait for the tiles
+        uint4 orow_g[8];
+        if (valid) {
+          const uint4* og = reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(p.o) + ((size_t)(b * p.L + i) * p.Hq + h) * HD + 64 * wg);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) orow_g[c] = og[c];
+        }
+        if (!mbar_wait_warp(bar_q, 0, p.status, &abort_flag)) aborted = true;
+        if (valid && !aborted) {
+          const uint8_t* orow = smem_raw + (sO - smem_u32(smem_raw)) + wg * SLAB + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 a = orow_g[c];
+            const uint4 d = *reinterpret_cast<const uint4*>(orow + ((c ^ (r & 7)) << 4));
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, dv4[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+              const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv4[e]));
+              dpart = fmaf(x.x, y.x, dpart);
+              dpart = fmaf(x.y, y.y, dpart);
+            }
+          }
+        }
+        dxch[wg][r] = dpart;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dx);
+        if (!mbar_wait_warp(bar_dx, 0, p.status, &abort_flag)) aborted = true;
+        dl = dpart + dxch[wg ^ 1][r];
+      }
+      if (wg == 0 && valid) p.delta[rr] = dl;
+    }
     const bool fin = isfinite(lse);
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
     ColPair rc;
@@ -796,7 +842,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       rc.a = make_float4(mul, mul, addl, addl);
       rc.b = make_float4(-dsc, -dsc, -dsc * radd, -dsc * radd);
     }
-    bool aborted = false;
     TileIter it(map, p.wk);
     for (int j = 0; j < n; ++j) {
       int t;
@@ -882,15 +927,7 @@ struct BwdTcLaunch {
     if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.L, p.Hkv, HD, BT);
     if (e == cudaSuccess) e = make_bhld_map(&mdo, p.dO, p.B, p.L, p.Hq, HD, BT);
     if (e != cudaSuccess) return e;
-    auto kdkv = dkv_tc_kernel<METHOD>;
-    e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    prof_begin(CAPATTN_KERNEL_DKV, s);
-    prof_count(CAPATTN_KERNEL_DKV, 1);
-    kdkv<<<dim3(p.Hkv * p.B, p.nk), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, mdo, p);
-    prof_end(CAPATTN_KERNEL_DKV, s);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // dQ first: it also computes delta, which the dK/dV kernel reads.
     auto kdq = dq_tc_kernel<METHOD>;
     e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -898,6 +935,15 @@ struct BwdTcLaunch {
     prof_count(CAPATTN_KERNEL_DQ, 1);
     kdq<<<dim3(p.Hq * p.B, p.nq), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, mdo, p);
     prof_end(CAPATTN_KERNEL_DQ, s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kdkv = dkv_tc_kernel<METHOD>;
+    e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_DKV, s);
+    prof_count(CAPATTN_KERNEL_DKV, 1);
+    kdkv<<<dim3(p.Hkv * p.B, p.nk), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, mdo, p);
+    prof_end(CAPATTN_KERNEL_DKV, s);
     return cudaGetLastError();
   }
 };

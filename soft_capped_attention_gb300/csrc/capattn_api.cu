@@ -206,8 +206,11 @@ capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void*
   p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta;
   cudaError_t e = launch_prepass(p, true, stream);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_delta(p, cfg->dtype == CAPATTN_BF16, stream);
-  if (e != cudaSuccess) return cuda_status(e);
+  // bf16: the dQ kernel computes delta itself; fp32: a separate pass
+  if (cfg->dtype != CAPATTN_BF16) {
+    e = launch_delta(p, false, stream);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   e = (cfg->dtype == CAPATTN_BF16) ? launch_bwd_bf16(p, stream) : launch_bwd_fp32(p, stream);
   return cuda_status(e);
 }
