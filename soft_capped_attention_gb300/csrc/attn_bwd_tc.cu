@@ -291,6 +291,9 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
   }
+  // the setup above overlaps the previous kernel's tail; global memory only after it
+  pdl_trigger();
+  pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -666,6 +669,9 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
   }
+  // the setup above overlaps the previous kernel's tail; global memory only after it
+  pdl_trigger();
+  pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -933,7 +939,8 @@ struct BwdTcLaunch {
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_DQ, s);
     prof_count(CAPATTN_KERNEL_DQ, 1);
-    kdq<<<dim3(p.Hq * p.B, p.nq), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, mdo, p);
+    e = launch_pdl(kdq, dim3(p.Hq * p.B, p.nq), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, p);
+    if (e != cudaSuccess) return e;
     prof_end(CAPATTN_KERNEL_DQ, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -942,7 +949,8 @@ struct BwdTcLaunch {
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_DKV, s);
     prof_count(CAPATTN_KERNEL_DKV, 1);
-    kdkv<<<dim3(p.Hkv * p.B, p.nk), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, mdo, p);
+    e = launch_pdl(kdkv, dim3(p.Hkv * p.B, p.nk), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, p);
+    if (e != cudaSuccess) return e;
     prof_end(CAPATTN_KERNEL_DKV, s);
     return cudaGetLastError();
   }

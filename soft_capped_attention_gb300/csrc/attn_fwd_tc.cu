@@ -307,6 +307,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
   }
+  // the setup above overlaps the previous kernel's tail; global memory only after it
+  pdl_trigger();
+  pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -660,7 +663,8 @@ struct FwdTcLaunch {
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_FWD, s);
     prof_count(CAPATTN_KERNEL_FWD, 1);
-    kern<<<dim3(p.Hq * p.B, (p.nq + 1) / 2), NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+    e = launch_pdl(kern, dim3(p.Hq * p.B, (p.nq + 1) / 2), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, p);
+    if (e != cudaSuccess) return e;
     prof_end(CAPATTN_KERNEL_FWD, s);
     return cudaGetLastError();
   }

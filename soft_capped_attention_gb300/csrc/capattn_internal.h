@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/capattn.h"
 #include "status_bits.h"
 
@@ -67,6 +69,33 @@ WorkspaceLayout workspace_layout(const capattn_config& c, int block_q, int block
 void prof_begin(int kind, cudaStream_t stream);
 void prof_end(int kind, cudaStream_t stream);
 void prof_count(int kind, int n);
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel of the stream finishes; every kernel launched this
+// way waits for its predecessor (griddepcontrol.wait) before it touches global
+// memory, and lets its own dependents be scheduled from its start.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+#ifdef __CUDACC__
+// Device side of the above: let the next kernel of the stream be scheduled now /
+// wait until the previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
 
 // Launchers.  Each returns cudaGetLastError() after the launch.
 cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s);

@@ -11,6 +11,8 @@ namespace capattn {
 // One thread per (b, i): the run of equal segment ids around i (binary search
 // on a non-decreasing row), the clamped ranker bounds, and the row's span.
 __global__ void rowinfo_kernel(Params p) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= p.L) return;
@@ -54,6 +56,8 @@ __device__ __forceinline__ void set_bit_range(uint32_t* bm, int a, int c) {
 __global__ void qmap_kernel(Params p) {
   extern __shared__ uint32_t bm[];
   __shared__ int full_lo, full_hi;
+  pdl_trigger();
+  pdl_wait();
   const int qt = blockIdx.x, b = blockIdx.y;
   for (int w = threadIdx.x; w < p.wk; w += blockDim.x) bm[w] = 0u;
   if (threadIdx.x == 0) {
@@ -87,6 +91,8 @@ __global__ void qmap_kernel(Params p) {
 
 // One CTA per (KV tile, b): transpose of the query-tile map.
 __global__ void kmap_kernel(Params p) {
+  pdl_trigger();
+  pdl_wait();
   const int kt = blockIdx.x, b = blockIdx.y;
   for (int w = threadIdx.x; w < p.wq; w += blockDim.x) {
     uint32_t word = 0u;
@@ -104,12 +110,15 @@ cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
   prof_begin(CAPATTN_KERNEL_PREPASS, s);
   prof_count(CAPATTN_KERNEL_PREPASS, build_kmap ? 3 : 2);
   dim3 g1((p.L + 255) / 256, p.B);
-  rowinfo_kernel<<<g1, 256, 0, s>>>(p);
+  cudaError_t e = launch_pdl(rowinfo_kernel, g1, dim3(256), 0, s, p);
+  if (e != cudaSuccess) return e;
   dim3 g2(p.nq, p.B);
-  qmap_kernel<<<g2, 128, p.wk * sizeof(uint32_t), s>>>(p);
+  e = launch_pdl(qmap_kernel, g2, dim3(128), p.wk * sizeof(uint32_t), s, p);
+  if (e != cudaSuccess) return e;
   if (build_kmap) {
     dim3 g3(p.nk, p.B);
-    kmap_kernel<<<g3, 32, 0, s>>>(p);
+    e = launch_pdl(kmap_kernel, g3, dim3(32), 0, s, p);
+    if (e != cudaSuccess) return e;
   }
   prof_end(CAPATTN_KERNEL_PREPASS, s);
   return cudaGetLastError();
@@ -119,6 +128,8 @@ cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
 // One warp per (b, i, h) row of D elements: delta[b, h, i] = sum_d O * dO.
 template <typename T, int D>
 __global__ void delta_kernel(Params p) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int VEC = D / 32;
   const long long row = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -161,6 +172,8 @@ __global__ void delta_kernel(Params p) {
 constexpr int kDeltaRowsPerWarp = 8;
 
 __global__ void delta_bf16_kernel(Params p) {
+  pdl_trigger();
+  pdl_wait();
   const long long nrows = (long long)p.B * p.L * p.Hq;
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, sub = lane & 15;
@@ -210,11 +223,15 @@ cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
   prof_count(CAPATTN_KERNEL_DELTA, 1);
   if (bf16) {
     const long long per_block = (long long)warps * kDeltaRowsPerWarp;
-    delta_bf16_kernel<<<(unsigned)((nrows + per_block - 1) / per_block), warps * 32, 0, s>>>(p);
+    const cudaError_t e = launch_pdl(delta_bf16_kernel, dim3((unsigned)((nrows + per_block - 1) / per_block)),
+                                     dim3(warps * 32), 0, s, p);
+    if (e != cudaSuccess) return e;
   } else if (p.D == 64) {
-    delta_kernel<float, 64><<<grid, warps * 32, 0, s>>>(p);
+    const cudaError_t e = launch_pdl(delta_kernel<float, 64>, dim3(grid), dim3(warps * 32), 0, s, p);
+    if (e != cudaSuccess) return e;
   } else {
-    delta_kernel<float, 128><<<grid, warps * 32, 0, s>>>(p);
+    const cudaError_t e = launch_pdl(delta_kernel<float, 128>, dim3(grid), dim3(warps * 32), 0, s, p);
+    if (e != cudaSuccess) return e;
   }
   prof_end(CAPATTN_KERNEL_DELTA, s);
   return cudaGetLastError();
