@@ -131,20 +131,20 @@ struct ColPair {
 // P and dX of one pair of scores of a key row, packed to bf16:
 //   P  = 2^(mul f(X) + addl)                        (0 where masked)
 //   dX = dscale f'(X) P (dP + radd) = (-f') P (ndsc dP + ndr)
-// For the tanh cap, -f' = f^2 - 1; with POLY, tanh runs on the FMA pipe (the
-// caller guarantees |X in| <= 0.5 for the whole warp).
+// For the tanh cap, -f' = f^2 - 1; with POLY, tanh runs on the FMA pipe through
+// the polynomial with the argument scale folded in (the caller guarantees
+// |X in| <= 0.5 and usable coefficients for the whole warp).
 template <int METHOD, bool POLY>
 __device__ __forceinline__ void dkv_pair(float X0, float X1, float dp0, float dp1, const Xf& xf,
-                                         const ColPair& c, bool l0, bool l1, uint32_t& pk,
-                                         uint32_t& xk) {
+                                         const TanhFold& tf, const ColPair& c, bool l0, bool l1,
+                                         uint32_t& pk, uint32_t& xk) {
   F2 f, e;
   if constexpr (METHOD == CAPATTN_CAP_TANH) {
-    const F2 u = f2_mul(f2(X0, X1), f2(xf.in, xf.in));
     if constexpr (POLY) {
-      f = tanh_poly2(u);
+      f = tanh_fold_eval(f2(X0, X1), tf, f2(0.f, 0.f));   // tanh(in X) = X Q(X^2)
     } else {
       float a, b;
-      f2_split(u, a, b);
+      f2_split(f2_mul(f2(X0, X1), f2(xf.in, xf.in)), a, b);
       f = f2(tanh_approx(a), tanh_approx(b));
     }
     e = f2_fma(f, f, f2(-1.f, -1.f));
@@ -173,7 +173,7 @@ constexpr int kDkvPolyPairs = 5;  // of the 8 column pairs of a chunk: tanh on t
 template <int METHOD, bool MASKED, bool POLY, int C>
 __device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_t (&dp)[16],
                                           const ColPair* cp, const int4* ci, int jrow, const Xf& xf,
-                                          uint32_t (&pk)[8], uint32_t (&xk)[8]) {
+                                          const TanhFold& tf, uint32_t (&pk)[8], uint32_t (&xk)[8]) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const ColPair c = cp[8 * C + e];
@@ -186,9 +186,9 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_
     const float X0 = __uint_as_float(s[16 * C + 2 * e]), X1 = __uint_as_float(s[16 * C + 2 * e + 1]);
     const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
     if (POLY && e < kDkvPolyPairs)
-      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, c, l0, l1, pk[e], xk[e]);
+      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, tf, c, l0, l1, pk[e], xk[e]);
     else
-      dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, c, l0, l1, pk[e], xk[e]);
+      dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, tf, c, l0, l1, pk[e], xk[e]);
   }
 }
 
@@ -198,15 +198,15 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_
 // range) and the chunk is handed to the MMA issuer.
 template <int METHOD, bool MASKED, bool POLY>
 __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair* cp,
-                                         const int4* ci, int jrow, const Xf& xf, uint32_t bar_chunk0,
-                                         int lane) {
+                                         const int4* ci, int jrow, const Xf& xf, const TanhFold& tf,
+                                         uint32_t bar_chunk0, int lane) {
   uint32_t da[16], db[16], pk[8], xk[8];
   tmem_ld16(dp_base, da);
   tmem_wait_ld();
 #define CAPATTN_DKV_CHUNK(C, CUR, NXT)                                                     \
   {                                                                                       \
     if (C < 3) tmem_ld16(dp_base + 16 * (C + 1), NXT);                                    \
-    dkv_chunk<METHOD, MASKED, POLY, C>(s, CUR, cp, ci, jrow, xf, pk, xk);                 \
+    dkv_chunk<METHOD, MASKED, POLY, C>(s, CUR, cp, ci, jrow, xf, tf, pk, xk);             \
     __syncwarp();                                                                         \
     tmem_st8(dp_base + 16 * C, pk);                                                       \
     tmem_st8(dp_base + 16 * C + 8, xk);                                                   \
@@ -418,6 +418,8 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_cols = lane_base + 64u * wg, dp_cols = lane_base + 128u + 64u * wg;
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
+    TanhFold tf{};
+    if constexpr (METHOD == CAPATTN_CAP_TANH) tf = tanh_fold(xf.in, 1.f);
     const int my_col = 64 * wg + tid;      // query column whose constants this thread loads
     bool aborted = false;
     // Per-step column constants go through a double buffer one step ahead of
@@ -497,7 +499,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         float am = 0.f;
 #pragma unroll
         for (int e = 0; e < 64; e += 2) am = fmax3_abs(am, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-        poly = __all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU);
+        poly = __all_sync(0xFFFFFFFFu, tf.ok && am * fabsf(xf.in) <= kTanhPolyMaxU);
       }
       if (!mbar_wait_warp(bar_dp, step & 1, p.status, &abort_flag)) {
         aborted = true;
@@ -508,14 +510,14 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int4* ci = &coli[cb][64 * wg];
       if (tile_full) {
         if (poly)
-          dkv_step<METHOD, false, true>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+          dkv_step<METHOD, false, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
         else
-          dkv_step<METHOD, false, false>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+          dkv_step<METHOD, false, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
       } else {
         if (poly)
-          dkv_step<METHOD, true, true>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+          dkv_step<METHOD, true, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
         else
-          dkv_step<METHOD, true, false>(sv, dp_cols, cp, ci, jrow, xf, bar_chunk, lane);
+          dkv_step<METHOD, true, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
       }
       mbar_arrive(my_cfree);
       r1 = r2;
@@ -563,7 +565,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 template <int METHOD, bool MASKED, bool POLY, int C>
 __device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t (&dp)[16],
                                          const ColPair& rc, int4 ri, int j0, const Xf& xf,
-                                         uint32_t (&xk)[8]) {
+                                         const TanhFold& tf, uint32_t (&xk)[8]) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     bool l0 = true, l1 = true;
@@ -576,9 +578,9 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t
     const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
     uint32_t pk;
     if (POLY && e < kDkvPolyPairs)
-      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, rc, l0, l1, pk, xk[e]);
+      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e]);
     else
-      dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, rc, l0, l1, pk, xk[e]);
+      dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e]);
   }
 }
 
@@ -586,14 +588,15 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t
 // first 8 of its 16 dP columns and handed to the MMA issuer.
 template <int METHOD, bool MASKED, bool POLY>
 __device__ __forceinline__ void dq_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair& rc,
-                                        int4 ri, int j0, const Xf& xf, uint32_t bar_chunk0, int lane) {
+                                        int4 ri, int j0, const Xf& xf, const TanhFold& tf,
+                                        uint32_t bar_chunk0, int lane) {
   uint32_t da[16], db[16], xk[8];
   tmem_ld16(dp_base, da);
   tmem_wait_ld();
 #define CAPATTN_DQ_CHUNK(C, CUR, NXT)                                                      \
   {                                                                                       \
     if (C < 3) tmem_ld16(dp_base + 16 * (C + 1), NXT);                                    \
-    dq_chunk<METHOD, MASKED, POLY, C>(s, CUR, rc, ri, j0, xf, xk);                        \
+    dq_chunk<METHOD, MASKED, POLY, C>(s, CUR, rc, ri, j0, xf, tf, xk);                    \
     __syncwarp();                                                                         \
     tmem_st8(dp_base + 16 * C, xk);                                                       \
     tmem_wait_st();                                                                       \
@@ -838,6 +841,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
     const bool fin = isfinite(lse);
     const Xf xf = make_xf<METHOD>(p.cap, p.sm_scale);
+    TanhFold tf{};
+    if constexpr (METHOD == CAPATTN_CAP_TANH) tf = tanh_fold(xf.in, 1.f);
     ColPair rc;
     {
       float mul, add;
@@ -873,7 +878,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         float am = 0.f;
 #pragma unroll
         for (int e = 0; e < 64; e += 2) am = fmax3_abs(am, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-        poly = __all_sync(0xFFFFFFFFu, am * fabsf(xf.in) <= kTanhPolyMaxU);
+        poly = __all_sync(0xFFFFFFFFu, tf.ok && am * fabsf(xf.in) <= kTanhPolyMaxU);
       }
       if (!mbar_wait_warp(bar_dp, j & 1, p.status, &abort_flag)) {
         aborted = true;
@@ -883,14 +888,14 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       const int j0 = k0 + 64 * wg;
       if (full) {
         if (poly)
-          dq_step<METHOD, false, true>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
+          dq_step<METHOD, false, true>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
         else
-          dq_step<METHOD, false, false>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
+          dq_step<METHOD, false, false>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
       } else {
         if (poly)
-          dq_step<METHOD, true, true>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
+          dq_step<METHOD, true, true>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
         else
-          dq_step<METHOD, true, false>(sv, dp_cols, rc, ri, j0, xf, bar_chunk, lane);
+          dq_step<METHOD, true, false>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
       }
     }
     bool have = false;
