@@ -151,6 +151,25 @@ capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void*
                            cudaStream_t stream);
 
 /*
+ * capattn_bwd plus the gradient of the per-query temperature, which the pages'
+ * backward returns as zeros (mosaic_attention_backward): the forward
+ * (triton_kernels.py make_triton_forward_kernel) multiplies the capped score
+ * c = cap(sm_scale * q.k) by temp, so dtemp[b, i] = sum over query heads h and
+ * keys j of dT[b,h,i,j] * c[b,h,i,j], with dT = P (dP - delta + z LSE) the
+ * gradient of the tempered logit (0 for masked pairs).
+ * temp and dtemp [B,L] float32 (device) are required (CAPATTN_ERR_INVALID_ARG
+ * if either is null); dtemp is overwritten (zeroed on `stream`, then the
+ * per-head sums are added with float32 atomics, so their order, and the last
+ * bits, vary from run to run).  Everything else is as in capattn_bwd.
+ */
+capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const void* k,
+                                 const void* v, const float* temp, const int32_t* seg,
+                                 const int32_t* bounds, const void* o, const float* lse,
+                                 const void* dO, void* dq, void* dk, void* dv, float* delta,
+                                 float* dtemp, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the device status word at the start
  * of `workspace`.  Returns CAPATTN_OK, CAPATTN_ERR_DEVICE_TIMEOUT or
  * CAPATTN_ERR_DEVICE_DATA; *raw_bits (nullable) receives the raw bits

@@ -322,6 +322,44 @@ def backward_kv_head(q, k, v, temp, seg, bounds, dO, cfg: OracleConfig, b: int, 
     return dQ, dK, dV, O, LSE
 
 
+def backward_dtemp(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
+    """Gradient with respect to the per-query temperature, [B, L] (float64).
+
+    The temperature multiplies the capped score, t = temp_i * c with
+    c = cap(sm_scale * Q K^T) (triton_kernels.py forward; the pages' backward
+    returns zeros for it).  With dT = dL/dt = P (dP - delta) + z P LSE as in
+    the backward above, dL/dtemp_i = sum over query heads h and keys j of
+    dT[h, i, j] * c[h, i, j] (the temperature is shared by all heads of a
+    row; masked pairs have P = 0 and add nothing).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    O = np.asarray(O, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    B, L, Hq, D = q.shape
+    G = Hq // k.shape[2]
+    delta = np.einsum("blhd,blhd->bhl", O, dO)
+    dtemp = np.zeros((B, L))
+    for b in range(B):
+        t_row, s_row, b_row = _row_inputs(temp, seg, bounds, b, L)
+        for r0 in range(0, L, ROW_BLOCK):
+            rows = np.arange(r0, min(L, r0 + ROW_BLOCK))
+            M = mask_rows(rows, L, cfg, s_row, b_row)
+            for h in range(Hq):
+                g = h // G
+                s = cfg.sm_scale * (q[b, rows, h] @ k[b, :, g].T)
+                c = cap_forward(s, cfg)
+                lse = LSE[b, h, rows]
+                live = np.isfinite(lse)
+                lse_safe = np.where(live, lse, 0.0)
+                P = np.where(M, np.exp(np.where(M, t_row[rows][:, None] * c, 0.0) - lse_safe[:, None]), 0.0)
+                dP = dO[b, rows, h] @ v[b, :, g].T
+                dT = P * (dP - delta[b, h, rows][:, None]) + cfg.z_loss_weight * P * lse_safe[:, None]
+                dtemp[b, rows] += np.sum(dT * c, axis=1)
+    return dtemp
+
+
 def loss(q, k, v, temp, seg, bounds, dO, cfg: OracleConfig) -> float:
     """L = sum(O * dO) + (z/2) * sum of LSE^2 over rows that are not fully masked.
 

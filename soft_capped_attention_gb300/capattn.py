@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         h.capattn_fwd.argtypes = [cfgp] + [vp] * 10 + [vp, sz, vp]
         h.capattn_bwd.restype = ctypes.c_int
         h.capattn_bwd.argtypes = [cfgp] + [vp] * 13 + [vp, sz, vp]
+        h.capattn_bwd_dtemp.restype = ctypes.c_int
+        h.capattn_bwd_dtemp.argtypes = [cfgp] + [vp] * 14 + [vp, sz, vp]
         h.capattn_device_status.restype = ctypes.c_int
         h.capattn_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         h.capattn_visit_map_host.restype = ctypes.c_int
@@ -95,7 +97,8 @@ def lib() -> ctypes.CDLL:
 
 
 EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn_workspace_bytes",
-                    "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_device_status",
+                    "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_bwd_dtemp",
+                    "capattn_device_status",
                     "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host",
                     "capattn_profile_enable", "capattn_profile_select", "capattn_profile_read", "capattn_kernel_name",
                     "capattn_fwd_noalloc")
@@ -211,6 +214,28 @@ def capattn_bwd(q, k, v, o, lse, do, ap: AttnParams, temp=None, seg=None, bounds
     return dq, dk, dv, delta
 
 
+def capattn_bwd_dtemp(q, k, v, o, lse, do, ap: AttnParams, temp, seg=None, bounds=None,
+                      workspace=None, stream=None):
+    """Backward with the temperature gradient.  Returns (dq, dk, dv, delta, dtemp [B,L])."""
+    if temp is None:
+        raise ValueError("capattn_bwd_dtemp needs the temperature tensor")
+    B, L, Hq, Hkv, D = _shape(q, k)
+    cfg = make_config(ap, B, L, Hq, Hkv, D, q.dtype)
+    if workspace is None:
+        workspace = new_workspace(cfg, q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    delta = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    dtemp = torch.empty(B, L, dtype=torch.float32, device=q.device)
+    st = lib().capattn_bwd_dtemp(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(temp), _ptr(seg),
+                                 _ptr(bounds), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(delta), _ptr(dtemp), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(st, "capattn_bwd_dtemp")
+    return dq, dk, dv, delta, dtemp
+
+
 def capattn_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
     """Synchronises the stream; returns (status, raw bits) and clears the word."""
     bits = ctypes.c_uint32(0)
@@ -296,7 +321,8 @@ def capattn_profile_read(reset: bool = True) -> dict:
 
 class CapAttnFunction(torch.autograd.Function):
     """Autograd wrapper: forward saves (o, lse); backward calls capattn_bwd.
-    Gradients flow to q, k, v; temperature, segment ids and bounds are inputs only."""
+    Gradients flow to q, k, v and, when it requires grad, to the temperature
+    (capattn_bwd_dtemp); segment ids and bounds are inputs only."""
 
     @staticmethod
     def forward(ctx, q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None):
@@ -308,6 +334,10 @@ class CapAttnFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, do, dlse):
         q, k, v, o, lse, temp, seg, bounds = ctx.saved_tensors
+        if temp is not None and ctx.needs_input_grad[4]:
+            dq, dk, dv, _, dtemp = capattn_bwd_dtemp(q, k, v, o, lse, do.contiguous(), ctx.ap, temp,
+                                                     seg, bounds)
+            return dq, dk, dv, None, dtemp, None, None
         dq, dk, dv, _ = capattn_bwd(q, k, v, o, lse, do.contiguous(), ctx.ap, temp, seg, bounds)
         return dq, dk, dv, None, None, None, None
 

@@ -134,10 +134,17 @@ struct ColPair {
 // For the tanh cap, -f' = f^2 - 1; with POLY, tanh runs on the FMA pipe through
 // the polynomial with the argument scale folded in (the caller guarantees
 // |X in| <= 0.5 and usable coefficients for the whole warp).
-template <int METHOD, bool POLY>
+// Temperature gradient terms of a row (dQ kernel): dT = P (dP + radd) and the
+// capped score c = kc f + bc, accumulated as sum dT c.
+struct DtempRow {
+  F2 radd, kc, bc;
+};
+
+template <int METHOD, bool POLY, bool DT = false>
 __device__ __forceinline__ void dkv_pair(float X0, float X1, float dp0, float dp1, const Xf& xf,
                                          const TanhFold& tf, const ColPair& c, bool l0, bool l1,
-                                         uint32_t& pk, uint32_t& xk) {
+                                         uint32_t& pk, uint32_t& xk, const DtempRow* dr = nullptr,
+                                         F2* dacc = nullptr) {
   F2 f, e;
   if constexpr (METHOD == CAPATTN_CAP_TANH) {
     if constexpr (POLY) {
@@ -164,6 +171,10 @@ __device__ __forceinline__ void dkv_pair(float X0, float X1, float dp0, float dp
   f2_split(f2_mul(e, f2_mul(f2(P0, P1), h)), g0, g1);
   pk = pack_bf16x2(P0, P1);
   xk = pack_bf16x2(g0, g1);
+  if constexpr (DT) {
+    const F2 dT = f2_mul(f2(P0, P1), f2_add(f2(dp0, dp1), dr->radd));
+    *dacc = f2_fma(dT, f2_fma(dr->kc, f, dr->bc), *dacc);
+  }
 }
 
 constexpr int kDkvPolyPairs = 5;  // of the 8 column pairs of a chunk: tanh on the FMA pipe
@@ -562,10 +573,11 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 // ======================================================================= dQ
 // One 16-column chunk (key columns 16 C .. 16 C + 15 of the warpgroup's 64) of a
 // query row: dX packed to bf16.  Row constants in rc (both halves equal).
-template <int METHOD, bool MASKED, bool POLY, int C>
+template <int METHOD, bool MASKED, bool POLY, int C, bool DT>
 __device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t (&dp)[16],
                                          const ColPair& rc, int4 ri, int j0, const Xf& xf,
-                                         const TanhFold& tf, uint32_t (&xk)[8]) {
+                                         const TanhFold& tf, uint32_t (&xk)[8], const DtempRow& dr,
+                                         F2& dacc) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     bool l0 = true, l1 = true;
@@ -578,25 +590,25 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t
     const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
     uint32_t pk;
     if (POLY && e < kDkvPolyPairs)
-      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e]);
+      dkv_pair<METHOD, true, DT>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e], &dr, &dacc);
     else
-      dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e]);
+      dkv_pair<METHOD, false, DT>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e], &dr, &dacc);
   }
 }
 
 // The warpgroup's 64 key columns of one step: dX of chunk C is packed over the
 // first 8 of its 16 dP columns and handed to the MMA issuer.
-template <int METHOD, bool MASKED, bool POLY>
+template <int METHOD, bool MASKED, bool POLY, bool DT>
 __device__ __forceinline__ void dq_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair& rc,
                                         int4 ri, int j0, const Xf& xf, const TanhFold& tf,
-                                        uint32_t bar_chunk0, int lane) {
+                                        uint32_t bar_chunk0, int lane, const DtempRow& dr, F2& dacc) {
   uint32_t da[16], db[16], xk[8];
   tmem_ld16(dp_base, da);
   tmem_wait_ld();
 #define CAPATTN_DQ_CHUNK(C, CUR, NXT)                                                      \
   {                                                                                       \
     if (C < 3) tmem_ld16(dp_base + 16 * (C + 1), NXT);                                    \
-    dq_chunk<METHOD, MASKED, POLY, C>(s, CUR, rc, ri, j0, xf, tf, xk);                    \
+    dq_chunk<METHOD, MASKED, POLY, C, DT>(s, CUR, rc, ri, j0, xf, tf, xk, dr, dacc);      \
     __syncwarp();                                                                         \
     tmem_st8(dp_base + 16 * C, xk);                                                       \
     tmem_wait_st();                                                                       \
@@ -620,7 +632,7 @@ __device__ __forceinline__ void dq_step(const uint32_t (&s)[64], uint32_t dp_bas
 // own 64 key columns each, copy their S columns to registers and release them
 // (S of step j + 1 then runs during step j's elementwise work), and pack dX over
 // their dP columns chunk by chunk.
-template <int METHOD>
+template <int METHOD, bool DT>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -844,6 +856,19 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     TanhFold tf{};
     if constexpr (METHOD == CAPATTN_CAP_TANH) tf = tanh_fold(xf.in, 1.f);
     ColPair rc;
+    DtempRow dr;
+    {
+      // capped score c = kc f + bc in terms of the cap's shape f
+      float kc = p.cap.cap, bc = 0.f;
+      if constexpr (METHOD == CAPATTN_CAP_ALSC) {
+        kc = p.cap.alsc_out;
+        bc = -p.cap.alsc_out * p.cap.alsc_sb;
+      } else if constexpr (METHOD == CAPATTN_CAP_NONE) {
+        kc = p.sm_scale;
+      }
+      dr.kc = f2(kc, kc);
+      dr.bc = f2(bc, bc);
+    }
     {
       float mul, add;
       row_consts<METHOD>(p.cap, p.sm_scale, temp, &mul, &add);
@@ -852,7 +877,9 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       const float radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
       rc.a = make_float4(mul, mul, addl, addl);
       rc.b = make_float4(-dsc, -dsc, -dsc * radd, -dsc * radd);
+      dr.radd = f2(radd, radd);
     }
+    F2 dacc = f2(0.f, 0.f);
     TileIter it(map, p.wk);
     for (int j = 0; j < n; ++j) {
       int t;
@@ -888,20 +915,26 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       const int j0 = k0 + 64 * wg;
       if (full) {
         if (poly)
-          dq_step<METHOD, false, true>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
+          dq_step<METHOD, false, true, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
         else
-          dq_step<METHOD, false, false>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
+          dq_step<METHOD, false, false, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
       } else {
         if (poly)
-          dq_step<METHOD, true, true>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
+          dq_step<METHOD, true, true, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
         else
-          dq_step<METHOD, true, false>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane);
+          dq_step<METHOD, true, false, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
       }
     }
     bool have = false;
     if (n > 0 && !aborted) {
       have = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
+    }
+    if constexpr (DT) {
+      // this warpgroup's part of sum over the row's keys of dT c (all heads add in)
+      float a0, a1;
+      f2_split(dacc, a0, a1);
+      if (valid && !aborted) atomicAdd(p.dtemp + (size_t)b * p.L + i, a0 + a1);
     }
     // warpgroup wg writes dQ columns [64 wg, 64 wg + 64)
     __nv_bfloat16* dqg = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)(b * p.L + i) * p.Hq + h) * HD;
@@ -939,7 +972,7 @@ struct BwdTcLaunch {
     if (e == cudaSuccess) e = make_bhld_map(&mdo, p.dO, p.B, p.L, p.Hq, HD, BT);
     if (e != cudaSuccess) return e;
     // dQ first: it also computes delta, which the dK/dV kernel reads.
-    auto kdq = dq_tc_kernel<METHOD>;
+    auto kdq = p.dtemp ? dq_tc_kernel<METHOD, true> : dq_tc_kernel<METHOD, false>;
     e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_DQ, s);

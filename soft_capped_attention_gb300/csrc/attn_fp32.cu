@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(NT) dq_fp32_kernel(Params p) {
   float acc[D / 4];
 #pragma unroll
   for (int d = 0; d < D / 4; ++d) acc[d] = 0.f;
+  float dta = 0.f;   // this thread's part of sum_j dT c (temperature gradient)
   const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
   for (int w = 0; w < p.wk; ++w) {
     uint32_t bits = map[w];
@@ -192,7 +193,9 @@ __global__ void __launch_bounds__(NT) dq_fp32_kernel(Params p) {
         float dc;
         const float cv = cap_value_grad<METHOD>(s * p.sm_scale, p.cap, &dc);
         const float pv = live(ri, k0 + col) ? ex2_approx(cv * tl - lse2) : 0.f;
-        Ss[ln.row * SP + col] = c1 * dc * pv * (dp + rowadd);
+        const float dT = pv * (dp + rowadd);   // gradient of the tempered logit
+        Ss[ln.row * SP + col] = c1 * dc * dT;
+        if (p.dtemp) dta = fmaf(dT, cv, dta);
       }
       __syncwarp();
 #pragma unroll
@@ -204,6 +207,12 @@ __global__ void __launch_bounds__(NT) dq_fp32_kernel(Params p) {
         acc[dd] = a;
       }
     }
+  }
+  if (p.dtemp) {
+    // the four threads of a row add their columns; every query head adds in
+    dta += __shfl_xor_sync(0xFFFFFFFFu, dta, 1);
+    dta += __shfl_xor_sync(0xFFFFFFFFu, dta, 2);
+    if (valid && ln.sub == 0) atomicAdd(p.dtemp + (size_t)b * p.L + i, dta);
   }
   if (valid) {
     float* dq = static_cast<float*>(p.dq) + ((size_t)(b * p.L + i) * p.Hq + h) * D;

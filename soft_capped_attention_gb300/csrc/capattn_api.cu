@@ -131,6 +131,43 @@ static void host_spans(const capattn_config& c, const int32_t* seg, const int32_
 
 using namespace capattn;
 
+// Backward with an optional temperature gradient (zeroed here, accumulated by
+// the dQ kernels).
+static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const void* k, const void* v,
+                               const float* temp, const int32_t* seg, const int32_t* bounds,
+                               const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                               void* dv, float* delta, float* dtemp, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
+    return CAPATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, temp, seg, bounds, dtemp};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
+  st = check_ws(*cfg, workspace, workspace_bytes);
+  if (st != CAPATTN_OK) return st;
+  Params p;
+  fill_params(p, *cfg, workspace);
+  p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
+  p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
+  p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta; p.dtemp = dtemp;
+  cudaError_t e = cudaSuccess;
+  if (dtemp) {
+    e = cudaMemsetAsync(dtemp, 0, (size_t)cfg->B * cfg->L * sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  e = launch_prepass(p, true, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  // bf16: the dQ kernel computes delta itself; fp32: a separate pass
+  if (cfg->dtype != CAPATTN_BF16) {
+    e = launch_delta(p, false, stream);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  e = (cfg->dtype == CAPATTN_BF16) ? launch_bwd_bf16(p, stream) : launch_bwd_fp32(p, stream);
+  return cuda_status(e);
+}
+
 extern "C" {
 
 const char* capattn_status_string(capattn_status s) {
@@ -190,29 +227,19 @@ capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void*
                            const void* o, const float* lse, const void* dO, void* dq, void* dk,
                            void* dv, float* delta, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
-  capattn_status st = validate(cfg);
-  if (st != CAPATTN_OK) return st;
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
-    return CAPATTN_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, temp, seg, bounds};
-  for (const void* ptr : ptrs)
-    if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
-  st = check_ws(*cfg, workspace, workspace_bytes);
-  if (st != CAPATTN_OK) return st;
-  Params p;
-  fill_params(p, *cfg, workspace);
-  p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
-  p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
-  p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta;
-  cudaError_t e = launch_prepass(p, true, stream);
-  if (e != cudaSuccess) return cuda_status(e);
-  // bf16: the dQ kernel computes delta itself; fp32: a separate pass
-  if (cfg->dtype != CAPATTN_BF16) {
-    e = launch_delta(p, false, stream);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
-  e = (cfg->dtype == CAPATTN_BF16) ? launch_bwd_bf16(p, stream) : launch_bwd_fp32(p, stream);
-  return cuda_status(e);
+  return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, dq, dk, dv, delta, nullptr, workspace,
+                  workspace_bytes, stream);
+}
+
+capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const void* k,
+                                 const void* v, const float* temp, const int32_t* seg,
+                                 const int32_t* bounds, const void* o, const float* lse,
+                                 const void* dO, void* dq, void* dk, void* dv, float* delta,
+                                 float* dtemp, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+  if (!temp || !dtemp) return CAPATTN_ERR_INVALID_ARG;
+  return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, dq, dk, dv, delta, dtemp, workspace,
+                  workspace_bytes, stream);
 }
 
 capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint32_t* raw_bits) {

@@ -42,6 +42,7 @@ struct Params {
   void* dk;
   void* dv;
   float* delta;
+  float* dtemp;           // [B, L] gradient of the temperature (accumulated), or null
   // workspace pieces
   uint32_t* status;
   int4* rowinfo;          // [B, L] (lo, hi, e, 0)

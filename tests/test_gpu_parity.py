@@ -217,3 +217,75 @@ def test_wide_cap_window_uses_running_max():
     ap = ca.AttnParams(sm_scale=float(1.0 / np.sqrt(128.0)), cap_method="tanh", cap=200.0, alpha=0.0,
                        beta=0.0, causal=True, window_len=0, z_loss_weight=0.0)
     compare(run_gpu(inp, ap, torch.bfloat16), run_oracle(inp, ap), torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# Temperature gradient (capattn_bwd_dtemp) against the oracle's definition.
+# ---------------------------------------------------------------------------
+
+def _run_dtemp(inp, ap, dtype):
+    q, k, v, do = (to_dev(inp[n], dtype) for n in ("q", "k", "v", "do"))
+    temp, seg, bounds = to_dev(inp.get("temp")), to_dev(inp.get("seg")), to_dev(inp.get("bounds"))
+    B, L, Hq, D = q.shape
+    cfg = ca.make_config(ap, B, L, Hq, k.shape[2], D, dtype)
+    ws = ca.new_workspace(cfg, q.device)
+    o, lse, _, _ = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws)
+    dq, dk, dv, _, dtemp = ca.capattn_bwd_dtemp(q, k, v, o, lse, do, ap, temp, seg, bounds, workspace=ws)
+    st, bits = ca.capattn_device_status(ws)
+    assert st == 0, f"device status {st} bits {bits}"
+    return {"dQ": dq.float().cpu().numpy(), "dtemp": dtemp.cpu().numpy(), "LSE": lse.cpu().numpy()}
+
+
+def _oracle_dtemp(inp, ap):
+    from parity_utils import oracle_cfg
+    cfg = oracle_cfg(ap)
+    O, LSE, _, _ = orc.forward(inp["q"], inp["k"], inp["v"], inp["temp"], inp.get("seg"),
+                               inp.get("bounds"), cfg)
+    return orc.backward_dtemp(inp["q"], inp["k"], inp["v"], inp["temp"], inp.get("seg"),
+                              inp.get("bounds"), O, LSE, inp["do"], cfg), LSE
+
+
+DTEMP_CASES = [
+    # (B, L, Hq, Hkv, cap, mask, z)
+    (2, 300, 4, 2, "tanh", "causal", 0.0),
+    (1, 513, 4, 1, "alsc", "window", 1e-4),
+    (2, 384, 2, 2, "soft_sign", "packed", 0.0),
+    (2, 400, 4, 2, "alsc", "ranker", 0.01),
+    (1, 257, 2, 1, "none", "window_nc", 0.0),
+]
+
+
+@pytest.mark.parametrize("case", DTEMP_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_dtemp_bf16_matches_oracle(case):
+    from parity_utils import rel_fro
+    B, L, Hq, Hkv, cap, mask, z = case
+    inp = make_case(B, L, Hq, Hkv, 128, torch.bfloat16, mask, True, seed=L + 7)
+    ap = params(cap, mask, z)
+    got = _run_dtemp(inp, ap, torch.bfloat16)
+    ref, LSE = _oracle_dtemp(inp, ap)
+    assert rel_fro(got["dtemp"], ref) <= 2e-2, rel_fro(got["dtemp"], ref)
+    dead = ~np.isfinite(LSE).any(axis=1)
+    assert np.all(got["dtemp"][dead] == 0.0)
+    # dQ is the same whether or not dtemp is asked for
+    plain = run_gpu(inp, ap, torch.bfloat16)
+    assert rel_fro(got["dQ"], plain["dQ"]) < 1e-3
+
+
+def test_dtemp_fp32_matches_oracle():
+    inp = make_case(1, 130, 2, 1, 64, torch.float32, "causal", True, seed=77)
+    ap = params("tanh", "causal", 0.02)
+    got = _run_dtemp(inp, ap, torch.float32)
+    ref, _ = _oracle_dtemp(inp, ap)
+    assert np.max(np.abs(got["dtemp"] - ref)) <= 1e-4 * max(1.0, float(np.max(np.abs(ref))))
+
+
+def test_autograd_temperature_gradient():
+    inp = make_case(1, 200, 2, 2, 128, torch.bfloat16, "causal", True, seed=91)
+    ap = params("soft_sign", "causal", 0.0)
+    q, k, v = (to_dev(inp[n], torch.bfloat16).requires_grad_(True) for n in ("q", "k", "v"))
+    temp = to_dev(inp["temp"]).requires_grad_(True)
+    o, lse = ca.CapAttnFunction.apply(q, k, v, ap, temp, None, None)
+    (o.float() * to_dev(inp["do"], torch.float32)).sum().backward()
+    ref, _ = _oracle_dtemp(inp, ap)
+    from parity_utils import rel_fro
+    assert rel_fro(temp.grad.cpu().numpy(), ref) <= 2e-2

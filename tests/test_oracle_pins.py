@@ -173,6 +173,38 @@ def test_gradients_match_finite_differences(method, cap, alpha, beta, mask, z):
         assert err < 1e-6, err
 
 
+@pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
+@pytest.mark.parametrize("mask", range(len(MASKS)))
+@pytest.mark.parametrize("z", [0.0, 0.05])
+def test_dtemp_matches_finite_differences(method, cap, alpha, beta, mask, z):
+    # dL/dtemp (shared by both query heads of a row) against central differences
+    mk = MASKS[mask]
+    rng = np.random.default_rng(211 + mask)
+    B, L, Hq, Hkv, D = 2, 7, 2, 1, 3
+    q, k, v, do, t, sg, bd = _inputs(rng, B, L, Hq, Hkv, D, temp=True, seg=mk["seg"],
+                                     bounds=mk["bounds"], scale=1.5)
+    cfg = orc.OracleConfig(sm_scale=0.7, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+                           causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=z)
+    O, LSE, _, _ = orc.forward(q, k, v, t, sg, bd, cfg)
+    dtemp = orc.backward_dtemp(q, k, v, t, sg, bd, O, LSE, do, cfg)
+    h = 1e-6
+    fd = np.zeros_like(t, dtype=np.float64)
+    for b in range(B):
+        for i in range(L):
+            t0 = t[b, i]
+            t[b, i] = t0 + h
+            lp = orc.loss(q, k, v, t, sg, bd, do, cfg)
+            t[b, i] = t0 - h
+            lm = orc.loss(q, k, v, t, sg, bd, do, cfg)
+            t[b, i] = t0
+            fd[b, i] = (lp - lm) / (2 * h)
+    err = np.linalg.norm(dtemp - fd) / max(np.linalg.norm(fd), 1e-30)
+    assert err < 1e-6, err
+    # fully masked rows contribute nothing
+    dead = ~np.isfinite(LSE).any(axis=1)
+    assert np.all(dtemp[dead] == 0.0)
+
+
 # ---------------------------------------------------------------------------
 # Brute force on tiny shapes: catches indexing / blocking / head-mapping bugs.
 # ---------------------------------------------------------------------------
