@@ -169,6 +169,14 @@ def run_capattn(args, rank, world, local_rank):
     ws = ca.new_workspace(cfg, dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    use_dtemp = args.dtemp and aux["temp"] is not None
+    if args.dtemp and not use_dtemp:
+        raise SystemExit("--dtemp needs a workload with a temperature")
+
+    def bwd(*a, **kw):
+        if use_dtemp:
+            return ca.capattn_bwd_dtemp(*a, **kw)[:3]
+        return ca.capattn_bwd(*a, **kw)[:3]
 
     def step(split=False):
         o, lse, _, _ = ca.capattn_fwd(d["q"], d["k"], d["v"], ap, da["temp"], da["seg"],
@@ -177,7 +185,7 @@ def run_capattn(args, rank, world, local_rank):
         if split:
             ev_mid = torch.cuda.Event(enable_timing=True)
             ev_mid.record(stream)
-        ca.capattn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], ap, da["temp"], da["seg"],
+        bwd(d["q"], d["k"], d["v"], o, lse, d["do"], ap, da["temp"], da["seg"],
                        da["bounds"], workspace=ws)
         return ev_mid
 
@@ -295,7 +303,7 @@ def run_capattn(args, rank, world, local_rank):
                     dabuf[n].copy_(pa[n], non_blocking=True)
             o, lse, _, _ = ca.capattn_fwd(dbuf["q"], dbuf["k"], dbuf["v"], ap, dabuf["temp"],
                                           dabuf["seg"], dabuf["bounds"], workspace=ws)
-            dq, dk, dv, _ = ca.capattn_bwd(dbuf["q"], dbuf["k"], dbuf["v"], o, lse, dbuf["do"], ap,
+            dq, dk, dv = bwd(dbuf["q"], dbuf["k"], dbuf["v"], o, lse, dbuf["do"], ap,
                                            dabuf["temp"], dabuf["seg"], dabuf["bounds"],
                                            workspace=ws)
             out_h["o"].copy_(o, non_blocking=True)
@@ -340,6 +348,7 @@ def run_capattn(args, rank, world, local_rank):
                        "D": w.D, "causal": w.causal, "window_len": w.window_len,
                        "cap": [w.cap_method, w.cap, w.alpha, w.beta],
                        "z_loss_weight": w.z_loss_weight, "unmasked_pairs": N,
+                       "dtemp": use_dtemp,
                        "flops_per_step": flops_step, "l2": "flushed before every timed step",
                        "parallelism": f"replicas x{world}"},
             "fwd_tflops": round(fwd_tf, 3), "bwd_tflops": round(bwd_tf, 3),
@@ -435,6 +444,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--dtemp", action="store_true",
+                    help="also compute the temperature gradient (workloads with a temperature)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_env()
