@@ -173,9 +173,29 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
  * Synchronises `stream`, reads and clears the device status word at the start
  * of `workspace`.  Returns CAPATTN_OK, CAPATTN_ERR_DEVICE_TIMEOUT or
  * CAPATTN_ERR_DEVICE_DATA; *raw_bits (nullable) receives the raw bits
- * (1 = wait timeout, 2 = decreasing segment ids, 4 = ranker bounds out of range).
+ * (1 = wait timeout, 2 = decreasing segment ids, 4 = ranker bounds out of range,
+ * 8 = history / candidate ids not contiguous, from capattn_ranker_bounds_from_ids).
  */
 capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint32_t* raw_bits);
+
+/*
+ * Ranker bounds from history / candidate segment ids (mosaic_backward.py's
+ * test marks a row's history positions with HISTORY_SEGMENT_ID and its
+ * candidates with CANDIDATE_SEGMENT_ID; the mapping to SegmentBounds is not
+ * shown, so this is a stated reading): per batch row, history = [first, last +
+ * 1) of the positions whose id is history_id, candidates likewise for
+ * candidate_id, (0, 0) when an id is absent.
+ * seg [B,L] int32 (device, 4-byte aligned); bounds [B,4] int32 (device, output,
+ * (hl, hu, cl, cu) as the ranker mask of capattn_fwd / capattn_bwd reads them).
+ * workspace (nullable; a capattn workspace): when given, a row whose history
+ * or candidate positions have gaps sets status bit 8 (capattn_device_status
+ * then returns CAPATTN_ERR_DEVICE_DATA); its bounds are still the hull.
+ * Async on `stream`.  CAPATTN_ERR_INVALID_ARG for null arrays, B or L < 1, equal
+ * ids or misaligned pointers.
+ */
+capattn_status capattn_ranker_bounds_from_ids(const int32_t* seg, int32_t B, int32_t L,
+                                              int32_t history_id, int32_t candidate_id,
+                                              int32_t* bounds, void* workspace, cudaStream_t stream);
 
 /*
  * Visit maps (host computation).  For which = CAPATTN_VISIT_Q_TILES, out holds

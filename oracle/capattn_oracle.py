@@ -372,6 +372,36 @@ def loss(q, k, v, temp, seg, bounds, dO, cfg: OracleConfig) -> float:
 
 
 # ---------------------------------------------------------------------------
+# Ranker bounds from history / candidate segment ids.
+# ---------------------------------------------------------------------------
+
+def ranker_bounds_from_ids(seg, history_id: int, candidate_id: int):
+    """Per batch row, (hl, hu, cl, cu) and whether both id runs are contiguous.
+
+    mosaic_backward.py's test marks the history positions of a row with
+    HISTORY_SEGMENT_ID and the candidate positions with CANDIDATE_SEGMENT_ID;
+    the mapping to bounds sits in a module the pages do not show.  Reading: the
+    history range is [first, last + 1) of the positions carrying history_id,
+    the candidate range likewise for candidate_id; an absent id gives the
+    empty range (0, 0); a run with gaps is not a range (flagged, its bounds
+    are still the hull).
+    """
+    seg = np.asarray(seg)
+    B, L = seg.shape
+    bounds = np.zeros((B, 4), np.int32)
+    contiguous = np.ones(B, bool)
+    for b in range(B):
+        for slot, ident in ((0, history_id), (2, candidate_id)):
+            pos = np.nonzero(seg[b] == ident)[0]
+            if pos.size:
+                lo, hi = int(pos[0]), int(pos[-1]) + 1
+                bounds[b, slot:slot + 2] = (lo, hi)
+                if hi - lo != pos.size:
+                    contiguous[b] = False
+    return bounds, contiguous
+
+
+# ---------------------------------------------------------------------------
 # Block visit sets and pair counts, by brute force over the mask.
 # ---------------------------------------------------------------------------
 

@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         h.capattn_bwd.argtypes = [cfgp] + [vp] * 13 + [vp, sz, vp]
         h.capattn_bwd_dtemp.restype = ctypes.c_int
         h.capattn_bwd_dtemp.argtypes = [cfgp] + [vp] * 14 + [vp, sz, vp]
+        h.capattn_ranker_bounds_from_ids.restype = ctypes.c_int
+        h.capattn_ranker_bounds_from_ids.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                     ctypes.c_int32, vp, vp, vp]
         h.capattn_device_status.restype = ctypes.c_int
         h.capattn_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         h.capattn_visit_map_host.restype = ctypes.c_int
@@ -98,7 +101,7 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn_workspace_bytes",
                     "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_bwd_dtemp",
-                    "capattn_device_status",
+                    "capattn_device_status", "capattn_ranker_bounds_from_ids",
                     "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host",
                     "capattn_profile_enable", "capattn_profile_select", "capattn_profile_read", "capattn_kernel_name",
                     "capattn_fwd_noalloc")
@@ -234,6 +237,17 @@ def capattn_bwd_dtemp(q, k, v, o, lse, do, ap: AttnParams, temp, seg=None, bound
                                  workspace.numel(), _stream(stream))
     _check(st, "capattn_bwd_dtemp")
     return dq, dk, dv, delta, dtemp
+
+
+def ranker_bounds_from_ids(seg: torch.Tensor, history_id: int, candidate_id: int, workspace=None,
+                           stream=None) -> torch.Tensor:
+    """[B, L] int32 segment ids on the GPU -> [B, 4] int32 ranker bounds (hl, hu, cl, cu)."""
+    B, L = seg.shape
+    bounds = torch.empty(B, 4, dtype=torch.int32, device=seg.device)
+    _check(lib().capattn_ranker_bounds_from_ids(_ptr(seg), B, L, int(history_id), int(candidate_id),
+                                                _ptr(bounds), _ptr(workspace), _stream(stream)),
+           "capattn_ranker_bounds_from_ids")
+    return bounds
 
 
 def capattn_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:

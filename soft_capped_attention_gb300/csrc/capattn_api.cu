@@ -242,6 +242,17 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
                   workspace_bytes, stream);
 }
 
+capattn_status capattn_ranker_bounds_from_ids(const int32_t* seg, int32_t B, int32_t L,
+                                              int32_t history_id, int32_t candidate_id,
+                                              int32_t* bounds, void* workspace, cudaStream_t stream) {
+  if (!seg || !bounds || B < 1 || L < 1 || history_id == candidate_id) return CAPATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seg) & 3u) || (reinterpret_cast<uintptr_t>(bounds) & 3u) ||
+      (workspace && !aligned16(workspace)))
+    return CAPATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_ranker_bounds(seg, B, L, history_id, candidate_id, bounds,
+                                          static_cast<uint32_t*>(workspace), stream));
+}
+
 capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint32_t* raw_bits) {
   if (!workspace) return CAPATTN_ERR_WORKSPACE;
   uint32_t bits = 0;

@@ -105,5 +105,8 @@ cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_bf16(const Params& p, cudaStream_t s);
+cudaError_t launch_ranker_bounds(const int32_t* seg, int B, int L, int32_t history_id,
+                                 int32_t candidate_id, int32_t* bounds, uint32_t* status,
+                                 cudaStream_t s);
 
 }  // namespace capattn

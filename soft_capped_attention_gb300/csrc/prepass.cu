@@ -237,4 +237,63 @@ cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// One CTA per batch row: the hull [first, last + 1) of the positions carrying
+// each of the two ids (empty (0, 0) when absent), and whether each run fills its
+// hull (count == length).
+__global__ void ranker_bounds_kernel(const int32_t* seg, int L, int32_t hid, int32_t cid,
+                                     int32_t* bounds, uint32_t* status) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int lo[2], hi[2], cnt[2];
+  const int b = blockIdx.x;
+  if (threadIdx.x < 2) {
+    lo[threadIdx.x] = L;
+    hi[threadIdx.x] = -1;
+    cnt[threadIdx.x] = 0;
+  }
+  __syncthreads();
+  int l_lo[2] = {L, L}, l_hi[2] = {-1, -1}, l_cnt[2] = {0, 0};
+  const int32_t* row = seg + (size_t)b * L;
+  for (int i = threadIdx.x; i < L; i += blockDim.x) {
+    const int32_t x = row[i];
+    if (x == hid) {
+      l_lo[0] = min(l_lo[0], i);
+      l_hi[0] = max(l_hi[0], i);
+      ++l_cnt[0];
+    }
+    if (x == cid) {
+      l_lo[1] = min(l_lo[1], i);
+      l_hi[1] = max(l_hi[1], i);
+      ++l_cnt[1];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (l_cnt[k] > 0) {
+      atomicMin(&lo[k], l_lo[k]);
+      atomicMax(&hi[k], l_hi[k]);
+      atomicAdd(&cnt[k], l_cnt[k]);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool contiguous = true;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const bool any = cnt[k] > 0;
+      bounds[(size_t)b * 4 + 2 * k] = any ? lo[k] : 0;
+      bounds[(size_t)b * 4 + 2 * k + 1] = any ? hi[k] + 1 : 0;
+      if (any && hi[k] + 1 - lo[k] != cnt[k]) contiguous = false;
+    }
+    if (!contiguous && status) atomicOr(status, kStatusRankerIdsBit);
+  }
+}
+
+cudaError_t launch_ranker_bounds(const int32_t* seg, int B, int L, int32_t history_id,
+                                 int32_t candidate_id, int32_t* bounds, uint32_t* status,
+                                 cudaStream_t s) {
+  return launch_pdl(ranker_bounds_kernel, dim3(B), dim3(256), 0, s, seg, L, history_id, candidate_id,
+                    bounds, status);
+}
+
 }  // namespace capattn

@@ -289,3 +289,36 @@ def test_autograd_temperature_gradient():
     ref, _ = _oracle_dtemp(inp, ap)
     from parity_utils import rel_fro
     assert rel_fro(temp.grad.cpu().numpy(), ref) <= 2e-2
+
+
+# ---------------------------------------------------------------------------
+# Ranker bounds from history / candidate segment ids (bit-exact).
+# ---------------------------------------------------------------------------
+
+def test_ranker_bounds_from_ids_bit_exact():
+    rng = np.random.default_rng(123)
+    H, C, B, L = 11, 12, 16, 4096
+    seg = np.full((B, L), 5, np.int32)
+    for b in range(B):
+        kind = b % 4
+        hl = int(rng.integers(0, 64))
+        hu = hl + int(rng.integers(1, 2048))
+        cu = min(L, hu + int(rng.integers(16, 128)))
+        if kind != 2:                       # kind 2: no history
+            seg[b, hl:hu] = H
+        if kind != 1:                       # kind 1: no candidates
+            seg[b, hu:cu] = C
+        if kind == 3:                       # kind 3: a gap in the history run
+            seg[b, (hl + hu) // 2] = 5
+    ref, contiguous = orc.ranker_bounds_from_ids(seg, H, C)
+    cfg = ca.make_config(ca.AttnParams(sm_scale=0.1), B, L, 2, 2, 128, torch.bfloat16)
+    ws = ca.new_workspace(cfg, torch.device("cuda"))
+    got = ca.ranker_bounds_from_ids(to_dev(seg), H, C, workspace=ws).cpu().numpy()
+    assert np.array_equal(got, ref)
+    st, bits = ca.capattn_device_status(ws)
+    assert (bits & 8) != 0 and not contiguous.all()
+    # contiguous rows only: no flag
+    ok_rows = np.nonzero(contiguous)[0]
+    got2 = ca.ranker_bounds_from_ids(to_dev(seg[ok_rows]), H, C, workspace=ws).cpu().numpy()
+    assert np.array_equal(got2, ref[ok_rows])
+    assert ca.capattn_device_status(ws) == (0, 0)

@@ -418,3 +418,50 @@ def test_stored_pair_counts_match_oracle():
         aux = make_aux(w, seed=idx)
         n = orc.pair_count(w.L, orc.config_from_workload(w), aux["seg"], aux["bounds"], B=w.B)
         assert stored[str(idx)]["pairs"] == n * w.Hq
+
+
+
+# ---------------------------------------------------------------------------
+# Ranker bounds from history / candidate segment ids.
+# ---------------------------------------------------------------------------
+
+def test_ranker_bounds_from_ids_layouts():
+    H, C = 7, 9
+    # the pages' test layout: first half history, second half candidates
+    seg = np.zeros((1, 128), np.int32)
+    seg[:, :64] = H
+    seg[:, 64:] = C
+    b, ok = orc.ranker_bounds_from_ids(seg, H, C)
+    assert b.tolist() == [[0, 64, 64, 128]] and ok.all()
+    # padding before and after, candidates absent, history absent, a gap
+    rows = np.full((4, 20), 3, np.int32)
+    rows[0, 2:10] = H
+    rows[0, 10:15] = C
+    rows[1, 5:9] = H
+    rows[2, 4:6] = C
+    rows[3, 1:4] = H
+    rows[3, 6:8] = H
+    b, ok = orc.ranker_bounds_from_ids(rows, H, C)
+    assert b.tolist() == [[2, 10, 10, 15], [5, 9, 0, 0], [0, 0, 4, 6], [1, 8, 0, 0]]
+    assert ok.tolist() == [True, True, True, False]
+
+
+def test_ranker_bounds_from_ids_equal_explicit_bounds():
+    # attention with bounds derived from ids equals attention with the same
+    # bounds given explicitly (and with the dense ranker mask of those ranges)
+    rng = np.random.default_rng(5)
+    B, L, Hq, Hkv, D = 2, 24, 2, 1, 4
+    q, k, v, do, t, _, _ = _inputs(rng, B, L, Hq, Hkv, D, temp=True)
+    seg = np.full((B, L), -1, np.int32)
+    seg[0, :15] = 1
+    seg[0, 15:20] = 2
+    seg[1, 3:11] = 1
+    seg[1, 11:24] = 2
+    bd, ok = orc.ranker_bounds_from_ids(seg, 1, 2)
+    assert ok.all() and bd.tolist() == [[0, 15, 15, 20], [3, 11, 11, 24]]
+    cfg = orc.OracleConfig(sm_scale=0.5, cap_method="alsc", cap=30.0, alpha=2.0, beta=0.5,
+                           causal=False, window_len=0, z_loss_weight=0.0)
+    O1, L1, _, _ = orc.forward(q, k, v, t, None, bd, cfg)
+    O2, L2, _, _ = orc.forward(q, k, v, t, None, np.array([[0, 15, 15, 20], [3, 11, 11, 24]]), cfg)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(L1, L2)
