@@ -50,19 +50,14 @@ constexpr int NSTAGE = 2;
 constexpr int NTHREADS = 320;
 constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
+// 32 fp32 values of row r as bf16 into 16-byte chunks q0 .. q0 + 3 of a
+// swizzled [128][64] bf16 slab (the layout the TMA store reads).
+__device__ __forceinline__ void st_row32_swz(uint32_t slab, int r, int q0, const uint32_t (&v)[32]) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-}
-
-__device__ __forceinline__ void store_zero_bf16(__nv_bfloat16* dst) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) d4[e] = make_uint4(0u, 0u, 0u, 0u);
+  for (int e = 0; e < 4; ++e) st_swz_chunk(slab, r, q0 + e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
 }
 
 // Steps of the dK/dV kernel: (query head of the group) x (visited query tile).
@@ -250,6 +245,7 @@ template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+              const __grid_constant__ CUtensorMap mdk, const __grid_constant__ CUtensorMap mdv,
               const Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[26];
@@ -319,6 +315,8 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (leader) {
         tma_prefetch_desc(&mq);
         tma_prefetch_desc(&mdo);
+        tma_prefetch_desc(&mdk);
+        tma_prefetch_desc(&mdv);
         mbar_expect_tx(bar_kv, 2 * TILE);
         tma_load_4d(sK, &mk, bar_kv, 0, g, k0, b);
         tma_load_4d(sK + SLAB, &mk, bar_kv, 64, g, k0, b);
@@ -541,20 +539,31 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       have = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
     }
-    // warpgroup 0 writes dV, warpgroup 1 writes dK
-    void* outp = wg == 0 ? p.dv : p.dk;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(outp) + ((size_t)(b * p.L + jrow) * p.Hkv + g) * HD;
+    // Warpgroup 0 writes dV, warpgroup 1 dK, each through the shared memory of
+    // the V or K tile (free once every MMA has completed) in the swizzled
+    // layout, then two TMA stores of 64 columns (rows past L are clipped).
+    const uint32_t oslab = wg == 0 ? sV : sK;
     const uint32_t acc = lane_base + (wg == 0 ? 256u : 384u);
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
       if (have) {
-        uint32_t v[32];
         tmem_ld32(acc + c * 32, v);
         tmem_wait_ld();
-        if (jrow < p.L) store_row_bf16(dst + c * 32, v);
-      } else if (jrow < p.L) {
-        store_zero_bf16(dst + c * 32);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
       }
+      st_row32_swz(oslab + (uint32_t)(c >> 1) * SLAB, r, 4 * (c & 1), v);
+    }
+    fence_async_smem();
+    named_bar_sync(1 + wg, 128);  // the warpgroup's rows are in shared memory
+    if (tid == 0) {
+      const CUtensorMap* mo = wg == 0 ? &mdv : &mdk;
+      tma_store_4d(mo, oslab, 0, g, k0, b);
+      tma_store_4d(mo, oslab + SLAB, 64, g, k0, b);
+      bulk_commit();
+      bulk_wait_read0();
     }
   }
   __syncwarp();  // warps 0 and 1 reach the CTA barrier converged
@@ -578,14 +587,10 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t
                                          const ColPair& rc, int4 ri, int j0, const Xf& xf,
                                          const TanhFold& tf, uint32_t (&xk)[8], const DtempRow& dr,
                                          F2& dacc) {
+  const uint32_t live = MASKED ? live_bits16(ri, j0 + 16 * C) : 0xFFFFu;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    bool l0 = true, l1 = true;
-    if constexpr (MASKED) {
-      const int ja = j0 + 16 * C + 2 * e, jb = ja + 1;
-      l0 = (ja >= ri.x && ja < ri.y) || ja == ri.z;
-      l1 = (jb >= ri.x && jb < ri.y) || jb == ri.z;
-    }
+    const bool l0 = (live >> (2 * e)) & 1u, l1 = (live >> (2 * e + 1)) & 1u;
     const float X0 = __uint_as_float(s[16 * C + 2 * e]), X1 = __uint_as_float(s[16 * C + 2 * e + 1]);
     const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
     uint32_t pk;
@@ -636,7 +641,7 @@ template <int METHOD, bool DT>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-             const Params p) {
+             const __grid_constant__ CUtensorMap mdq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[20];
   __shared__ uint32_t tmem_slot;
@@ -700,6 +705,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       if (leader) {
         tma_prefetch_desc(&mk);
         tma_prefetch_desc(&mv);
+        tma_prefetch_desc(&mdq);
         mbar_expect_tx(bar_q, 2 * TILE);
         tma_load_4d(sQ, &mq, bar_q, 0, h, q0, b);
         tma_load_4d(sQ + SLAB, &mq, bar_q, 64, h, q0, b);
@@ -936,19 +942,28 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       f2_split(dacc, a0, a1);
       if (valid && !aborted) atomicAdd(p.dtemp + (size_t)b * p.L + i, a0 + a1);
     }
-    // warpgroup wg writes dQ columns [64 wg, 64 wg + 64)
-    __nv_bfloat16* dqg = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)(b * p.L + i) * p.Hq + h) * HD;
+    // Warpgroup wg writes dQ columns [64 wg, 64 wg + 64) through slab wg of
+    // the Q tile's shared memory (free once every MMA has completed) and one
+    // TMA store (rows past L are clipped).
+    const uint32_t oslab = sQ + (uint32_t)wg * SLAB;
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
-      const int col = 64 * wg + 32 * c;
+      uint32_t v[32];
       if (have) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + 256u + col, v);
+        tmem_ld32(lane_base + 256u + 64 * wg + 32 * c, v);
         tmem_wait_ld();
-        if (valid) store_row_bf16(dqg + col, v);
-      } else if (valid) {
-        store_zero_bf16(dqg + col);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
       }
+      st_row32_swz(oslab, r, 4 * c, v);
+    }
+    fence_async_smem();
+    named_bar_sync(1 + wg, 128);  // the warpgroup's rows are in shared memory
+    if (warp == 2 + 4 * wg && lane == 0) {
+      tma_store_4d(&mdq, oslab, 64 * wg, h, q0, b);
+      bulk_commit();
+      bulk_wait_read0();
     }
   }
   __syncwarp();  // warps 0 and 1 reach the CTA barrier converged
@@ -965,11 +980,14 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 template <int METHOD>
 struct BwdTcLaunch {
   static cudaError_t run(const Params& p, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
     cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BT);
     if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.L, p.Hkv, HD, BT);
     if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.L, p.Hkv, HD, BT);
     if (e == cudaSuccess) e = make_bhld_map(&mdo, p.dO, p.B, p.L, p.Hq, HD, BT);
+    if (e == cudaSuccess) e = make_bhld_map(&mdq, p.dq, p.B, p.L, p.Hq, HD, BT);
+    if (e == cudaSuccess) e = make_bhld_map(&mdk, p.dk, p.B, p.L, p.Hkv, HD, BT);
+    if (e == cudaSuccess) e = make_bhld_map(&mdv, p.dv, p.B, p.L, p.Hkv, HD, BT);
     if (e != cudaSuccess) return e;
     // dQ first: it also computes delta, which the dK/dV kernel reads.
     auto kdq = p.dtemp ? dq_tc_kernel<METHOD, true> : dq_tc_kernel<METHOD, false>;
@@ -977,7 +995,7 @@ struct BwdTcLaunch {
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_DQ, s);
     prof_count(CAPATTN_KERNEL_DQ, 1);
-    e = launch_pdl(kdq, dim3(p.Hq * p.B, p.nq), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, p);
+    e = launch_pdl(kdq, dim3(p.Hq * p.B, p.nq), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdq, p);
     if (e != cudaSuccess) return e;
     prof_end(CAPATTN_KERNEL_DQ, s);
     e = cudaGetLastError();
@@ -987,7 +1005,7 @@ struct BwdTcLaunch {
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_DKV, s);
     prof_count(CAPATTN_KERNEL_DKV, 1);
-    e = launch_pdl(kdkv, dim3(p.Hkv * p.B, p.nk), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, p);
+    e = launch_pdl(kdkv, dim3(p.Hkv * p.B, p.nk), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdk, mdv, p);
     if (e != cudaSuccess) return e;
     prof_end(CAPATTN_KERNEL_DKV, s);
     return cudaGetLastError();

@@ -31,6 +31,8 @@
 // complete, PV_j is complete too and O may be rescaled in place.
 // TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); packed P of a
 // tile's key columns [0, 64) at S [0, 32), of [64, 128) at S [64, 96).
+// At the end each (tile, half) group writes its normalised O as bf16 into its
+// slab of the tile's Q in shared memory and one thread stores the slab by TMA.
 #include <math.h>
 
 #include "cap_math.cuh"
@@ -167,8 +169,7 @@ __device__ __forceinline__ void row_range_full(const uint32_t (&v)[NC], float& v
 // the FMA pipe, 2^x on MUFU.
 template <bool MASKED, int NP>
 __device__ __forceinline__ float p_chunk_tanh_fold(const uint32_t (&v)[2 * NP], uint32_t (&pk)[NP],
-                                                   const TanhFold& tf, float addm, int j0, int4 ri,
-                                                   bool any) {
+                                                   const TanhFold& tf, float addm, uint32_t live) {
   const F2 add2 = f2(addm, addm);
   F2 acc = f2(0.f, 0.f);
 #pragma unroll
@@ -178,9 +179,8 @@ __device__ __forceinline__ float p_chunk_tanh_fold(const uint32_t (&v)[2 * NP], 
              x0, x1);
     float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
     if constexpr (MASKED) {
-      const int ja = j0 + 2 * e, jb = ja + 1;
-      if (!(any && ((ja >= ri.x && ja < ri.y) || ja == ri.z))) p0 = 0.f;
-      if (!(any && ((jb >= ri.x && jb < ri.y) || jb == ri.z))) p1 = 0.f;
+      if (!(live & (1u << (2 * e)))) p0 = 0.f;
+      if (!(live & (2u << (2 * e)))) p1 = 0.f;
     }
     acc = f2_add(acc, f2(p0, p1));
     pk[e] = pack_bf16x2(p0, p1);
@@ -191,20 +191,20 @@ __device__ __forceinline__ float p_chunk_tanh_fold(const uint32_t (&v)[2 * NP], 
 }
 
 // NP column pairs of P = 2^(mul * f(X) + addm), packed to bf16 into pk; returns
-// their sum.  (No TMEM access here: callers branch per row, and the warp-wide
-// tcgen05 store must run after the branch has reconverged.)
+// their sum.  With MASKED, bit k of `live` says whether column k is live.  (No
+// TMEM access here: callers branch per row, and the warp-wide tcgen05 store
+// must run after the branch has reconverged.)
 template <int METHOD, bool MASKED, int NP>
 __device__ __forceinline__ float p_chunk(const uint32_t (&v)[2 * NP], uint32_t (&pk)[NP], const Xf& xf,
-                                         float mul, float addm, int j0, int4 ri, bool any) {
+                                         float mul, float addm, uint32_t live) {
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
   for (int e = 0; e < NP; ++e) {
     float p0 = ex2_approx(fmaf(mul, cap_f<METHOD>(__uint_as_float(v[2 * e]), xf), addm));
     float p1 = ex2_approx(fmaf(mul, cap_f<METHOD>(__uint_as_float(v[2 * e + 1]), xf), addm));
     if constexpr (MASKED) {
-      const int ja = j0 + 2 * e, jb = ja + 1;
-      if (!(any && ((ja >= ri.x && ja < ri.y) || ja == ri.z))) p0 = 0.f;
-      if (!(any && ((jb >= ri.x && jb < ri.y) || jb == ri.z))) p1 = 0.f;
+      if (!(live & (1u << (2 * e)))) p0 = 0.f;
+      if (!(live & (2u << (2 * e)))) p1 = 0.f;
     }
     s0 += p0;
     s1 += p1;
@@ -239,20 +239,24 @@ template <int METHOD>
 __device__ __forceinline__ float p_dispatch(bool full_any, bool poly, const uint32_t (&v)[16],
                                            uint32_t (&pk)[8], const Xf& xf, const TanhFold& tf,
                                            float mul, float addm, int j0, int4 ri, bool any) {
-  if constexpr (METHOD == CAPATTN_CAP_TANH) {
-    if (poly) {
-      return full_any ? p_chunk_tanh_fold<false, 8>(v, pk, tf, addm, j0, ri, any)
-                      : p_chunk_tanh_fold<true, 8>(v, pk, tf, addm, j0, ri, any);
+  if (full_any) {
+    if constexpr (METHOD == CAPATTN_CAP_TANH) {
+      if (poly) return p_chunk_tanh_fold<false, 8>(v, pk, tf, addm, 0xFFFFu);
     }
+    return p_chunk<METHOD, false, 8>(v, pk, xf, mul, addm, 0xFFFFu);
   }
-  return full_any ? p_chunk<METHOD, false, 8>(v, pk, xf, mul, addm, j0, ri, any)
-                  : p_chunk<METHOD, true, 8>(v, pk, xf, mul, addm, j0, ri, any);
+  const uint32_t live = any ? live_bits16(ri, j0) : 0u;
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    if (poly) return p_chunk_tanh_fold<true, 8>(v, pk, tf, addm, live);
+  }
+  return p_chunk<METHOD, true, 8>(v, pk, xf, mul, addm, live);
 }
 
 template <int METHOD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-              const __grid_constant__ CUtensorMap mv, const Params p) {
+              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+              const Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[16];
   __shared__ uint32_t tmem_slot;
@@ -348,6 +352,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         tma_prefetch_desc(&mq);
         tma_prefetch_desc(&mk);
         tma_prefetch_desc(&mv);
+        tma_prefetch_desc(&mo);
         mbar_expect_tx(bar_q, 2 * TILE);
         tma_load_4d(sQ0, &mq, bar_q, 0, h, qt0 * BM, b);
         tma_load_4d(sQ0 + SLAB, &mq, bar_q, 64, h, qt0 * BM, b);
@@ -608,8 +613,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
     const bool live = l_row > 0.f;
     const float inv = live ? 1.f / l_row : 0.f;
-    __nv_bfloat16* og =
-        static_cast<__nv_bfloat16*>(p.o) + ((size_t)(b * p.L + i) * p.Hq + h) * HD + 64 * half;
+    // O leaves through shared memory: once every MMA has completed, this
+    // half's slab of the tile's Q is free and takes the rows' 64 bf16 values in
+    // the swizzled layout; one TMA store per (tile, half) writes the slab (rows
+    // past L are clipped by the tensor map).
+    const uint32_t oslab = (tsel ? sQ1 : sQ0) + (uint32_t)half * SLAB;
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
       uint32_t o[32];
@@ -624,11 +632,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const float bb = (have_o && live) ? __uint_as_float(o[2 * e + 1]) * inv : 0.f;
         pk[e] = pack_bf16x2(a, bb);
       }
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(og + c * 32);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-      }
+      for (int e = 0; e < 4; ++e)
+        st_swz_chunk(oslab, r, 4 * c + e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    }
+    fence_async_smem();
+    named_bar_sync(1 + (sw >> 2), 128);  // the four warps of this (tile, half)
+    if ((sw & 3) == 0 && lane == 0 && (tsel == 0 || has1)) {
+      tma_store_4d(&mo, oslab, 64 * half, h, (qt0 + tsel) * BM, b);
+      bulk_commit();
+      bulk_wait_read0();
     }
     if (valid && half == 0) {
       const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
@@ -653,17 +666,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 template <int METHOD>
 struct FwdTcLaunch {
   static cudaError_t run(const Params& p, cudaStream_t s) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BM);
     if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.L, p.Hkv, HD, BN);
     if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.L, p.Hkv, HD, BN);
+    if (e == cudaSuccess) e = make_bhld_map(&mo, p.o, p.B, p.L, p.Hq, HD, BM);
     if (e != cudaSuccess) return e;
     auto kern = fwd_tc_kernel<METHOD>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     prof_begin(CAPATTN_KERNEL_FWD, s);
     prof_count(CAPATTN_KERNEL_FWD, 1);
-    e = launch_pdl(kern, dim3(p.Hq * p.B, (p.nq + 1) / 2), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, p);
+    e = launch_pdl(kern, dim3(p.Hq * p.B, (p.nq + 1) / 2), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mo, p);
     if (e != cudaSuccess) return e;
     prof_end(CAPATTN_KERNEL_FWD, s);
     return cudaGetLastError();

@@ -161,7 +161,7 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
   if (e != cudaSuccess) return cuda_status(e);
   // bf16: the dQ kernel computes delta itself; fp32: a separate pass
   if (cfg->dtype != CAPATTN_BF16) {
-    e = launch_delta(p, false, stream);
+    e = launch_delta_fp32(p, stream);
     if (e != cudaSuccess) return cuda_status(e);
   }
   e = (cfg->dtype == CAPATTN_BF16) ? launch_bwd_bf16(p, stream) : launch_bwd_fp32(p, stream);

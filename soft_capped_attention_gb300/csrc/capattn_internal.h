@@ -100,7 +100,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // Launchers.  Each returns cudaGetLastError() after the launch.
 cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s);
-cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s);
+cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);

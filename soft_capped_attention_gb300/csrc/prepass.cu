@@ -125,8 +125,9 @@ cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ delta
-// One warp per (b, i, h) row of D elements: delta[b, h, i] = sum_d O * dO.
-template <typename T, int D>
+// fp32 inputs: one warp per (b, i, h) row of D elements, delta[b, h, i] =
+// sum_d O * dO.  (The bf16 path computes delta inside the dQ kernel.)
+template <int D>
 __global__ void delta_kernel(Params p) {
   pdl_trigger();
   pdl_wait();
@@ -135,26 +136,11 @@ __global__ void delta_kernel(Params p) {
   const int lane = threadIdx.x & 31;
   const long long nrows = (long long)p.B * p.L * p.Hq;
   if (row >= nrows) return;
-  const T* o = static_cast<const T*>(p.o) + row * D + lane * VEC;
-  const T* g = static_cast<const T*>(p.dO) + row * D + lane * VEC;
+  const float* o = static_cast<const float*>(p.o) + row * D + lane * VEC;
+  const float* g = static_cast<const float*>(p.dO) + row * D + lane * VEC;
   float acc = 0.f;
-  if constexpr (sizeof(T) == 2) {
-    static_assert(VEC == 4, "bf16 path expects D = 128");
-    const uint2 a = *reinterpret_cast<const uint2*>(o);
-    const uint2 c = *reinterpret_cast<const uint2*>(g);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const float2 x = __bfloat1622float2(a2[t]);
-      const float2 y = __bfloat1622float2(c2[t]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
-    }
-  } else {
-#pragma unroll
-    for (int t = 0; t < VEC; ++t) acc = fmaf(o[t], g[t], acc);
-  }
+  for (int t = 0; t < VEC; ++t) acc = fmaf(o[t], g[t], acc);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
   if (lane == 0) {
@@ -166,73 +152,15 @@ __global__ void delta_kernel(Params p) {
   }
 }
 
-// bf16, D = 128: 16 lanes per row with 16-byte loads; each warp takes 8 rows
-// (4 per half-warp) and issues all of its loads before reducing, to keep
-// enough bytes in flight to stream O and dO at HBM speed.
-constexpr int kDeltaRowsPerWarp = 8;
-
-__global__ void delta_bf16_kernel(Params p) {
-  pdl_trigger();
-  pdl_wait();
-  const long long nrows = (long long)p.B * p.L * p.Hq;
-  const int lane = threadIdx.x & 31;
-  const int half = lane >> 4, sub = lane & 15;
-  const long long row0 = ((long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kDeltaRowsPerWarp;
-  uint4 a[kDeltaRowsPerWarp / 2], c[kDeltaRowsPerWarp / 2];
-#pragma unroll
-  for (int t = 0; t < kDeltaRowsPerWarp / 2; ++t) {
-    const long long row = row0 + 2 * t + half;
-    if (row < nrows) {
-      a[t] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + row * 128)[sub];
-      c[t] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dO) + row * 128)[sub];
-    } else {
-      a[t] = make_uint4(0u, 0u, 0u, 0u);
-      c[t] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kDeltaRowsPerWarp / 2; ++t) {
-    const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&a[t]);
-    const __nv_bfloat162* y2 = reinterpret_cast<const __nv_bfloat162*>(&c[t]);
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(x2[e]);
-      const float2 y = __bfloat1622float2(y2[e]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
-    }
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    const long long row = row0 + 2 * t + half;
-    if (sub == 0 && row < nrows) {
-      const int h = (int)(row % p.Hq);
-      const long long bi = row / p.Hq;
-      const int i = (int)(bi % p.L);
-      const int b = (int)(bi / p.L);
-      p.delta[((size_t)b * p.Hq + h) * p.L + i] = acc;
-    }
-  }
-}
-
-cudaError_t launch_delta(const Params& p, bool bf16, cudaStream_t s) {
+cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s) {
   const long long nrows = (long long)p.B * p.L * p.Hq;
   const int warps = 8;
   const unsigned grid = (unsigned)((nrows + warps - 1) / warps);
   prof_begin(CAPATTN_KERNEL_DELTA, s);
   prof_count(CAPATTN_KERNEL_DELTA, 1);
-  if (bf16) {
-    const long long per_block = (long long)warps * kDeltaRowsPerWarp;
-    const cudaError_t e = launch_pdl(delta_bf16_kernel, dim3((unsigned)((nrows + per_block - 1) / per_block)),
-                                     dim3(warps * 32), 0, s, p);
-    if (e != cudaSuccess) return e;
-  } else if (p.D == 64) {
-    const cudaError_t e = launch_pdl(delta_kernel<float, 64>, dim3(grid), dim3(warps * 32), 0, s, p);
-    if (e != cudaSuccess) return e;
-  } else {
-    const cudaError_t e = launch_pdl(delta_kernel<float, 128>, dim3(grid), dim3(warps * 32), 0, s, p);
-    if (e != cudaSuccess) return e;
-  }
+  const cudaError_t e = p.D == 64 ? launch_pdl(delta_kernel<64>, dim3(grid), dim3(warps * 32), 0, s, p)
+                                  : launch_pdl(delta_kernel<128>, dim3(grid), dim3(warps * 32), 0, s, p);
+  if (e != cudaSuccess) return e;
   prof_end(CAPATTN_KERNEL_DELTA, s);
   return cudaGetLastError();
 }

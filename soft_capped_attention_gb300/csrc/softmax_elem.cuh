@@ -115,6 +115,18 @@ __device__ __forceinline__ float cap_f_d(float X, const Xf& xf, float* d) {
   }
 }
 
+// Which of the 16 columns j0 .. j0 + 15 are live for a row with live span
+// [ri.x, ri.y) and extra live column ri.z, as bits 0 .. 15 (computed once per
+// 16 columns, so that each element's mask test is a single bit test).
+__device__ __forceinline__ uint32_t live_bits16(int4 ri, int j0) {
+  const int lo = min(max(ri.x - j0, 0), 16);
+  const int hi = min(max(ri.y - j0, 0), 16);
+  uint32_t bits = hi > lo ? ((1u << hi) - 1u) & ~((1u << lo) - 1u) : 0u;
+  const uint32_t ez = (uint32_t)(ri.z - j0);
+  if (ez < 16u) bits |= 1u << ez;
+  return bits;
+}
+
 // max(acc, |a|, |b|) with the three-input max instruction.
 __device__ __forceinline__ float fmax3_abs(float acc, float a, float b) {
   float r;
