@@ -8,38 +8,6 @@
 
 namespace capattn {
 
-// One thread per (b, i): the run of equal segment ids around i (binary search
-// on a non-decreasing row), the clamped ranker bounds, and the row's span.
-__global__ void rowinfo_kernel(Params p) {
-  pdl_trigger();
-  pdl_wait();
-  const int b = blockIdx.y;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= p.L) return;
-  int32_t first = 0, last1 = p.L;
-  if (p.seg) {
-    const int32_t* srow = p.seg + (size_t)b * p.L;
-    const int32_t x = srow[i];
-    if (i > 0 && srow[i - 1] > x) atomicOr(p.status, kStatusBadSegmentsBit);
-    first = lower_bound_i32(srow, p.L, x);
-    last1 = upper_bound_i32(srow, p.L, x);
-  }
-  int32_t hl = 0, hu = 0, cl = 0, cu = 0;
-  if (p.bounds) {
-    const int4 bd = reinterpret_cast<const int4*>(p.bounds)[b];
-    if (i == 0 && !(bd.x >= 0 && bd.x <= bd.y && bd.y <= p.L && bd.z >= 0 && bd.z <= bd.w &&
-                    bd.w <= p.L))
-      atomicOr(p.status, kStatusBadBoundsBit);
-    hl = imin32(imax32(bd.x, 0), p.L);
-    hu = imin32(imax32(bd.y, 0), p.L);
-    cl = imin32(imax32(bd.z, 0), p.L);
-    cu = imin32(imax32(bd.w, 0), p.L);
-  }
-  const RowSpan r = row_span(i, p.L, p.causal, p.window_len, first, last1, p.bounds ? 1 : 0, hl,
-                             hu, cl, cu);
-  p.rowinfo[(size_t)b * p.L + i] = make_int4(r.lo, r.hi, r.e, 0);
-}
-
 __device__ __forceinline__ void set_bit_range(uint32_t* bm, int a, int c) {
   for (int w = a >> 5; w <= (c >> 5); ++w) {
     const int lo = (w == (a >> 5)) ? (a & 31) : 0;
@@ -49,11 +17,13 @@ __device__ __forceinline__ void set_bit_range(uint32_t* bm, int a, int c) {
   }
 }
 
-// One CTA per (query tile, b): OR of the KV tiles touched by the tile's rows,
-// and the range of KV tiles every row of the tile covers completely (the
-// tiles in which no pair needs a mask test).  A tile with rows past L has no
-// fully covered KV tile.
-__global__ void qmap_kernel(Params p) {
+// One CTA per (query tile, b).  Per row i of the tile: the run of equal segment
+// ids around i (binary search on a non-decreasing row), the clamped ranker
+// bounds and the row's live key span, written to rowinfo.  Per tile: the OR of
+// the KV tiles its rows touch, and the range of KV tiles every row covers
+// completely (the tiles in which no pair needs a mask test); a tile with rows
+// past L has no fully covered KV tile.
+__global__ void rowmap_kernel(Params p) {
   extern __shared__ uint32_t bm[];
   __shared__ int full_lo, full_hi;
   pdl_trigger();
@@ -64,19 +34,40 @@ __global__ void qmap_kernel(Params p) {
     full_lo = 0;
     full_hi = p.nk;
   }
+  int32_t hl = 0, hu = 0, cl = 0, cu = 0;
+  if (p.bounds) {
+    const int4 bd = reinterpret_cast<const int4*>(p.bounds)[b];
+    if (qt == 0 && threadIdx.x == 0 &&
+        !(bd.x >= 0 && bd.x <= bd.y && bd.y <= p.L && bd.z >= 0 && bd.z <= bd.w && bd.w <= p.L))
+      atomicOr(p.status, kStatusBadBoundsBit);
+    hl = imin32(imax32(bd.x, 0), p.L);
+    hu = imin32(imax32(bd.y, 0), p.L);
+    cl = imin32(imax32(bd.z, 0), p.L);
+    cu = imin32(imax32(bd.w, 0), p.L);
+  }
   __syncthreads();
   for (int t = threadIdx.x; t < p.block_q; t += blockDim.x) {
     const int i = qt * p.block_q + t;
     int fa = 1, fb = 0;  // empty
     if (i < p.L) {
-      const int4 r = p.rowinfo[(size_t)b * p.L + i];
-      if (r.y > r.x) {
-        set_bit_range(bm, r.x / p.block_kv, (r.y - 1) / p.block_kv);
-        fa = (r.x + p.block_kv - 1) / p.block_kv;
-        fb = r.y / p.block_kv;
+      int32_t first = 0, last1 = p.L;
+      if (p.seg) {
+        const int32_t* srow = p.seg + (size_t)b * p.L;
+        const int32_t x = srow[i];
+        if (i > 0 && srow[i - 1] > x) atomicOr(p.status, kStatusBadSegmentsBit);
+        first = lower_bound_i32(srow, p.L, x);
+        last1 = upper_bound_i32(srow, p.L, x);
       }
-      if (r.z >= 0) {
-        const int kt = r.z / p.block_kv;
+      const RowSpan r = row_span(i, p.L, p.causal, p.window_len, first, last1, p.bounds ? 1 : 0, hl,
+                                 hu, cl, cu);
+      p.rowinfo[(size_t)b * p.L + i] = make_int4(r.lo, r.hi, r.e, 0);
+      if (r.hi > r.lo) {
+        set_bit_range(bm, r.lo / p.block_kv, (r.hi - 1) / p.block_kv);
+        fa = (r.lo + p.block_kv - 1) / p.block_kv;
+        fb = r.hi / p.block_kv;
+      }
+      if (r.e >= 0) {
+        const int kt = r.e / p.block_kv;
         atomicOr(&bm[kt >> 5], 1u << (kt & 31));
       }
     }
@@ -108,12 +99,9 @@ __global__ void kmap_kernel(Params p) {
 
 cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
   prof_begin(CAPATTN_KERNEL_PREPASS, s);
-  prof_count(CAPATTN_KERNEL_PREPASS, build_kmap ? 3 : 2);
-  dim3 g1((p.L + 255) / 256, p.B);
-  cudaError_t e = launch_pdl(rowinfo_kernel, g1, dim3(256), 0, s, p);
-  if (e != cudaSuccess) return e;
-  dim3 g2(p.nq, p.B);
-  e = launch_pdl(qmap_kernel, g2, dim3(128), p.wk * sizeof(uint32_t), s, p);
+  prof_count(CAPATTN_KERNEL_PREPASS, build_kmap ? 2 : 1);
+  dim3 g1(p.nq, p.B);
+  cudaError_t e = launch_pdl(rowmap_kernel, g1, dim3(128), p.wk * sizeof(uint32_t), s, p);
   if (e != cudaSuccess) return e;
   if (build_kmap) {
     dim3 g3(p.nk, p.B);
