@@ -51,18 +51,19 @@ def _live(i, j, causal, window_len, seg, bnd):
 
 
 def brute_attention(q, k, v, do, temp, seg, bounds, p):
-    """q, do: nested lists [B][L][Hq][D]; k, v: [B][L][Hkv][D]; p: dict with
+    """q, do: nested lists [B][L][Hq][D]; k, v: [B][Lk][Hkv][D] (Lk may differ
+    from L; query i and key j positions are compared directly); p: dict with
     sm_scale, cap_method, cap, alpha, beta, causal, window_len, z_loss_weight.
 
     Returns dict of O, LSE, dQ, dK, dV as nested lists."""
     B, L, Hq, D = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
-    Hkv = len(k[0][0])
+    Lk, Hkv = len(k[0]), len(k[0][0])
     G = Hq // Hkv
     O = [[[[0.0] * D for _ in range(Hq)] for _ in range(L)] for _ in range(B)]
     LSE = [[[0.0] * L for _ in range(Hq)] for _ in range(B)]
     dQ = [[[[0.0] * D for _ in range(Hq)] for _ in range(L)] for _ in range(B)]
-    dK = [[[[0.0] * D for _ in range(Hkv)] for _ in range(L)] for _ in range(B)]
-    dV = [[[[0.0] * D for _ in range(Hkv)] for _ in range(L)] for _ in range(B)]
+    dK = [[[[0.0] * D for _ in range(Hkv)] for _ in range(Lk)] for _ in range(B)]
+    dV = [[[[0.0] * D for _ in range(Hkv)] for _ in range(Lk)] for _ in range(B)]
     z = p["z_loss_weight"]
     for b in range(B):
         sg = None if seg is None else list(seg[b])
@@ -72,7 +73,7 @@ def brute_attention(q, k, v, do, temp, seg, bounds, p):
             for i in range(L):
                 ti = 1.0 if temp is None else float(temp[b][i])
                 svals, tvals, dcap, live = [], [], [], []
-                for j in range(L):
+                for j in range(Lk):
                     x = 0.0
                     for d in range(D):
                         x += q[b][i][h][d] * k[b][j][g][d]
@@ -82,7 +83,7 @@ def brute_attention(q, k, v, do, temp, seg, bounds, p):
                     tvals.append(ti * c)
                     dcap.append(dc)
                     live.append(_live(i, j, p["causal"], p["window_len"], sg, bd))
-                lt = [tvals[j] for j in range(L) if live[j]]
+                lt = [tvals[j] for j in range(Lk) if live[j]]
                 if not lt:
                     LSE[b][h][i] = -math.inf
                     continue
@@ -90,11 +91,11 @@ def brute_attention(q, k, v, do, temp, seg, bounds, p):
                 lsum = sum(math.exp(t - mx) for t in lt)
                 lse = mx + math.log(lsum)
                 LSE[b][h][i] = lse
-                P = [math.exp(tvals[j] - lse) if live[j] else 0.0 for j in range(L)]
+                P = [math.exp(tvals[j] - lse) if live[j] else 0.0 for j in range(Lk)]
                 for d in range(D):
-                    O[b][i][h][d] = sum(P[j] * v[b][j][g][d] for j in range(L))
+                    O[b][i][h][d] = sum(P[j] * v[b][j][g][d] for j in range(Lk))
                 delta = sum(O[b][i][h][d] * do[b][i][h][d] for d in range(D))
-                for j in range(L):
+                for j in range(Lk):
                     if not live[j]:
                         continue
                     dp = sum(do[b][i][h][d] * v[b][j][g][d] for d in range(D))

@@ -36,6 +36,12 @@ design notes):
   gradient contribution.
 * Window: key j is kept when j > i - window_len (one-sided, as printed).
 * Natural-log LSE.  GQA: kv_head = q_head // (Hq // Hkv).
+* Query and key lengths may differ (mosaic_backward.py's orchestration reads
+  q as (B, Q, H, D) and k as (B, KV, H_kv, D)): query position i < Lq and key
+  position j < Lk are compared directly, as the pages' masks compare positions
+  (causal keeps j <= i, the window j > i - window_len).  Segment ids and
+  ranker bounds are per-position arrays of one sequence, so they are used only
+  when Lq == Lk.
 
 parity unpinned: the ALSC gradient reading, the 1/2 in the z-loss loss and the
 fully-masked-row convention are readings, not facts fixed by the pages; the
@@ -134,11 +140,12 @@ def cap_derivative(s, cfg: OracleConfig):
 # also sees itself), written here in query x key orientation.
 # ---------------------------------------------------------------------------
 
-def mask_rows(rows, L: int, cfg: OracleConfig, seg_row=None, bounds_row=None) -> np.ndarray:
-    """Boolean mask M[len(rows), L] for query positions ``rows`` of one batch row."""
+def mask_rows(rows, Lk: int, cfg: OracleConfig, seg_row=None, bounds_row=None) -> np.ndarray:
+    """Boolean mask M[len(rows), Lk] for query positions ``rows`` of one batch
+    row against key positions 0 .. Lk - 1."""
     i = np.asarray(rows, dtype=np.int64)[:, None]
-    j = np.arange(L, dtype=np.int64)[None, :]
-    M = np.ones((i.shape[0], L), dtype=bool)
+    j = np.arange(Lk, dtype=np.int64)[None, :]
+    M = np.ones((i.shape[0], Lk), dtype=bool)
     if seg_row is not None:
         seg_row = np.asarray(seg_row)
         M &= seg_row[i] == seg_row[j]
@@ -156,8 +163,14 @@ def mask_rows(rows, L: int, cfg: OracleConfig, seg_row=None, bounds_row=None) ->
     return M
 
 
-def mask_matrix(L: int, cfg: OracleConfig, seg_row=None, bounds_row=None) -> np.ndarray:
-    return mask_rows(np.arange(L), L, cfg, seg_row, bounds_row)
+def mask_matrix(L: int, cfg: OracleConfig, seg_row=None, bounds_row=None, Lk: int | None = None) -> np.ndarray:
+    return mask_rows(np.arange(L), L if Lk is None else Lk, cfg, seg_row, bounds_row)
+
+
+def _check_lengths(Lq: int, Lk: int, seg, bounds):
+    # segment ids and ranker bounds describe one sequence (reading in the module docstring)
+    if Lq != Lk and (seg is not None or bounds is not None):
+        raise ValueError("segment ids and ranker bounds need equal query and key lengths")
 
 
 def _row_inputs(temp, seg, bounds, b, L):
@@ -194,7 +207,7 @@ def _forward_block(q_rows, k, v, temp_rows, M, cfg: OracleConfig):
 
 
 def forward(q, k, v, temp, seg, bounds, cfg: OracleConfig):
-    """q [B,L,Hq,D], k/v [B,L,Hkv,D] (any float dtype; used as float64).
+    """q [B,L,Hq,D], k/v [B,Lk,Hkv,D] (any float dtype; used as float64).
 
     Returns O [B,L,Hq,D], LSE [B,Hq,L], m [B,Hq,L], l [B,Hq,L], all float64.
     """
@@ -202,7 +215,8 @@ def forward(q, k, v, temp, seg, bounds, cfg: OracleConfig):
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     B, L, Hq, D = q.shape
-    Hkv = k.shape[2]
+    Lk, Hkv = k.shape[1], k.shape[2]
+    _check_lengths(L, Lk, seg, bounds)
     G = Hq // Hkv
     O = np.zeros((B, L, Hq, D))
     LSE = np.empty((B, Hq, L))
@@ -212,7 +226,7 @@ def forward(q, k, v, temp, seg, bounds, cfg: OracleConfig):
         t_row, s_row, b_row = _row_inputs(temp, seg, bounds, b, L)
         for r0 in range(0, L, ROW_BLOCK):
             rows = np.arange(r0, min(L, r0 + ROW_BLOCK))
-            M = mask_rows(rows, L, cfg, s_row, b_row)
+            M = mask_rows(rows, Lk, cfg, s_row, b_row)
             for h in range(Hq):
                 g = h // G
                 o, lse, m, l, _, _ = _forward_block(q[b, rows, h], k[b, :, g], v[b, :, g],
@@ -228,10 +242,11 @@ def forward_rows(q, k, v, temp, seg, bounds, cfg: OracleConfig, b: int, h: int, 
     """O [len(rows), D] and LSE [len(rows)] for selected query rows of head (b, h)."""
     Hq, Hkv = q.shape[2], k.shape[2]
     g = h // (Hq // Hkv)
-    L = q.shape[1]
+    L, Lk = q.shape[1], k.shape[1]
+    _check_lengths(L, Lk, seg, bounds)
     t_row, s_row, b_row = _row_inputs(temp, seg, bounds, b, L)
     rows = np.asarray(rows)
-    M = mask_rows(rows, L, cfg, s_row, b_row)
+    M = mask_rows(rows, Lk, cfg, s_row, b_row)
     o, lse, m, l, _, _ = _forward_block(np.asarray(q[b, rows, h], np.float64),
                                         np.asarray(k[b, :, g], np.float64),
                                         np.asarray(v[b, :, g], np.float64), t_row[rows], M, cfg)
@@ -257,7 +272,7 @@ def _backward_block(q_rows, k, v, do_rows, temp_rows, M, lse_rows, delta_rows, c
 
 
 def backward(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
-    """Returns dQ [B,L,Hq,D], dK and dV [B,L,Hkv,D] and delta [B,Hq,L] (float64).
+    """Returns dQ [B,L,Hq,D], dK and dV [B,Lk,Hkv,D] and delta [B,Hq,L] (float64).
 
     delta_i = sum_d O_id dO_id; dP = dO V^T; dT = P (dP - delta) + z P LSE;
     dX = sm_scale * cap'(s) * temp_i * dT; dQ = dX K; dK_g = sum over the
@@ -269,7 +284,8 @@ def backward(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
     O = np.asarray(O, dtype=np.float64)
     dO = np.asarray(dO, dtype=np.float64)
     B, L, Hq, D = q.shape
-    Hkv = k.shape[2]
+    Lk, Hkv = k.shape[1], k.shape[2]
+    _check_lengths(L, Lk, seg, bounds)
     G = Hq // Hkv
     delta = np.einsum("blhd,blhd->bhl", O, dO)
     dQ = np.zeros_like(q)
@@ -279,7 +295,7 @@ def backward(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
         t_row, s_row, b_row = _row_inputs(temp, seg, bounds, b, L)
         for r0 in range(0, L, ROW_BLOCK):
             rows = np.arange(r0, min(L, r0 + ROW_BLOCK))
-            M = mask_rows(rows, L, cfg, s_row, b_row)
+            M = mask_rows(rows, Lk, cfg, s_row, b_row)
             for h in range(Hq):
                 g = h // G
                 dq, dk, dv = _backward_block(q[b, rows, h], k[b, :, g], v[b, :, g], dO[b, rows, h],
@@ -292,21 +308,22 @@ def backward(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
 
 def backward_kv_head(q, k, v, temp, seg, bounds, dO, cfg: OracleConfig, b: int, g: int):
     """Full recomputation for one (batch, KV head): returns (dQ [L,G,D] for the
-    group's query heads, dK [L,D], dV [L,D], O [L,G,D], LSE [G,L])."""
+    group's query heads, dK [Lk,D], dV [Lk,D], O [L,G,D], LSE [G,L])."""
     Hq, Hkv = q.shape[2], k.shape[2]
     G = Hq // Hkv
-    L, D = q.shape[1], q.shape[3]
+    L, D, Lk = q.shape[1], q.shape[3], k.shape[1]
+    _check_lengths(L, Lk, seg, bounds)
     t_row, s_row, b_row = _row_inputs(temp, seg, bounds, b, L)
     kk = np.asarray(k[b, :, g], np.float64)
     vv = np.asarray(v[b, :, g], np.float64)
     dQ = np.zeros((L, G, D))
     O = np.zeros((L, G, D))
     LSE = np.zeros((G, L))
-    dK = np.zeros((L, D))
-    dV = np.zeros((L, D))
+    dK = np.zeros((Lk, D))
+    dV = np.zeros((Lk, D))
     for r0 in range(0, L, ROW_BLOCK):
         rows = np.arange(r0, min(L, r0 + ROW_BLOCK))
-        M = mask_rows(rows, L, cfg, s_row, b_row)
+        M = mask_rows(rows, Lk, cfg, s_row, b_row)
         for hh in range(G):
             h = g * G + hh
             qr = np.asarray(q[b, rows, h], np.float64)
@@ -338,6 +355,8 @@ def backward_dtemp(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
     O = np.asarray(O, dtype=np.float64)
     dO = np.asarray(dO, dtype=np.float64)
     B, L, Hq, D = q.shape
+    Lk = k.shape[1]
+    _check_lengths(L, Lk, seg, bounds)
     G = Hq // k.shape[2]
     delta = np.einsum("blhd,blhd->bhl", O, dO)
     dtemp = np.zeros((B, L))
@@ -345,7 +364,7 @@ def backward_dtemp(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
         t_row, s_row, b_row = _row_inputs(temp, seg, bounds, b, L)
         for r0 in range(0, L, ROW_BLOCK):
             rows = np.arange(r0, min(L, r0 + ROW_BLOCK))
-            M = mask_rows(rows, L, cfg, s_row, b_row)
+            M = mask_rows(rows, Lk, cfg, s_row, b_row)
             for h in range(Hq):
                 g = h // G
                 s = cfg.sm_scale * (q[b, rows, h] @ k[b, :, g].T)
@@ -406,16 +425,17 @@ def ranker_bounds_from_ids(seg, history_id: int, candidate_id: int):
 # ---------------------------------------------------------------------------
 
 def visit_matrix(L: int, block_q: int, block_kv: int, cfg: OracleConfig, seg_row=None,
-                 bounds_row=None) -> np.ndarray:
+                 bounds_row=None, Lk: int | None = None) -> np.ndarray:
     """V[qt, kt] = True iff the (block_q x block_kv) tile (qt, kt) holds at least
-    one unmasked pair.  The forward and dQ kernels visit row qt of V; the dK/dV
-    kernel visits column kt."""
+    one unmasked pair (L query rows, Lk keys, Lk = L by default).  The forward
+    and dQ kernels visit row qt of V; the dK/dV kernel visits column kt."""
+    Lk = L if Lk is None else Lk
     nq = -(-L // block_q)
-    nk = -(-L // block_kv)
+    nk = -(-Lk // block_kv)
     V = np.zeros((nq, nk), dtype=bool)
     for r0 in range(0, L, ROW_BLOCK):
         rows = np.arange(r0, min(L, r0 + ROW_BLOCK))
-        M = mask_rows(rows, L, cfg, seg_row, bounds_row)
+        M = mask_rows(rows, Lk, cfg, seg_row, bounds_row)
         qt = rows // block_q
         for kt in range(nk):
             any_live = M[:, kt * block_kv:(kt + 1) * block_kv].any(axis=1)
@@ -423,13 +443,16 @@ def visit_matrix(L: int, block_q: int, block_kv: int, cfg: OracleConfig, seg_row
     return V
 
 
-def pair_count(L: int, cfg: OracleConfig, seg=None, bounds=None, B: int = 1) -> int:
-    """Number of unmasked (query, key) pairs summed over the batch (one head)."""
+def pair_count(L: int, cfg: OracleConfig, seg=None, bounds=None, B: int = 1,
+               Lk: int | None = None) -> int:
+    """Number of unmasked (query, key) pairs summed over the batch (one head;
+    L query rows, Lk keys, Lk = L by default)."""
+    Lk = L if Lk is None else Lk
     total = 0
     for b in range(B):
         s_row = None if seg is None else seg[b]
         b_row = None if bounds is None else bounds[b]
         for r0 in range(0, L, ROW_BLOCK):
             rows = np.arange(r0, min(L, r0 + ROW_BLOCK))
-            total += int(mask_rows(rows, L, cfg, s_row, b_row).sum())
+            total += int(mask_rows(rows, Lk, cfg, s_row, b_row).sum())
     return total

@@ -465,3 +465,149 @@ def test_ranker_bounds_from_ids_equal_explicit_bounds():
     O2, L2, _, _ = orc.forward(q, k, v, t, None, np.array([[0, 15, 15, 20], [3, 11, 11, 24]]), cfg)
     np.testing.assert_array_equal(O1, O2)
     np.testing.assert_array_equal(L1, L2)
+
+
+# ---------------------------------------------------------------------------
+# Unequal query and key lengths (q [B, Lq, Hq, D], k / v [B, Lk, Hkv, D];
+# positions compared directly, as the pages' masks compare them).
+# ---------------------------------------------------------------------------
+
+def _cross_inputs(rng, B, Lq, Lk, Hq, Hkv, D, temp=True, scale=1.0):
+    q = _rand((B, Lq, Hq, D), rng, scale)
+    k = _rand((B, Lk, Hkv, D), rng, scale)
+    v = _rand((B, Lk, Hkv, D), rng)
+    do = _rand((B, Lq, Hq, D), rng)
+    t = rng.uniform(0.5, 1.5, size=(B, Lq)) if temp else None
+    return q, k, v, do, t
+
+
+CROSS_SHAPES = [(23, 41), (41, 23), (5, 64)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("G", [1, 2])
+@pytest.mark.parametrize("Lq,Lk", CROSS_SHAPES)
+def test_cross_lengths_match_torch_sdpa(causal, G, Lq, Lk):
+    # PyTorch's is_causal with unequal lengths keeps key j for query i iff j <= i
+    # (its reference mask is ones(Lq, Lk).tril()), the same position comparison
+    rng = np.random.default_rng(31)
+    B, Hkv, D = 2, 2, 16
+    Hq = Hkv * G
+    q, k, v, do, _ = _cross_inputs(rng, B, Lq, Lk, Hq, Hkv, D, temp=False)
+    cfg = orc.OracleConfig(sm_scale=0.3, causal=causal)
+    O, LSE, _, _ = orc.forward(q, k, v, None, None, None, cfg)
+    dQ, dK, dV, _ = orc.backward(q, k, v, None, None, None, O, LSE, do, cfg)
+    assert O.shape == (B, Lq, Hq, D) and dK.shape == (B, Lk, Hkv, D) and LSE.shape == (B, Hq, Lq)
+
+    tq = torch.tensor(q).permute(0, 2, 1, 3).requires_grad_(True)
+    tk = torch.tensor(k).permute(0, 2, 1, 3).requires_grad_(True)
+    tv = torch.tensor(v).permute(0, 2, 1, 3).requires_grad_(True)
+    kk = tk.repeat_interleave(G, dim=1)
+    vv = tv.repeat_interleave(G, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(tq, kk, vv, is_causal=causal, scale=0.3)
+    (out * torch.tensor(do).permute(0, 2, 1, 3)).sum().backward()
+    np.testing.assert_allclose(O, out.detach().permute(0, 2, 1, 3).numpy(), atol=1e-12)
+    np.testing.assert_allclose(dQ, tq.grad.permute(0, 2, 1, 3).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dK, tk.grad.permute(0, 2, 1, 3).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dV, tv.grad.permute(0, 2, 1, 3).numpy(), atol=1e-11)
+    s = 0.3 * torch.einsum("bhid,bhjd->bhij", tq.detach(), kk.detach())
+    if causal:
+        s = s.masked_fill(torch.ones(Lq, Lk, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(LSE, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
+CROSS_MASKS = [dict(causal=False, window_len=0), dict(causal=True, window_len=0),
+               dict(causal=True, window_len=4), dict(causal=False, window_len=3)]
+
+
+@pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
+@pytest.mark.parametrize("mask", range(len(CROSS_MASKS)))
+@pytest.mark.parametrize("Lq,Lk", [(9, 14), (14, 9)])
+def test_cross_lengths_dense_matches_brute_force(method, cap, alpha, beta, mask, Lq, Lk, monkeypatch):
+    monkeypatch.setattr(orc, "ROW_BLOCK", 4)
+    mk = CROSS_MASKS[mask]
+    rng = np.random.default_rng(400 + mask)
+    B, Hq, Hkv, D = 2, 4, 2, 5
+    q, k, v, do, t = _cross_inputs(rng, B, Lq, Lk, Hq, Hkv, D)
+    cfg = orc.OracleConfig(sm_scale=0.45, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+                           causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=0.03)
+    O, LSE, _, _ = orc.forward(q, k, v, t, None, None, cfg)
+    dQ, dK, dV, _ = orc.backward(q, k, v, t, None, None, O, LSE, do, cfg)
+    p = dict(sm_scale=0.45, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+             causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=0.03)
+    ref = brute_attention(q.tolist(), k.tolist(), v.tolist(), do.tolist(), t.tolist(), None, None, p)
+    np.testing.assert_allclose(O, np.array(ref["O"]), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(np.isinf(LSE), np.isinf(np.array(ref["LSE"])))
+    fin = np.isfinite(LSE)
+    np.testing.assert_allclose(LSE[fin], np.array(ref["LSE"])[fin], rtol=1e-12, atol=1e-12)
+    for a, r in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
+        np.testing.assert_allclose(a, np.array(ref[r]), rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
+@pytest.mark.parametrize("Lq,Lk,causal,window", [(4, 7, True, 0), (7, 4, True, 3), (5, 3, False, 0)])
+def test_cross_lengths_gradients_match_finite_differences(method, cap, alpha, beta, Lq, Lk, causal,
+                                                          window):
+    rng = np.random.default_rng(77 + Lq)
+    q, k, v, do, t = _cross_inputs(rng, 1, Lq, Lk, 2, 1, 3, scale=1.5)
+    cfg = orc.OracleConfig(sm_scale=0.7, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+                           causal=causal, window_len=window, z_loss_weight=0.05)
+    O, LSE, _, _ = orc.forward(q, k, v, t, None, None, cfg)
+    grads = orc.backward(q, k, v, t, None, None, O, LSE, do, cfg)[:3]
+    h = 1e-6
+    for x, gx in zip((q, k, v), grads):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            x0 = x[idx]
+            x[idx] = x0 + h
+            lp = orc.loss(q, k, v, t, None, None, do, cfg)
+            x[idx] = x0 - h
+            lm = orc.loss(q, k, v, t, None, None, do, cfg)
+            x[idx] = x0
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(gx - fd) / max(np.linalg.norm(fd), 1e-30)
+        assert err < 1e-6, err
+
+
+def test_causal_keys_past_the_last_query_are_never_seen():
+    # with Lk > Lq, causal query i sees keys 0..i < Lq: the same as attention over
+    # the first Lq keys, and the later keys get exactly zero gradient
+    rng = np.random.default_rng(8)
+    Lq, Lk = 11, 19
+    q, k, v, do, t = _cross_inputs(rng, 2, Lq, Lk, 2, 2, 4)
+    cfg = orc.OracleConfig(sm_scale=0.5, cap_method="tanh", cap=5.0, causal=True, window_len=6)
+    O, LSE, _, _ = orc.forward(q, k, v, t, None, None, cfg)
+    dQ, dK, dV, _ = orc.backward(q, k, v, t, None, None, O, LSE, do, cfg)
+    O2, LSE2, _, _ = orc.forward(q, k[:, :Lq], v[:, :Lq], t, None, None, cfg)
+    dQ2, dK2, dV2, _ = orc.backward(q, k[:, :Lq], v[:, :Lq], t, None, None, O2, LSE2, do, cfg)
+    # (equal up to the rounding of sums over more, exactly-zero, terms)
+    np.testing.assert_allclose(O, O2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(LSE, LSE2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dQ, dQ2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dK[:, :Lq], dK2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dV[:, :Lq], dV2, rtol=0, atol=1e-13)
+    assert np.all(dK[:, Lq:] == 0.0) and np.all(dV[:, Lq:] == 0.0)
+
+
+@pytest.mark.parametrize("Lq,Lk", [(300, 700), (700, 300), (129, 129)])
+def test_cross_lengths_pair_count_closed_forms(Lq, Lk):
+    none = orc.OracleConfig(sm_scale=1.0)
+    assert orc.pair_count(Lq, none, Lk=Lk) == Lq * Lk
+    causal = orc.OracleConfig(sm_scale=1.0, causal=True)
+    assert orc.pair_count(Lq, causal, Lk=Lk) == sum(min(i + 1, Lk) for i in range(Lq))
+    W = 50
+    win = orc.OracleConfig(sm_scale=1.0, causal=True, window_len=W)
+    assert orc.pair_count(Lq, win, Lk=Lk) == sum(max(0, min(i, Lk - 1) - max(0, i - W + 1) + 1)
+                                               for i in range(Lq))
+
+
+def test_cross_lengths_reject_segments_and_ranker_bounds():
+    rng = np.random.default_rng(2)
+    q, k, v, do, t = _cross_inputs(rng, 1, 6, 9, 2, 2, 4)
+    cfg = orc.OracleConfig(sm_scale=0.5)
+    with pytest.raises(ValueError):
+        orc.forward(q, k, v, t, np.zeros((1, 6), np.int32), None, cfg)
+    with pytest.raises(ValueError):
+        orc.forward(q, k, v, t, None, np.array([[0, 2, 2, 4]]), cfg)
