@@ -31,14 +31,19 @@
  *   dQ_i = sum_j dX_ij K_j;  dK_j = sum_{h in g} sum_i dX_ij Q_i;  dV_j = sum_{h in g} sum_i P_ij dO_i
  * which is the gradient of sum(O * dO) + (z_loss_weight / 2) * sum over live rows of LSE^2.
  *
- * Layouts (all contiguous, row-major):
- *   q, o, dO, dq : [B, L, Hq, D]      k, v, dk, dv : [B, L, Hkv, D]
+ * Layouts (all contiguous, row-major), with L query rows and Lk keys:
+ *   q, o, dO, dq : [B, L, Hq, D]      k, v, dk, dv : [B, Lk, Hkv, D]
  *   lse, m, l, delta : [B, Hq, L] float32
  *   temp : [B, L] float32 (NULL means 1)
  *   seg  : [B, L] int32 segment ids, non-decreasing along each batch row
  *          (packed documents); NULL means one segment.
  *   bounds : [B, 4] int32 (hl, hu, cl, cu) per batch row with
  *            0 <= hl <= hu <= L and 0 <= cl <= cu <= L; NULL disables the ranker mask.
+ *   Query and key lengths may differ (mosaic_backward.py's orchestration reads
+ *   q as (B, Q, H, D) and k as (B, KV, H_kv, D)): query i and key j positions
+ *   are compared directly (causal keeps j <= i, the window j > i - window_len).
+ *   seg and bounds describe one sequence and require Lk == L
+ *   (CAPATTN_ERR_INVALID_ARG otherwise).
  *   Element type of q/k/v/o/dO/dq/dk/dv: bf16 (CAPATTN_BF16) or float32 (CAPATTN_FP32).
  *   Every tensor pointer must be 16-byte aligned.
  *
@@ -98,6 +103,7 @@ typedef struct capattn_config {
   int32_t q_heads_per_kv_head; /* G = Hq / Hkv */
   int32_t B, L, Hq, Hkv, D;    /* batch, sequence length, heads, head dim */
   int32_t dtype;               /* CAPATTN_BF16 or CAPATTN_FP32 */
+  int32_t Lk;                  /* key / value length; 0 means Lk = L */
 } capattn_config;
 
 /* Human-readable name of a status code (static string). */
@@ -222,8 +228,8 @@ capattn_status capattn_visit_map_device(const capattn_config* cfg, const int32_t
 
 /*
  * Live-pair bit matrix of batch row b (host computation with the same per-row
- * rule the kernels use): bit j of word bits[i * ceil(L/64) + j / 64] is set iff
- * pair (i, j) is live.  seg and bounds: host, nullable (full [B, L] / [B, 4]).
+ * rule the kernels use): bit j of word bits[i * ceil(Lk/64) + j / 64] is set iff
+ * pair (i, j) is live (i < L, j < Lk).  seg and bounds: host, nullable (full [B, L] / [B, 4]).
  */
 capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* seg,
                                       const int32_t* bounds, int32_t b, uint64_t* bits,

@@ -44,7 +44,7 @@ class CapattnConfig(ctypes.Structure):
                 ("window_len", ctypes.c_int32), ("z_loss_weight", ctypes.c_float),
                 ("q_heads_per_kv_head", ctypes.c_int32), ("B", ctypes.c_int32),
                 ("L", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
-                ("D", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("D", ctypes.c_int32), ("dtype", ctypes.c_int32), ("Lk", ctypes.c_int32)]
 
 
 _lib_handle = None
@@ -128,7 +128,8 @@ def params_from_workload(w) -> AttnParams:
 
 
 def make_config(ap: AttnParams, B: int, L: int, Hq: int, Hkv: int, D: int,
-                dtype: torch.dtype) -> CapattnConfig:
+                dtype: torch.dtype, Lk: int = 0) -> CapattnConfig:
+    """Lk: key / value length (0: equal to the query length L)."""
     if dtype not in DTYPES:
         raise ValueError(f"unsupported dtype {dtype}")
     if ap.cap_method not in CAP_METHODS:
@@ -144,7 +145,12 @@ def make_config(ap: AttnParams, B: int, L: int, Hq: int, Hkv: int, D: int,
     c.q_heads_per_kv_head = Hq // Hkv if Hkv > 0 else 0
     c.B, c.L, c.Hq, c.Hkv, c.D = B, L, Hq, Hkv, D
     c.dtype = DTYPES[dtype]
+    c.Lk = Lk
     return c
+
+
+def key_len(cfg: CapattnConfig) -> int:
+    return cfg.Lk if cfg.Lk > 0 else cfg.L
 
 
 def _ptr(t):
@@ -173,18 +179,19 @@ def new_workspace(cfg: CapattnConfig, device) -> torch.Tensor:
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-def _shape(q, k):
+def _config(q, k, ap: AttnParams) -> CapattnConfig:
+    """Config for q [B, L, Hq, D] and k [B, Lk, Hkv, D]."""
     B, L, Hq, D = q.shape
-    Hkv = k.shape[2]
-    return B, L, Hq, Hkv, D
+    Lk, Hkv = k.shape[1], k.shape[2]
+    return make_config(ap, B, L, Hq, Hkv, D, q.dtype, Lk=Lk)
 
 
 def capattn_fwd(q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None, workspace=None,
                 want_ml=False, stream=None):
-    """Forward.  q [B,L,Hq,D], k/v [B,L,Hkv,D] (bf16 or fp32, contiguous, on the GPU).
+    """Forward.  q [B,L,Hq,D], k/v [B,Lk,Hkv,D] (bf16 or fp32, contiguous, on the GPU).
     Returns (o, lse, m, l); m and l are None unless want_ml."""
-    B, L, Hq, Hkv, D = _shape(q, k)
-    cfg = make_config(ap, B, L, Hq, Hkv, D, q.dtype)
+    cfg = _config(q, k, ap)
+    B, L, Hq = cfg.B, cfg.L, cfg.Hq
     if workspace is None:
         workspace = new_workspace(cfg, q.device)
     o = torch.empty_like(q)
@@ -201,8 +208,8 @@ def capattn_fwd(q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None, works
 def capattn_bwd(q, k, v, o, lse, do, ap: AttnParams, temp=None, seg=None, bounds=None,
                 workspace=None, stream=None):
     """Backward.  Returns (dq, dk, dv, delta)."""
-    B, L, Hq, Hkv, D = _shape(q, k)
-    cfg = make_config(ap, B, L, Hq, Hkv, D, q.dtype)
+    cfg = _config(q, k, ap)
+    B, L, Hq = cfg.B, cfg.L, cfg.Hq
     if workspace is None:
         workspace = new_workspace(cfg, q.device)
     dq = torch.empty_like(q)
@@ -222,8 +229,8 @@ def capattn_bwd_dtemp(q, k, v, o, lse, do, ap: AttnParams, temp, seg=None, bound
     """Backward with the temperature gradient.  Returns (dq, dk, dv, delta, dtemp [B,L])."""
     if temp is None:
         raise ValueError("capattn_bwd_dtemp needs the temperature tensor")
-    B, L, Hq, Hkv, D = _shape(q, k)
-    cfg = make_config(ap, B, L, Hq, Hkv, D, q.dtype)
+    cfg = _config(q, k, ap)
+    B, L, Hq = cfg.B, cfg.L, cfg.Hq
     if workspace is None:
         workspace = new_workspace(cfg, q.device)
     dq = torch.empty_like(q)
@@ -286,7 +293,7 @@ def capattn_visit_map_device(cfg: CapattnConfig, seg=None, bounds=None, which=VI
     """The same bitmap built by the device pre-pass (seg / bounds: device tensors)."""
     import numpy as np
     bq, bk = capattn_tile_sizes(cfg)
-    nq, nk = -(-cfg.L // bq), -(-cfg.L // bk)
+    nq, nk = -(-cfg.L // bq), -(-key_len(cfg) // bk)
     words = cfg.B * (nq * (-(-nk // 32)) if which == VISIT_Q_TILES else nk * (-(-nq // 32)))
     dev = torch.device("cuda")
     if workspace is None:
@@ -299,14 +306,15 @@ def capattn_visit_map_device(cfg: CapattnConfig, seg=None, bounds=None, which=VI
 
 
 def capattn_mask_bits_host(cfg: CapattnConfig, b: int, seg=None, bounds=None):
-    """Live-pair bit matrix of batch row b as a numpy bool array [L, L]."""
+    """Live-pair bit matrix of batch row b as a numpy bool array [L, Lk]."""
     import numpy as np
-    wpr = -(-cfg.L // 64)
+    Lk = key_len(cfg)
+    wpr = -(-Lk // 64)
     bits = np.zeros(wpr * cfg.L, dtype=np.uint64)
     _check(lib().capattn_mask_bits_host(ctypes.byref(cfg), _np_ptr(seg), _np_ptr(bounds), b,
                                         _np_ptr(bits), bits.size), "capattn_mask_bits_host")
     by = bits.reshape(cfg.L, wpr).view(np.uint8)
-    return np.unpackbits(by, axis=1, bitorder="little")[:, :cfg.L].astype(bool)
+    return np.unpackbits(by, axis=1, bitorder="little")[:, :Lk].astype(bool)
 
 
 def capattn_profile_enable(on: bool = True):

@@ -982,12 +982,12 @@ struct BwdTcLaunch {
   static cudaError_t run(const Params& p, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
     cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.L, p.Hkv, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.L, p.Hkv, HD, BT);
+    if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.Lk, p.Hkv, HD, BT);
+    if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.Lk, p.Hkv, HD, BT);
     if (e == cudaSuccess) e = make_bhld_map(&mdo, p.dO, p.B, p.L, p.Hq, HD, BT);
     if (e == cudaSuccess) e = make_bhld_map(&mdq, p.dq, p.B, p.L, p.Hq, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mdk, p.dk, p.B, p.L, p.Hkv, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mdv, p.dv, p.B, p.L, p.Hkv, HD, BT);
+    if (e == cudaSuccess) e = make_bhld_map(&mdk, p.dk, p.B, p.Lk, p.Hkv, HD, BT);
+    if (e == cudaSuccess) e = make_bhld_map(&mdv, p.dv, p.B, p.Lk, p.Hkv, HD, BT);
     if (e != cudaSuccess) return e;
     // dQ first: it also computes delta, which the dK/dV kernel reads.
     auto kdq = p.dtemp ? dq_tc_kernel<METHOD, true> : dq_tc_kernel<METHOD, false>;

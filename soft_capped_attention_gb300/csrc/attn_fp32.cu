@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(NT) fwd_fp32_kernel(Params p) {
   const int i = q0 + ln.row;
   const size_t qstride = (size_t)p.Hq * D, kstride = (size_t)p.Hkv * D;
   const float* qg = static_cast<const float*>(p.q) + ((size_t)b * p.L * p.Hq + h) * D;
-  const float* kg = static_cast<const float*>(p.k) + ((size_t)b * p.L * p.Hkv + g) * D;
-  const float* vg = static_cast<const float*>(p.v) + ((size_t)b * p.L * p.Hkv + g) * D;
+  const float* kg = static_cast<const float*>(p.k) + ((size_t)b * p.Lk * p.Hkv + g) * D;
+  const float* vg = static_cast<const float*>(p.v) + ((size_t)b * p.Lk * p.Hkv + g) * D;
   load_tile<D>(Qs, D, qg, q0, p.L, qstride);
   const int4 ri = i < p.L ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
   const float tl = (p.temp && i < p.L ? p.temp[(size_t)b * p.L + i] : 1.f) * kLog2e;
@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(NT) fwd_fp32_kernel(Params p) {
       bits &= bits - 1;
       const int k0 = kt * BT;
       __syncthreads();
-      load_tile<D>(Ks, D + 1, kg, k0, p.L, kstride);
-      load_tile<D>(Vs, D, vg, k0, p.L, kstride);
+      load_tile<D>(Ks, D + 1, kg, k0, p.Lk, kstride);
+      load_tile<D>(Vs, D, vg, k0, p.Lk, kstride);
       __syncthreads();
       float x[16];
       float tmax = -INFINITY;
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(NT) dq_fp32_kernel(Params p) {
   const int i = q0 + ln.row;
   const size_t qstride = (size_t)p.Hq * D, kstride = (size_t)p.Hkv * D;
   const size_t qoff = ((size_t)b * p.L * p.Hq + h) * D;
-  const float* kg = static_cast<const float*>(p.k) + ((size_t)b * p.L * p.Hkv + g) * D;
-  const float* vg = static_cast<const float*>(p.v) + ((size_t)b * p.L * p.Hkv + g) * D;
+  const float* kg = static_cast<const float*>(p.k) + ((size_t)b * p.Lk * p.Hkv + g) * D;
+  const float* vg = static_cast<const float*>(p.v) + ((size_t)b * p.Lk * p.Hkv + g) * D;
   load_tile<D>(Qs, D, static_cast<const float*>(p.q) + qoff, q0, p.L, qstride);
   load_tile<D>(Gs, D, static_cast<const float*>(p.dO) + qoff, q0, p.L, qstride);
   const bool valid = i < p.L;
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(NT) dq_fp32_kernel(Params p) {
       bits &= bits - 1;
       const int k0 = kt * BT;
       __syncthreads();
-      load_tile<D>(Ks, D + 1, kg, k0, p.L, kstride);
-      load_tile<D>(Vs, D + 1, vg, k0, p.L, kstride);
+      load_tile<D>(Ks, D + 1, kg, k0, p.Lk, kstride);
+      load_tile<D>(Vs, D + 1, vg, k0, p.Lk, kstride);
       __syncthreads();
 #pragma unroll 4
       for (int c = 0; c < 16; ++c) {
@@ -238,9 +238,9 @@ __global__ void __launch_bounds__(NT) dkv_fp32_kernel(Params p) {
   const int k0 = kt * BT;
   const int j = k0 + ln.row;
   const size_t qstride = (size_t)p.Hq * D, kstride = (size_t)p.Hkv * D;
-  const size_t koff = ((size_t)b * p.L * p.Hkv + g) * D;
-  load_tile<D>(Ks, D + 1, static_cast<const float*>(p.k) + koff, k0, p.L, kstride);
-  load_tile<D>(Vs, D + 1, static_cast<const float*>(p.v) + koff, k0, p.L, kstride);
+  const size_t koff = ((size_t)b * p.Lk * p.Hkv + g) * D;
+  load_tile<D>(Ks, D + 1, static_cast<const float*>(p.k) + koff, k0, p.Lk, kstride);
+  load_tile<D>(Vs, D + 1, static_cast<const float*>(p.v) + koff, k0, p.Lk, kstride);
   float dk[D / 4], dv[D / 4];
 #pragma unroll
   for (int d = 0; d < D / 4; ++d) dk[d] = dv[d] = 0.f;
@@ -304,9 +304,9 @@ __global__ void __launch_bounds__(NT) dkv_fp32_kernel(Params p) {
       }
     }
   }
-  if (j < p.L) {
-    float* dkg = static_cast<float*>(p.dk) + ((size_t)(b * p.L + j) * p.Hkv + g) * D;
-    float* dvg = static_cast<float*>(p.dv) + ((size_t)(b * p.L + j) * p.Hkv + g) * D;
+  if (j < p.Lk) {
+    float* dkg = static_cast<float*>(p.dk) + ((size_t)(b * p.Lk + j) * p.Hkv + g) * D;
+    float* dvg = static_cast<float*>(p.dv) + ((size_t)(b * p.Lk + j) * p.Hkv + g) * D;
 #pragma unroll
     for (int dd = 0; dd < D / 4; ++dd) {
       dkg[ln.sub + 4 * dd] = dk[dd];

@@ -668,8 +668,8 @@ struct FwdTcLaunch {
   static cudaError_t run(const Params& p, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mo;
     cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BM);
-    if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.L, p.Hkv, HD, BN);
-    if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.L, p.Hkv, HD, BN);
+    if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.Lk, p.Hkv, HD, BN);
+    if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.Lk, p.Hkv, HD, BN);
     if (e == cudaSuccess) e = make_bhld_map(&mo, p.o, p.B, p.L, p.Hq, HD, BM);
     if (e != cudaSuccess) return e;
     auto kern = fwd_tc_kernel<METHOD>;

@@ -14,10 +14,12 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static int tile_q(const capattn_config& c) { return c.dtype == CAPATTN_BF16 ? 128 : 64; }
 static int tile_kv(const capattn_config& c) { return c.dtype == CAPATTN_BF16 ? 128 : 64; }
+// Key / value length (0 in the config means equal to the query length).
+static int key_len(const capattn_config& c) { return c.Lk > 0 ? c.Lk : c.L; }
 
 WorkspaceLayout workspace_layout(const capattn_config& c, int bq, int bk) {
   WorkspaceLayout w;
-  const size_t nq = (c.L + bq - 1) / bq, nk = (c.L + bk - 1) / bk;
+  const size_t nq = (c.L + bq - 1) / bq, nk = (key_len(c) + bk - 1) / bk;
   const size_t wq = (nq + 31) / 32, wk = (nk + 31) / 32;
   w.status_off = 0;
   w.rowinfo_off = 256;
@@ -30,10 +32,17 @@ WorkspaceLayout workspace_layout(const capattn_config& c, int bq, int bk) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Segment ids and ranker bounds describe positions of one sequence: they need
+// equal query and key lengths.
+static capattn_status check_masks(const capattn_config& c, const void* seg, const void* bounds) {
+  return (key_len(c) != c.L && (seg || bounds)) ? CAPATTN_ERR_INVALID_ARG : CAPATTN_OK;
+}
+
 static capattn_status validate(const capattn_config* c) {
   if (!c) return CAPATTN_ERR_INVALID_ARG;
   if (c->struct_size != sizeof(capattn_config)) return CAPATTN_ERR_INVALID_ARG;
-  if (c->B < 1 || c->L < 1 || c->Hq < 1 || c->Hkv < 1 || c->D < 1) return CAPATTN_ERR_INVALID_ARG;
+  if (c->B < 1 || c->L < 1 || c->Lk < 0 || c->Hq < 1 || c->Hkv < 1 || c->D < 1)
+    return CAPATTN_ERR_INVALID_ARG;
   if (c->q_heads_per_kv_head < 1 || c->Hkv * c->q_heads_per_kv_head != c->Hq)
     return CAPATTN_ERR_INVALID_ARG;
   if (c->dtype != CAPATTN_BF16 && c->dtype != CAPATTN_FP32) return CAPATTN_ERR_INVALID_ARG;
@@ -46,6 +55,7 @@ static capattn_status validate(const capattn_config* c) {
   // Index arithmetic in the kernels is 32-bit per (batch, head) plane and
   // 64-bit across planes; keep one plane comfortably inside int32.
   if ((int64_t)c->L * c->Hq * c->D >= (1ll << 31)) return CAPATTN_ERR_UNSUPPORTED;
+  if ((int64_t)key_len(*c) * c->Hkv * c->D >= (1ll << 31)) return CAPATTN_ERR_UNSUPPORTED;
   if (c->dtype == CAPATTN_BF16 && c->D != 128) return CAPATTN_ERR_UNSUPPORTED;
   if (c->dtype == CAPATTN_FP32 && c->D != 64 && c->D != 128) return CAPATTN_ERR_UNSUPPORTED;
   return CAPATTN_OK;
@@ -73,11 +83,12 @@ static CapConsts make_cap(const capattn_config& c) {
 
 static void fill_params(Params& p, const capattn_config& c, void* ws) {
   memset(&p, 0, sizeof(p));
-  p.B = c.B; p.L = c.L; p.Hq = c.Hq; p.Hkv = c.Hkv; p.D = c.D; p.G = c.q_heads_per_kv_head;
+  p.B = c.B; p.L = c.L; p.Lk = key_len(c); p.Hq = c.Hq; p.Hkv = c.Hkv; p.D = c.D;
+  p.G = c.q_heads_per_kv_head;
   p.block_q = tile_q(c);
   p.block_kv = tile_kv(c);
   p.nq = (c.L + p.block_q - 1) / p.block_q;
-  p.nk = (c.L + p.block_kv - 1) / p.block_kv;
+  p.nk = (p.Lk + p.block_kv - 1) / p.block_kv;
   p.wq = (p.nq + 31) / 32;
   p.wk = (p.nk + 31) / 32;
   p.sm_scale = c.sm_scale;
@@ -116,13 +127,14 @@ static void host_spans(const capattn_config& c, const int32_t* seg, const int32_
     cl = imin32(imax32(bounds[4 * b + 2], 0), c.L);
     cu = imin32(imax32(bounds[4 * b + 3], 0), c.L);
   }
+  const int32_t Lk = key_len(c);
   for (int i = 0; i < c.L; ++i) {
-    int32_t first = 0, last1 = c.L;
+    int32_t first = 0, last1 = Lk;
     if (srow) {
       first = lower_bound_i32(srow, c.L, srow[i]);
       last1 = upper_bound_i32(srow, c.L, srow[i]);
     }
-    spans[i] = row_span(i, c.L, c.causal ? 1 : 0, c.window_len, first, last1, bounds ? 1 : 0, hl,
+    spans[i] = row_span(i, Lk, c.causal ? 1 : 0, c.window_len, first, last1, bounds ? 1 : 0, hl,
                         hu, cl, cu);
   }
 }
@@ -142,6 +154,8 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
   if (st != CAPATTN_OK) return st;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
     return CAPATTN_ERR_INVALID_ARG;
+  st = check_masks(*cfg, seg, bounds);
+  if (st != CAPATTN_OK) return st;
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, temp, seg, bounds, dtemp};
   for (const void* ptr : ptrs)
     if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
@@ -207,6 +221,8 @@ capattn_status capattn_fwd(const capattn_config* cfg, const void* q, const void*
   capattn_status st = validate(cfg);
   if (st != CAPATTN_OK) return st;
   if (!q || !k || !v || !o || !lse) return CAPATTN_ERR_INVALID_ARG;
+  st = check_masks(*cfg, seg, bounds);
+  if (st != CAPATTN_OK) return st;
   const void* ptrs[] = {q, k, v, o, lse, temp, seg, bounds, m, l};
   for (const void* ptr : ptrs)
     if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
@@ -276,8 +292,10 @@ capattn_status capattn_visit_map_host(const capattn_config* cfg, const int32_t* 
   if (st != CAPATTN_OK) return st;
   if (which != CAPATTN_VISIT_Q_TILES && which != CAPATTN_VISIT_KV_TILES)
     return CAPATTN_ERR_INVALID_ARG;
+  st = check_masks(*cfg, seg, bounds);
+  if (st != CAPATTN_OK) return st;
   const int bq = tile_q(*cfg), bk = tile_kv(*cfg);
-  const int nq = (cfg->L + bq - 1) / bq, nk = (cfg->L + bk - 1) / bk;
+  const int nq = (cfg->L + bq - 1) / bq, nk = (key_len(*cfg) + bk - 1) / bk;
   const int wq = (nq + 31) / 32, wk = (nk + 31) / 32;
   const size_t need = which == CAPATTN_VISIT_Q_TILES ? (size_t)cfg->B * nq * wk
                                                      : (size_t)cfg->B * nk * wq;
@@ -313,6 +331,8 @@ capattn_status capattn_visit_map_device(const capattn_config* cfg, const int32_t
   if (st != CAPATTN_OK) return st;
   if (which != CAPATTN_VISIT_Q_TILES && which != CAPATTN_VISIT_KV_TILES)
     return CAPATTN_ERR_INVALID_ARG;
+  st = check_masks(*cfg, seg, bounds);
+  if (st != CAPATTN_OK) return st;
   st = check_ws(*cfg, workspace, workspace_bytes);
   if (st != CAPATTN_OK) return st;
   Params p;
@@ -335,13 +355,16 @@ capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* 
   capattn_status st = validate(cfg);
   if (st != CAPATTN_OK) return st;
   if (b < 0 || b >= cfg->B || !bits) return CAPATTN_ERR_INVALID_ARG;
-  const size_t wpr = (cfg->L + 63) / 64;
+  st = check_masks(*cfg, seg, bounds);
+  if (st != CAPATTN_OK) return st;
+  const int Lk = key_len(*cfg);
+  const size_t wpr = (Lk + 63) / 64;
   if (n_words < wpr * cfg->L) return CAPATTN_ERR_INVALID_ARG;
   memset(bits, 0, wpr * cfg->L * sizeof(uint64_t));
   std::vector<RowSpan> spans;
   host_spans(*cfg, seg, bounds, b, spans);
   for (int i = 0; i < cfg->L; ++i)
-    for (int j = 0; j < cfg->L; ++j)
+    for (int j = 0; j < Lk; ++j)
       if (span_live(spans[i], j)) bits[i * wpr + j / 64] |= 1ull << (j % 64);
   return CAPATTN_OK;
 }

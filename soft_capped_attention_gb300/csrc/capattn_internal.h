@@ -49,8 +49,8 @@ struct Params {
   uint32_t* qmap;         // [B, nq, wk]
   uint32_t* kmap;         // [B, nk, wq]
   int2* qfull;            // [B, nq]: KV tiles [x, y) in which every pair is live
-  // shapes
-  int32_t B, L, Hq, Hkv, D, G;
+  // shapes (L query rows, Lk keys)
+  int32_t B, L, Lk, Hq, Hkv, D, G;
   int32_t block_q, block_kv, nq, nk, wq, wk;
   // method
   float sm_scale;

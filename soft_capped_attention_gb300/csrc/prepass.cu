@@ -50,7 +50,7 @@ __global__ void rowmap_kernel(Params p) {
     const int i = qt * p.block_q + t;
     int fa = 1, fb = 0;  // empty
     if (i < p.L) {
-      int32_t first = 0, last1 = p.L;
+      int32_t first = 0, last1 = p.Lk;
       if (p.seg) {
         const int32_t* srow = p.seg + (size_t)b * p.L;
         const int32_t x = srow[i];
@@ -58,7 +58,7 @@ __global__ void rowmap_kernel(Params p) {
         first = lower_bound_i32(srow, p.L, x);
         last1 = upper_bound_i32(srow, p.L, x);
       }
-      const RowSpan r = row_span(i, p.L, p.causal, p.window_len, first, last1, p.bounds ? 1 : 0, hl,
+      const RowSpan r = row_span(i, p.Lk, p.causal, p.window_len, first, last1, p.bounds ? 1 : 0, hl,
                                  hu, cl, cu);
       p.rowinfo[(size_t)b * p.L + i] = make_int4(r.lo, r.hi, r.e, 0);
       if (r.hi > r.lo) {

@@ -30,7 +30,7 @@ def run_gpu(inp, ap, dtype, want_ml=False):
     q, k, v, do = (to_dev(inp[n], dtype) for n in ("q", "k", "v", "do"))
     temp, seg, bounds = to_dev(inp.get("temp")), to_dev(inp.get("seg")), to_dev(inp.get("bounds"))
     B, L, Hq, D = q.shape
-    cfg = ca.make_config(ap, B, L, Hq, k.shape[2], D, dtype)
+    cfg = ca.make_config(ap, B, L, Hq, k.shape[2], D, dtype, Lk=k.shape[1])
     ws = ca.new_workspace(cfg, q.device)
     o, lse, m, l = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws, want_ml=want_ml)
     dq, dk, dv, delta = ca.capattn_bwd(q, k, v, o, lse, do, ap, temp, seg, bounds, workspace=ws)

@@ -202,3 +202,66 @@ def test_visit_maps_of_the_five_workloads(lib, idx):
         got = ca.capattn_visit_map_host(c, seg, bounds, which)
         ref = oracle_visit_words(B, w.L, bq, bk, ocfg, seg, bounds, which)
         assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------------------
+# Unequal query and key lengths (config field Lk; 0 means Lk = L).
+# ---------------------------------------------------------------------------
+
+CROSS = [(300, 700), (700, 300), (129, 1000), (1, 64), (64, 1)]
+CROSS_MASKS = [dict(causal=False, window_len=0), dict(causal=True, window_len=0),
+               dict(causal=True, window_len=37), dict(causal=False, window_len=50)]
+
+
+def test_key_length_validation(lib):
+    v = lambda c: lib.capattn_validate_config(ctypes.byref(c))
+    assert v(_cfg(Lk=0)) == 0 and v(_cfg(Lk=301)) == 0 and v(_cfg(Lk=1)) == 0
+    assert v(_cfg(Lk=-1)) == 1
+    ws = lambda c: lib.capattn_workspace_bytes(ctypes.byref(c), 1)
+    assert ws(_cfg(Lk=0)) == ws(_cfg(Lk=300))
+    assert ws(_cfg(Lk=30000)) > ws(_cfg(Lk=300))
+
+
+def test_unequal_lengths_reject_segments_and_bounds(lib):
+    c = _cfg(L=300, Lk=500)
+    seg = np.zeros((2, 300), np.int32)
+    bounds = np.array([[0, 10, 10, 20], [0, 10, 10, 20]], np.int32)
+    for s, bd in ((seg, None), (None, bounds)):
+        with pytest.raises(ca.CapattnError):
+            ca.capattn_visit_map_host(c, s, bd, ca.VISIT_Q_TILES)
+        with pytest.raises(ca.CapattnError):
+            ca.capattn_mask_bits_host(c, 0, s, bd)
+    # the compute calls reject them on the host, before any launch
+    p16 = ctypes.c_void_p(16)
+    st = lib.capattn_fwd(ctypes.byref(c), p16, p16, p16, None, p16, None, p16, p16, None, None,
+                         ctypes.c_void_p(256), 1 << 24, None)
+    assert st == 1
+    st = lib.capattn_bwd(ctypes.byref(c), p16, p16, p16, None, None, p16, *([p16] * 7),
+                         ctypes.c_void_p(256), 1 << 24, None)
+    assert st == 1
+
+
+@pytest.mark.parametrize("mask", range(len(CROSS_MASKS)))
+@pytest.mark.parametrize("L,Lk", CROSS)
+def test_unequal_lengths_mask_bits_match_oracle(lib, mask, L, Lk):
+    cs = CROSS_MASKS[mask]
+    c = _cfg(B=1, L=L, Lk=Lk, causal=cs["causal"], window_len=cs["window_len"])
+    bits = ca.capattn_mask_bits_host(c, 0)
+    ref = orc.mask_matrix(L, _oracle_cfg(cs["causal"], cs["window_len"]), Lk=Lk)
+    assert bits.shape == (L, Lk) and np.array_equal(bits, ref)
+
+
+@pytest.mark.parametrize("mask", range(len(CROSS_MASKS)))
+@pytest.mark.parametrize("L,Lk", CROSS)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_unequal_lengths_visit_maps_match_oracle(lib, mask, L, Lk, dtype):
+    cs = CROSS_MASKS[mask]
+    D = 128 if dtype == torch.bfloat16 else 64
+    c = _cfg(B=2, L=L, Lk=Lk, D=D, dtype=dtype, causal=cs["causal"], window_len=cs["window_len"])
+    bq, bk = ca.capattn_tile_sizes(c)
+    ocfg = _oracle_cfg(cs["causal"], cs["window_len"])
+    V = orc.visit_matrix(L, bq, bk, ocfg, Lk=Lk)
+    for which in (ca.VISIT_Q_TILES, ca.VISIT_KV_TILES):
+        got = ca.capattn_visit_map_host(c, None, None, which)
+        ref = np.concatenate([_pack(V if which == ca.VISIT_Q_TILES else V.T)] * 2, axis=0).reshape(-1)
+        assert np.array_equal(got, ref)
