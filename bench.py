@@ -165,7 +165,7 @@ def run_capattn(args, rank, world, local_rank):
            for n in ("temp", "seg", "bounds")}
     d = {n: t.to(dev) for n, t in host.items()}
     da = {n: (None if t is None else t.to(dev)) for n, t in aux.items()}
-    cfg = ca.make_config(ap, w.B, w.L, w.Hq, w.Hkv, w.D, dtype)
+    cfg = ca.make_config(ap, w.B, w.L, w.Hq, w.Hkv, w.D, dtype, Lk=w.key_len)
     ws = ca.new_workspace(cfg, dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -344,7 +344,7 @@ def run_capattn(args, rank, world, local_rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded normal Q, K, V, dO; seeded masks)",
-            "config": {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv,
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "Lk": w.key_len, "Hq": w.Hq, "Hkv": w.Hkv,
                        "D": w.D, "causal": w.causal, "window_len": w.window_len,
                        "cap": [w.cap_method, w.cap, w.alpha, w.beta],
                        "z_loss_weight": w.z_loss_weight, "unmasked_pairs": N,
@@ -386,7 +386,8 @@ def oracle_sample(w, idx, seconds: float, start: int = 0):
             orc.backward_kv_head(inp["q"], inp["k"], inp["v"], inp["temp"], inp["seg"],
                                  inp["bounds"], inp["do"], cfg, b, g)
             n_head = orc.pair_count(w.L, cfg, None if inp["seg"] is None else inp["seg"][b:b + 1],
-                                    None if inp["bounds"] is None else inp["bounds"][b:b + 1], B=1)
+                                    None if inp["bounds"] is None else inp["bounds"][b:b + 1], B=1,
+                                    Lk=w.key_len)
             flops += 14.0 * w.D * n_head * w.G
             planes += 1
             if time.perf_counter() - t0 >= seconds:
@@ -423,7 +424,7 @@ def run_reference(args, rank, world):
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded normal Q, K, V, dO; seeded masks)", "impl": "reference",
-            "config": {"workload": w.name, "B": w.B, "L": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D},
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "Lk": w.key_len, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle",
                              "sample": f"each step: one (batch, KV head) plane of {w.name}, "

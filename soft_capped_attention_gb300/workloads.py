@@ -17,6 +17,8 @@ Five workloads are defined, all synthetic (no dataset is involved):
 5. ``ranker_alsc``: B=32, Hq=8, Hkv=2, L=4096, D=128, bf16, history/candidate
    ranker bounds with hl=0, hu ~ U[1024, 3968], cl=hu,
    cu=min(hu + U[16, 128], L); ALSC cap (30, 2, 0.5).
+6. ``cross_tanh``: cross attention with unequal lengths, B=2, Hq=Hkv=16,
+   L=2048 queries against Lk=8192 keys, D=128, bf16, no mask, tanh cap 50.
 
 Random streams (a stated choice; the pages fix no generator):
 
@@ -60,10 +62,15 @@ class Workload:
     ranker_hu_range: tuple | None = None  # None: no ranker bounds
     ranker_cand_range: tuple | None = None
     z_loss_weight: float = 0.0
+    Lk: int | None = None  # key / value length; None: equal to L
 
     @property
     def G(self) -> int:
         return self.Hq // self.Hkv
+
+    @property
+    def key_len(self) -> int:
+        return self.L if self.Lk is None else self.Lk
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -86,6 +93,8 @@ WORKLOADS = {
                 sm_scale=1.0 / np.sqrt(128.0), cap_method="alsc", cap=30.0,
                 alpha=2.0, beta=0.5, ranker_hu_range=(1024, 3968),
                 ranker_cand_range=(16, 128)),
+    6: Workload("cross_tanh", B=2, L=2048, Lk=8192, Hq=16, Hkv=16, D=128, dtype="bf16",
+                sm_scale=1.0 / np.sqrt(128.0), cap_method="tanh", cap=50.0),
 }
 
 
@@ -137,11 +146,12 @@ def make_aux(w: Workload, seed: int) -> dict:
 
 
 def make_tensors(w: Workload, seed: int) -> dict:
-    """Q [B,L,Hq,D], K and V [B,L,Hkv,D], dO [B,L,Hq,D] as float32 arrays
+    """Q [B,L,Hq,D], K and V [B,Lk,Hkv,D], dO [B,L,Hq,D] as float32 arrays
     (bf16-exact for bf16 workloads)."""
     rng = np.random.Generator(np.random.PCG64(seed))
-    shapes = {"q": (w.B, w.L, w.Hq, w.D), "k": (w.B, w.L, w.Hkv, w.D),
-              "v": (w.B, w.L, w.Hkv, w.D), "do": (w.B, w.L, w.Hq, w.D)}
+    Lk = w.key_len
+    shapes = {"q": (w.B, w.L, w.Hq, w.D), "k": (w.B, Lk, w.Hkv, w.D),
+              "v": (w.B, Lk, w.Hkv, w.D), "do": (w.B, w.L, w.Hq, w.D)}
     out = {}
     for name in ("q", "k", "v", "do"):
         x = rng.standard_normal(size=shapes[name], dtype=np.float32)

@@ -2,7 +2,7 @@
 
     python tests/golden/make_golden.py
 
-pair_counts.json: for each of the five seeded workloads, the exact number of
+pair_counts.json: for each seeded workload, the exact number of
 unmasked (query, key) pairs summed over batch and query heads (the N in the
 mask-aware FLOP counts 4*D*N forward, 10*D*N backward), counted by the oracle's
 brute-force mask from the seeded segment ids / ranker bounds.  Only the
@@ -26,7 +26,7 @@ def main():
     for idx, w in WORKLOADS.items():
         aux = make_aux(w, seed=idx)
         cfg = orc.config_from_workload(w)
-        per_head = orc.pair_count(w.L, cfg, aux["seg"], aux["bounds"], B=w.B)
+        per_head = orc.pair_count(w.L, cfg, aux["seg"], aux["bounds"], B=w.B, Lk=w.key_len)
         out[str(idx)] = {"name": w.name, "seed": idx, "pairs": per_head * w.Hq,
                          "pairs_per_head_summed_over_batch": per_head}
         print(idx, w.name, per_head * w.Hq)

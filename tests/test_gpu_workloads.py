@@ -24,14 +24,14 @@ def _planes(w):
     return [(0, 0), last] if last != (0, 0) else [(0, 0)]
 
 
-@pytest.mark.parametrize("idx", [2, 3, 4, 5])
+@pytest.mark.parametrize("idx", [2, 3, 4, 5, 6])
 def test_full_size_workload_matches_oracle_on_sampled_planes(idx):
     w = WORKLOADS[idx]
     inp = make_inputs(w, seed=idx)
     ap = ca.params_from_workload(w)
     q, k, v, do = (to_dev(inp[n], torch.bfloat16) for n in ("q", "k", "v", "do"))
     temp, seg, bounds = to_dev(inp["temp"]), to_dev(inp["seg"]), to_dev(inp["bounds"])
-    cfg = ca.make_config(ap, w.B, w.L, w.Hq, w.Hkv, w.D, torch.bfloat16)
+    cfg = ca.make_config(ap, w.B, w.L, w.Hq, w.Hkv, w.D, torch.bfloat16, Lk=w.key_len)
     ws = ca.new_workspace(cfg, q.device)
     o, lse, _, _ = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws)
     dq, dk, dv, _ = ca.capattn_bwd(q, k, v, o, lse, do, ap, temp, seg, bounds, workspace=ws)

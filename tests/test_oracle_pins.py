@@ -416,8 +416,12 @@ def test_stored_pair_counts_match_oracle():
         stored = json.load(f)
     for idx, w in WORKLOADS.items():
         aux = make_aux(w, seed=idx)
-        n = orc.pair_count(w.L, orc.config_from_workload(w), aux["seg"], aux["bounds"], B=w.B)
+        n = orc.pair_count(w.L, orc.config_from_workload(w), aux["seg"], aux["bounds"], B=w.B,
+                           Lk=w.key_len)
         assert stored[str(idx)]["pairs"] == n * w.Hq
+    # the unmasked cross-attention workload: every (query, key) pair
+    w6 = WORKLOADS[6]
+    assert stored["6"]["pairs"] == w6.B * w6.Hq * w6.L * w6.key_len
 
 
 
