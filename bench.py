@@ -62,6 +62,16 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over all ranks (the slowest rank's
+    times), or the list itself in a single process."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return [float(x) for x in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def pairs_of(idx: int) -> int:
     with open(PAIR_COUNTS) as f:
         return int(json.load(f)[str(idx)]["pairs"])
@@ -253,9 +263,7 @@ def run_capattn(args, rank, world, local_rank):
     tot = sum(e0.elapsed_time(e2) for e0, e2 in times_total)
     ms_step = tot / args.steps
     if world > 1:
-        t = torch.tensor([tot, fw, bw], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot, fw, bw = (float(x) for x in t.tolist())
+        tot, fw, bw = max_over_ranks([tot, fw, bw], dev)
         ms_step = tot / args.steps
 
     value = flops_step * args.steps * world / (tot * 1e-3) / 1e12
