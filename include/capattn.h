@@ -128,7 +128,7 @@ capattn_status capattn_tile_sizes(const capattn_config* cfg, int32_t* block_q, i
 /*
  * Forward (triton_kernels.py make_triton_forward_kernel, with its residuals).
  * Inputs q, k, v, temp (nullable), seg (nullable), bounds (nullable): device.
- * Outputs (device): o [B,L,Hq,D] in the input element type; lse [B,Hq,L]
+ * k, v: [B,Lk,Hkv,D].  Outputs (device): o [B,L,Hq,D] in the input element type; lse [B,Hq,L]
  * natural-log log-sum-exp; m and l [B,Hq,L] (nullable): row max of t and
  * sum of exp(t - m), so that lse = m + log(l).  A fully masked row gives
  * o = 0, lse = m = -inf, l = 0.
@@ -146,7 +146,7 @@ capattn_status capattn_fwd(const capattn_config* cfg, const void* q, const void*
  * done inside the dK/dV kernel).
  * Inputs (device): q, k, v, temp, seg, bounds as in capattn_fwd; o and lse as
  * written by capattn_fwd; dO [B,L,Hq,D] upstream gradient.
- * Outputs (device): dq [B,L,Hq,D], dk and dv [B,L,Hkv,D] (input element type,
+ * Outputs (device): dq [B,L,Hq,D], dk and dv [B,Lk,Hkv,D] (input element type,
  * fully overwritten); delta [B,Hq,L] float32 = rowsum(o * dO).
  * workspace: device, >= capattn_workspace_bytes(cfg, CAPATTN_PASS_BWD).
  */
