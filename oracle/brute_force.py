@@ -55,12 +55,16 @@ def brute_attention(q, k, v, do, temp, seg, bounds, p):
     from L; query i and key j positions are compared directly); p: dict with
     sm_scale, cap_method, cap, alpha, beta, causal, window_len, z_loss_weight.
 
-    Returns dict of O, LSE, dQ, dK, dV as nested lists."""
+    Returns dict of O, LSE, m, l, dQ, dK, dV as nested lists; m [B][Hq][L] is
+    the largest live tempered logit of a row and l the sum of exp(t - m) over its
+    live keys (-inf and 0 for a row with no live key)."""
     B, L, Hq, D = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
     Lk, Hkv = len(k[0]), len(k[0][0])
     G = Hq // Hkv
     O = [[[[0.0] * D for _ in range(Hq)] for _ in range(L)] for _ in range(B)]
     LSE = [[[0.0] * L for _ in range(Hq)] for _ in range(B)]
+    Mx = [[[-math.inf] * L for _ in range(Hq)] for _ in range(B)]
+    Ls = [[[0.0] * L for _ in range(Hq)] for _ in range(B)]
     dQ = [[[[0.0] * D for _ in range(Hq)] for _ in range(L)] for _ in range(B)]
     dK = [[[[0.0] * D for _ in range(Hkv)] for _ in range(Lk)] for _ in range(B)]
     dV = [[[[0.0] * D for _ in range(Hkv)] for _ in range(Lk)] for _ in range(B)]
@@ -91,6 +95,8 @@ def brute_attention(q, k, v, do, temp, seg, bounds, p):
                 lsum = sum(math.exp(t - mx) for t in lt)
                 lse = mx + math.log(lsum)
                 LSE[b][h][i] = lse
+                Mx[b][h][i] = mx
+                Ls[b][h][i] = lsum
                 P = [math.exp(tvals[j] - lse) if live[j] else 0.0 for j in range(Lk)]
                 for d in range(D):
                     O[b][i][h][d] = sum(P[j] * v[b][j][g][d] for j in range(Lk))
@@ -105,4 +111,4 @@ def brute_attention(q, k, v, do, temp, seg, bounds, p):
                         dQ[b][i][h][d] += dx * k[b][j][g][d]
                         dK[b][j][g][d] += dx * q[b][i][h][d]
                         dV[b][j][g][d] += P[j] * do[b][i][h][d]
-    return {"O": O, "LSE": LSE, "dQ": dQ, "dK": dK, "dV": dV}
+    return {"O": O, "LSE": LSE, "m": Mx, "l": Ls, "dQ": dQ, "dK": dK, "dV": dV}

@@ -174,6 +174,33 @@ def test_gradients_match_finite_differences(method, cap, alpha, beta, mask, z):
 
 
 @pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
+def test_gradients_match_finite_differences_nonpositive_temperature(method, cap, alpha, beta):
+    rng = np.random.default_rng(17)
+    B, L, Hq, Hkv, D = 1, 7, 2, 1, 3
+    q, k, v, do, _, _, _ = _inputs(rng, B, L, Hq, Hkv, D, scale=1.5)
+    t = np.array([[-1.1, 0.0, 0.6, -0.3, 0.0, 1.2, -0.7]])
+    cfg = orc.OracleConfig(sm_scale=0.7, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+                           causal=True, window_len=4, z_loss_weight=0.05)
+    O, LSE, _, _ = orc.forward(q, k, v, t, None, None, cfg)
+    grads = orc.backward(q, k, v, t, None, None, O, LSE, do, cfg)[:3]
+    h = 1e-6
+    for x, gx in zip((q, k, v), grads):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            x0 = x[idx]
+            x[idx] = x0 + h
+            lp = orc.loss(q, k, v, t, None, None, do, cfg)
+            x[idx] = x0 - h
+            lm = orc.loss(q, k, v, t, None, None, do, cfg)
+            x[idx] = x0
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(gx - fd) / max(np.linalg.norm(fd), 1e-30)
+        assert err < 1e-6, err
+
+
+@pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
 @pytest.mark.parametrize("mask", range(len(MASKS)))
 @pytest.mark.parametrize("z", [0.0, 0.05])
 def test_dtemp_matches_finite_differences(method, cap, alpha, beta, mask, z):
@@ -219,19 +246,107 @@ def test_dense_matches_brute_force(method, cap, alpha, beta, mask, monkeypatch):
     q, k, v, do, t, sg, bd = _inputs(rng, B, L, Hq, Hkv, D, seg=mk["seg"], bounds=mk["bounds"])
     cfg = orc.OracleConfig(sm_scale=0.45, cap_method=method, cap=cap, alpha=alpha, beta=beta,
                            causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=0.03)
-    O, LSE, _, _ = orc.forward(q, k, v, t, sg, bd, cfg)
+    O, LSE, Mx, Lx = orc.forward(q, k, v, t, sg, bd, cfg)
     dQ, dK, dV, _ = orc.backward(q, k, v, t, sg, bd, O, LSE, do, cfg)
     p = dict(sm_scale=0.45, cap_method=method, cap=cap, alpha=alpha, beta=beta,
              causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=0.03)
     ref = brute_attention(q.tolist(), k.tolist(), v.tolist(), do.tolist(),
                           None if t is None else t.tolist(), None if sg is None else sg.tolist(),
                           None if bd is None else bd.tolist(), p)
+    _compare_with_brute(O, LSE, Mx, Lx, dQ, dK, dV, ref)
+
+
+def _compare_with_brute(O, LSE, Mx, Lx, dQ, dK, dV, ref):
     np.testing.assert_allclose(O, np.array(ref["O"]), rtol=1e-12, atol=1e-12)
     assert np.array_equal(np.isinf(LSE), np.isinf(np.array(ref["LSE"])))
     fin = np.isfinite(LSE)
     np.testing.assert_allclose(LSE[fin], np.array(ref["LSE"])[fin], rtol=1e-12, atol=1e-12)
+    # the softmax residuals: m is the largest LIVE tempered logit, l = sum exp(t - m)
+    # over live keys; a row with no live key has m = -inf, l = 0
+    rm, rl = np.array(ref["m"]), np.array(ref["l"])
+    assert np.array_equal(np.isneginf(Mx), np.isneginf(rm)) and np.array_equal(fin, np.isfinite(rm))
+    np.testing.assert_allclose(Mx[fin], rm[fin], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(Lx, rl, rtol=1e-12, atol=1e-12)
+    assert np.all(Lx[~fin] == 0.0)
     for a, r in ((dQ, "dQ"), (dK, "dK"), (dV, "dV")):
         np.testing.assert_allclose(a, np.array(ref[r]), rtol=1e-10, atol=1e-11)
+
+
+# Temperatures that are negative on some rows and exactly zero on others (the
+# forward then takes the row's minimum capped score as its largest logit, or
+# a uniform softmax over the live keys).
+@pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
+@pytest.mark.parametrize("mask", [0, 1, 3])
+def test_dense_matches_brute_force_nonpositive_temperature(method, cap, alpha, beta, mask,
+                                                           monkeypatch):
+    monkeypatch.setattr(orc, "ROW_BLOCK", 4)
+    mk = MASKS[mask]
+    rng = np.random.default_rng(300 + mask)
+    B, L, Hq, Hkv, D = 2, 11, 4, 2, 5
+    q, k, v, do, _, sg, bd = _inputs(rng, B, L, Hq, Hkv, D, seg=mk["seg"], bounds=mk["bounds"])
+    t = rng.choice([-1.3, -0.4, 0.0, 0.8], size=(B, L))
+    cfg = orc.OracleConfig(sm_scale=0.45, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+                           causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=0.03)
+    O, LSE, Mx, Lx = orc.forward(q, k, v, t, sg, bd, cfg)
+    dQ, dK, dV, _ = orc.backward(q, k, v, t, sg, bd, O, LSE, do, cfg)
+    p = dict(sm_scale=0.45, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+             causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=0.03)
+    ref = brute_attention(q.tolist(), k.tolist(), v.tolist(), do.tolist(), t.tolist(),
+                          None if sg is None else sg.tolist(), None if bd is None else bd.tolist(), p)
+    _compare_with_brute(O, LSE, Mx, Lx, dQ, dK, dV, ref)
+
+
+def test_residuals_of_a_hand_worked_row():
+    """One query against three keys with scores worked out by hand.
+
+    D = 1, q = 1, k = (2, 5, -1), sm_scale = 1, no cap, temperature 0.5, and a
+    ranker mask that hides key 1 (history [0, 1), candidates [2, 3), query 2 is
+    a candidate: it sees history key 0 and itself, key 2).  Tempered logits:
+    t = (1, 2.5, -0.5); key 1 has the largest logit but is masked, so
+    m = 1 (not 2.5), l = 1 + e^-1.5, LSE = 1 + ln(1 + e^-1.5), and
+    O = (v0 + e^-1.5 v2) / (1 + e^-1.5).
+    """
+    q = np.zeros((1, 3, 1, 1))
+    q[0, 2, 0, 0] = 1.0
+    k = np.array([2.0, 5.0, -1.0]).reshape(1, 3, 1, 1)
+    v = np.array([3.0, -7.0, 11.0]).reshape(1, 3, 1, 1)
+    temp = np.full((1, 3), 0.5)
+    bounds = np.array([[0, 1, 2, 3]], np.int32)
+    cfg = orc.OracleConfig(sm_scale=1.0)
+    O, LSE, Mx, Lx = orc.forward(q, k, v, temp, None, bounds, cfg)
+    e = math.exp(-1.5)
+    assert Mx[0, 0, 2] == 1.0
+    assert abs(Lx[0, 0, 2] - (1.0 + e)) < 1e-15
+    assert abs(LSE[0, 0, 2] - (1.0 + math.log1p(e))) < 1e-15
+    assert abs(O[0, 2, 0, 0] - (3.0 + 11.0 * e) / (1.0 + e)) < 1e-14
+    # query 1 is outside history and candidates: fully masked
+    assert Mx[0, 0, 1] == -math.inf and Lx[0, 0, 1] == 0.0 and LSE[0, 0, 1] == -math.inf
+    # query 0 (history) sees key 0 only: m = t = 0 (q_0 = 0), l = 1
+    assert Mx[0, 0, 0] == 0.0 and Lx[0, 0, 0] == 1.0 and O[0, 0, 0, 0] == 3.0
+    # a negative temperature flips which key wins: temp = -0.5 gives t = (-1, ., 0.5)
+    temp[0, 2] = -0.5
+    O, LSE, Mx, Lx = orc.forward(q, k, v, temp, None, bounds, cfg)
+    assert Mx[0, 0, 2] == 0.5 and abs(Lx[0, 0, 2] - (1.0 + e)) < 1e-15
+    assert abs(O[0, 2, 0, 0] - (11.0 + 3.0 * e) / (1.0 + e)) < 1e-14
+
+
+@pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
+def test_zero_temperature_is_a_uniform_softmax(method, cap, alpha, beta):
+    """temp_i = 0 makes every live logit 0: P is uniform over the live keys, so
+    O is their mean value, m = 0, l = the live count and LSE = ln(count)."""
+    rng = np.random.default_rng(41)
+    B, L, H, D = 1, 9, 2, 4
+    q, k, v, do, _, _, _ = _inputs(rng, B, L, H, H, D)
+    t = np.zeros((B, L))
+    cfg = orc.OracleConfig(sm_scale=0.7, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+                           causal=True)
+    O, LSE, Mx, Lx = orc.forward(q, k, v, t, None, None, cfg)
+    for h in range(H):
+        for i in range(L):
+            n = i + 1
+            np.testing.assert_allclose(O[0, i, h], v[0, :n, h].mean(axis=0), rtol=1e-13, atol=1e-14)
+            assert Mx[0, h, i] == 0.0 and Lx[0, h, i] == n
+            assert abs(LSE[0, h, i] - math.log(n)) < 1e-14
 
 
 # ---------------------------------------------------------------------------
