@@ -176,6 +176,24 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
                                  cudaStream_t stream);
 
 /*
+ * The backward with every optional input and output; capattn_bwd is this call
+ * with dlse = dtemp = NULL, capattn_bwd_dtemp with dlse = NULL.
+ * dlse [B,Hq,L] float32 (device, nullable): an upstream gradient of the lse
+ * that capattn_fwd returns.  Since d lse_i / d t_ij = P_ij, it adds
+ * dlse_i * P_ij to dT (the same form as the z-loss term of
+ * mosaic_backward.py's backward kernels), so a caller whose own loss uses lse
+ * gets that part of the gradient in dq, dk, dv (and dtemp).  Rows that are
+ * fully masked ignore it.  dtemp [B,L] float32 (nullable) as in
+ * capattn_bwd_dtemp; it needs temp (CAPATTN_ERR_INVALID_ARG otherwise).
+ * Everything else is as in capattn_bwd.
+ */
+capattn_status capattn_bwd_ex(const capattn_config* cfg, const void* q, const void* k, const void* v,
+                              const float* temp, const int32_t* seg, const int32_t* bounds,
+                              const void* o, const float* lse, const void* dO, const float* dlse,
+                              void* dq, void* dk, void* dv, float* delta, float* dtemp,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the device status word at the start
  * of `workspace`.  Returns CAPATTN_OK, CAPATTN_ERR_DEVICE_TIMEOUT or
  * CAPATTN_ERR_DEVICE_DATA; *raw_bits (nullable) receives the raw bits
@@ -183,6 +201,23 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
  * 8 = history / candidate ids not contiguous, from capattn_ranker_bounds_from_ids).
  */
 capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint32_t* raw_bits);
+
+/*
+ * Self-check of the kernels' bounded waits (the pages have no counterpart:
+ * this library bounds every mbarrier wait of its tcgen05 kernels instead of
+ * waiting forever, and this call exercises that protocol).  Launches one CTA
+ * per SM, each shaped like the attention kernels: it allocates all 512 TMEM
+ * columns, one warp waits on an mbarrier that nothing arrives on for limit_ns
+ * nanoseconds of the global timer (1 .. 100,000,000), gives up, records the
+ * timeout bit (1) in the status word at the start of `workspace` and raises the
+ * CTA's abort flag; the other waiting warps leave on the flag; TMEM is freed.
+ * Afterwards capattn_device_status returns CAPATTN_ERR_DEVICE_TIMEOUT, and the
+ * attention kernels run normally (a leaked TMEM allocation would stall them).
+ * workspace: device, 256-byte aligned, at least 256 bytes.  Async on `stream`.
+ * CAPATTN_ERR_WORKSPACE for a null or misaligned workspace,
+ * CAPATTN_ERR_INVALID_ARG for a limit outside the range.
+ */
+capattn_status capattn_check_bounded_wait(void* workspace, uint64_t limit_ns, cudaStream_t stream);
 
 /*
  * Ranker bounds from history / candidate segment ids (mosaic_backward.py's
@@ -248,16 +283,30 @@ capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* 
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress with that device current); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: after cudaDeviceReset (or anything else that tears down the
+ *    device's primary context) it is stale, so do not call this entry point on
+ *    that device again.
  *  - All calls on a device share the one array: calls that may overlap on the
  *    GPU (different streams, or concurrent host threads) race on it and must be
- *    serialised by the caller.  Device-side status bits are not reported; use
- *    capattn_fwd with a workspace to read them.
+ *    serialised by the caller.  Each call clears the array's status word first;
+ *    read the bits that call left (wait timeouts, bad segment ids or ranker
+ *    bounds) with capattn_noalloc_status before the next call.
  */
 capattn_status capattn_fwd_noalloc(const capattn_config* cfg, const void* q, const void* k,
                                    const void* v, const float* temp, const int32_t* seg,
                                    const int32_t* bounds, void* o, float* lse, float* m, float* l,
                                    cudaStream_t stream);
+
+/*
+ * Device status left by the last capattn_fwd_noalloc call on the current
+ * device (no counterpart on the pages; the companion of that entry point).
+ * Synchronises `stream`, copies the status word of the fixed array into a host
+ * word, clears it, and returns as capattn_device_status does (CAPATTN_OK,
+ * CAPATTN_ERR_DEVICE_TIMEOUT or CAPATTN_ERR_DEVICE_DATA, raw bits in *raw_bits,
+ * nullable).  Allocates no device memory.
+ */
+capattn_status capattn_noalloc_status(cudaStream_t stream, uint32_t* raw_bits);
 
 /*
  * Per-kernel timing.  While enabled, every kernel the library launches whose

@@ -238,27 +238,13 @@ def forward(q, k, v, temp, seg, bounds, cfg: OracleConfig):
     return O, LSE, Mx, Lx
 
 
-def forward_rows(q, k, v, temp, seg, bounds, cfg: OracleConfig, b: int, h: int, rows):
-    """O [len(rows), D] and LSE [len(rows)] for selected query rows of head (b, h)."""
-    Hq, Hkv = q.shape[2], k.shape[2]
-    g = h // (Hq // Hkv)
-    L, Lk = q.shape[1], k.shape[1]
-    _check_lengths(L, Lk, seg, bounds)
-    t_row, s_row, b_row = _row_inputs(temp, seg, bounds, b, L)
-    rows = np.asarray(rows)
-    M = mask_rows(rows, Lk, cfg, s_row, b_row)
-    o, lse, m, l, _, _ = _forward_block(np.asarray(q[b, rows, h], np.float64),
-                                        np.asarray(k[b, :, g], np.float64),
-                                        np.asarray(v[b, :, g], np.float64), t_row[rows], M, cfg)
-    return o, lse
-
-
 # ---------------------------------------------------------------------------
 # Backward: mosaic_backward.py dQ / dK-dV kernels and the delta pre-pass,
 # triton_kernels.py dQ / dK-dV kernels for where temperature enters.
 # ---------------------------------------------------------------------------
 
-def _backward_block(q_rows, k, v, do_rows, temp_rows, M, lse_rows, delta_rows, cfg):
+def _backward_block(q_rows, k, v, do_rows, temp_rows, M, lse_rows, delta_rows, cfg,
+                    dlse_rows=None):
     """dQ rows plus this block's contributions to dK and dV of its KV head."""
     s = cfg.sm_scale * (q_rows @ k.T)
     t = temp_rows[:, None] * cap_forward(s, cfg)
@@ -267,16 +253,21 @@ def _backward_block(q_rows, k, v, do_rows, temp_rows, M, lse_rows, delta_rows, c
     P = np.where(M, np.exp(np.where(M, t, 0.0) - lse_safe[:, None]), 0.0)
     dP = do_rows @ v.T
     dT = P * (dP - delta_rows[:, None]) + cfg.z_loss_weight * P * lse_safe[:, None]
+    if dlse_rows is not None:
+        # d LSE_i / d t_ij = P_ij: an upstream gradient of the LSE adds dLSE_i P_ij
+        dT = dT + P * np.where(live, dlse_rows, 0.0)[:, None]
     dX = cfg.sm_scale * cap_derivative(s, cfg) * temp_rows[:, None] * dT
     return dX @ k, dX.T @ q_rows, P.T @ do_rows
 
 
-def backward(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
+def backward(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig, dLSE=None):
     """Returns dQ [B,L,Hq,D], dK and dV [B,Lk,Hkv,D] and delta [B,Hq,L] (float64).
 
     delta_i = sum_d O_id dO_id; dP = dO V^T; dT = P (dP - delta) + z P LSE;
     dX = sm_scale * cap'(s) * temp_i * dT; dQ = dX K; dK_g = sum over the
-    group's query heads of dX^T Q; dV_g likewise of P^T dO.
+    group's query heads of dX^T Q; dV_g likewise of P^T dO.  dLSE [B,Hq,L]
+    (optional) is an upstream gradient of the returned LSE; it adds
+    dLSE_i P_ij to dT (ignored on fully masked rows).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -299,7 +290,8 @@ def backward(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
             for h in range(Hq):
                 g = h // G
                 dq, dk, dv = _backward_block(q[b, rows, h], k[b, :, g], v[b, :, g], dO[b, rows, h],
-                                             t_row[rows], M, LSE[b, h, rows], delta[b, h, rows], cfg)
+                                             t_row[rows], M, LSE[b, h, rows], delta[b, h, rows], cfg,
+                                             None if dLSE is None else dLSE[b, h, rows])
                 dQ[b, rows, h] = dq
                 dK[b, :, g] += dk
                 dV[b, :, g] += dv
@@ -339,7 +331,7 @@ def backward_kv_head(q, k, v, temp, seg, bounds, dO, cfg: OracleConfig, b: int, 
     return dQ, dK, dV, O, LSE
 
 
-def backward_dtemp(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
+def backward_dtemp(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig, dLSE=None):
     """Gradient with respect to the per-query temperature, [B, L] (float64).
 
     The temperature multiplies the capped score, t = temp_i * c with
@@ -375,19 +367,24 @@ def backward_dtemp(q, k, v, temp, seg, bounds, O, LSE, dO, cfg: OracleConfig):
                 P = np.where(M, np.exp(np.where(M, t_row[rows][:, None] * c, 0.0) - lse_safe[:, None]), 0.0)
                 dP = dO[b, rows, h] @ v[b, :, g].T
                 dT = P * (dP - delta[b, h, rows][:, None]) + cfg.z_loss_weight * P * lse_safe[:, None]
+                if dLSE is not None:
+                    dT = dT + P * np.where(live, dLSE[b, h, rows], 0.0)[:, None]
                 dtemp[b, rows] += np.sum(dT * c, axis=1)
     return dtemp
 
 
-def loss(q, k, v, temp, seg, bounds, dO, cfg: OracleConfig) -> float:
-    """L = sum(O * dO) + (z/2) * sum of LSE^2 over rows that are not fully masked.
+def loss(q, k, v, temp, seg, bounds, dO, cfg: OracleConfig, dLSE=None) -> float:
+    """L = sum(O * dO) + (z/2) * sum of LSE^2 over rows that are not fully masked
+    (+ sum of LSE * dLSE over those rows when dLSE is given).
 
     The backward above is the gradient of this scalar with respect to Q, K, V.
     """
     O, LSE, _, _ = forward(q, k, v, temp, seg, bounds, cfg)
     live = np.isfinite(LSE)
+    lse = np.where(live, LSE, 0.0)
+    extra = 0.0 if dLSE is None else float(np.sum(lse * np.asarray(dLSE, np.float64)))
     return float(np.sum(O * np.asarray(dO, np.float64))
-                 + 0.5 * cfg.z_loss_weight * np.sum(np.where(live, LSE, 0.0) ** 2))
+                 + 0.5 * cfg.z_loss_weight * np.sum(lse ** 2)) + extra
 
 
 # ---------------------------------------------------------------------------

@@ -74,11 +74,15 @@ def lib() -> ctypes.CDLL:
         h.capattn_bwd.argtypes = [cfgp] + [vp] * 13 + [vp, sz, vp]
         h.capattn_bwd_dtemp.restype = ctypes.c_int
         h.capattn_bwd_dtemp.argtypes = [cfgp] + [vp] * 14 + [vp, sz, vp]
+        h.capattn_bwd_ex.restype = ctypes.c_int
+        h.capattn_bwd_ex.argtypes = [cfgp] + [vp] * 15 + [vp, sz, vp]
         h.capattn_ranker_bounds_from_ids.restype = ctypes.c_int
         h.capattn_ranker_bounds_from_ids.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                      ctypes.c_int32, vp, vp, vp]
         h.capattn_device_status.restype = ctypes.c_int
         h.capattn_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        h.capattn_check_bounded_wait.restype = ctypes.c_int
+        h.capattn_check_bounded_wait.argtypes = [vp, ctypes.c_uint64, vp]
         h.capattn_visit_map_host.restype = ctypes.c_int
         h.capattn_visit_map_host.argtypes = [cfgp, vp, vp, ctypes.c_int, vp, sz,
                                              ctypes.POINTER(sz)]
@@ -100,11 +104,11 @@ def lib() -> ctypes.CDLL:
 
 
 EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn_workspace_bytes",
-                    "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_bwd_dtemp",
+                    "capattn_tile_sizes", "capattn_fwd", "capattn_bwd", "capattn_bwd_dtemp", "capattn_bwd_ex",
                     "capattn_device_status", "capattn_ranker_bounds_from_ids",
                     "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host",
                     "capattn_profile_enable", "capattn_profile_select", "capattn_profile_read", "capattn_kernel_name",
-                    "capattn_fwd_noalloc")
+                    "capattn_fwd_noalloc", "capattn_noalloc_status", "capattn_check_bounded_wait")
 KERNEL_KINDS = ("prepass", "fwd", "delta", "dkv", "dq")
 
 
@@ -246,6 +250,29 @@ def capattn_bwd_dtemp(q, k, v, o, lse, do, ap: AttnParams, temp, seg=None, bound
     return dq, dk, dv, delta, dtemp
 
 
+def capattn_bwd_ex(q, k, v, o, lse, do, ap: AttnParams, temp=None, seg=None, bounds=None, dlse=None,
+                   want_dtemp=False, workspace=None, stream=None):
+    """Backward with an optional upstream LSE gradient dlse [B,Hq,L] (fp32) and,
+    with want_dtemp, the temperature gradient.  Returns (dq, dk, dv, delta, dtemp)."""
+    if want_dtemp and temp is None:
+        raise ValueError("the temperature gradient needs the temperature tensor")
+    cfg = _config(q, k, ap)
+    B, L, Hq = cfg.B, cfg.L, cfg.Hq
+    if workspace is None:
+        workspace = new_workspace(cfg, q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    delta = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    dtemp = torch.empty(B, L, dtype=torch.float32, device=q.device) if want_dtemp else None
+    st = lib().capattn_bwd_ex(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(temp), _ptr(seg),
+                              _ptr(bounds), _ptr(o), _ptr(lse), _ptr(do), _ptr(dlse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), _ptr(delta), _ptr(dtemp), _ptr(workspace),
+                              workspace.numel(), _stream(stream))
+    _check(st, "capattn_bwd_ex")
+    return dq, dk, dv, delta, dtemp
+
+
 def ranker_bounds_from_ids(seg: torch.Tensor, history_id: int, candidate_id: int, workspace=None,
                            stream=None) -> torch.Tensor:
     """[B, L] int32 segment ids on the GPU -> [B, 4] int32 ranker bounds (hl, hu, cl, cu)."""
@@ -262,6 +289,12 @@ def capattn_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, in
     bits = ctypes.c_uint32(0)
     st = lib().capattn_device_status(_ptr(workspace), _stream(stream), ctypes.byref(bits))
     return int(st), int(bits.value)
+
+
+def capattn_check_bounded_wait(workspace: torch.Tensor, limit_ns: int, stream=None):
+    """Runs the bounded-wait self-check (a wait that times out after limit_ns)."""
+    _check(lib().capattn_check_bounded_wait(_ptr(workspace), int(limit_ns), _stream(stream)),
+           "capattn_check_bounded_wait")
 
 
 def capattn_tile_sizes(cfg: CapattnConfig):
@@ -342,26 +375,29 @@ def capattn_profile_read(reset: bool = True) -> dict:
 
 
 class CapAttnFunction(torch.autograd.Function):
-    """Autograd wrapper: forward saves (o, lse); backward calls capattn_bwd.
-    Gradients flow to q, k, v and, when it requires grad, to the temperature
-    (capattn_bwd_dtemp); segment ids and bounds are inputs only."""
+    """Autograd wrapper: forward saves (o, lse); backward calls capattn_bwd_ex.
+    Gradients flow to q, k, v and, when it requires grad, to the temperature;
+    a loss that uses the returned lse contributes through its gradient dlse
+    (d lse_i / d t_ij = P_ij).  Segment ids and bounds are inputs only."""
 
     @staticmethod
     def forward(ctx, q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None):
         o, lse, _, _ = capattn_fwd(q, k, v, ap, temp, seg, bounds)
         ctx.save_for_backward(q, k, v, o, lse, temp, seg, bounds)
         ctx.ap = ap
+        ctx.set_materialize_grads(False)
         return o, lse
 
     @staticmethod
     def backward(ctx, do, dlse):
         q, k, v, o, lse, temp, seg, bounds = ctx.saved_tensors
-        if temp is not None and ctx.needs_input_grad[4]:
-            dq, dk, dv, _, dtemp = capattn_bwd_dtemp(q, k, v, o, lse, do.contiguous(), ctx.ap, temp,
-                                                     seg, bounds)
-            return dq, dk, dv, None, dtemp, None, None
-        dq, dk, dv, _ = capattn_bwd(q, k, v, o, lse, do.contiguous(), ctx.ap, temp, seg, bounds)
-        return dq, dk, dv, None, None, None, None
+        want_dtemp = temp is not None and ctx.needs_input_grad[4]
+        do = torch.zeros_like(o) if do is None else do.contiguous()
+        if dlse is not None:
+            dlse = dlse.to(torch.float32).contiguous()
+        dq, dk, dv, _, dtemp = capattn_bwd_ex(q, k, v, o, lse, do, ctx.ap, temp, seg, bounds,
+                                              dlse=dlse, want_dtemp=want_dtemp)
+        return dq, dk, dv, None, dtemp, None, None
 
 
 def attention(q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None):

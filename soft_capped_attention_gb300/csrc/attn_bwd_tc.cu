@@ -5,7 +5,8 @@
 //
 // Per live pair (query i, key j), with x = temp_i * cap(s_ij) * log2(e):
 //   P_ij  = 2^(x - LSE_i * log2(e))                       (0 when masked)
-//   dX_ij = sm_scale * temp_i * cap'(s_ij) * P_ij * (dP_ij - delta_i + z * LSE_i)
+//   dX_ij = sm_scale * temp_i * cap'(s_ij) * P_ij * (dP_ij - delta_i + z * LSE_i + dLSE_i)
+// (dLSE: an optional upstream gradient of the forward's LSE, 0 without one)
 //
 // Both kernels work in 128 x 128 steps with four tcgen05 phases per step:
 // score MMAs (S and dP, N = 128, separately committed), the elementwise pass,
@@ -82,7 +83,7 @@ struct StepIter {
 // Raw per-query-column inputs of one step, loaded ahead of use and left
 // untouched until then (arithmetic on them here would stall on the loads).
 struct ColRaw {
-  float lse, dl, temp;
+  float lse, dl, gl, temp;  // gl: upstream gradient of the LSE (0 without one)
   int4 ri;
 };
 
@@ -90,6 +91,7 @@ __device__ __forceinline__ ColRaw load_col_raw(const Params& p, int b, int h, in
   ColRaw r;
   r.lse = -INFINITY;
   r.dl = 0.f;
+  r.gl = 0.f;
   r.temp = 1.f;
   r.ri = make_int4(0, 0, -1, 0);
   const int i = qt * BT + c;
@@ -97,6 +99,7 @@ __device__ __forceinline__ ColRaw load_col_raw(const Params& p, int b, int h, in
     const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
     r.lse = p.lse[rr];
     r.dl = p.delta[rr];
+    if (p.dlse) r.gl = p.dlse[rr];
     if (p.temp) r.temp = p.temp[(size_t)b * p.L + i];
     r.ri = p.rowinfo[(size_t)b * p.L + i];
   }
@@ -438,7 +441,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (tid < 64) {
         const bool fin = isfinite(r.lse);
         const float lse2 = fin ? r.lse * kL2E : 0.f;
-        const float radd = -r.dl + (fin ? p.z_loss_weight * r.lse : 0.f);
+        const float radd = -r.dl + (fin ? p.z_loss_weight * r.lse + r.gl : 0.f);
         float mul, add;
         row_consts<METHOD>(p.cap, p.sm_scale, r.temp, &mul, &add);
         const float dsc = row_dscale<METHOD>(p.cap, p.sm_scale, r.temp);
@@ -813,6 +816,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
     const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
     const float lse = valid ? p.lse[rr] : -INFINITY;
+    const float gl = (p.dlse && valid) ? p.dlse[rr] : 0.f;
     bool aborted = false;
     // delta_i = rowsum(O * dO) (the pre-pass of the backward), computed here for
     // the tile's rows: each warpgroup sums its 64 dims, O from global memory and
@@ -880,7 +884,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       row_consts<METHOD>(p.cap, p.sm_scale, temp, &mul, &add);
       const float addl = add - (fin ? lse * kL2E : 0.f);
       const float dsc = row_dscale<METHOD>(p.cap, p.sm_scale, temp);
-      const float radd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
+      const float radd = -dl + (fin ? p.z_loss_weight * lse + gl : 0.f);
       rc.a = make_float4(mul, mul, addl, addl);
       rc.b = make_float4(-dsc, -dsc, -dsc * radd, -dsc * radd);
       dr.radd = f2(radd, radd);

@@ -161,9 +161,10 @@ __global__ void __launch_bounds__(NT) dq_fp32_kernel(Params p) {
   const size_t r = ((size_t)b * p.Hq + h) * p.L + i;
   const float lse = valid ? p.lse[r] : -INFINITY;
   const float dl = valid ? p.delta[r] : 0.f;
+  const float gl = (p.dlse && valid) ? p.dlse[r] : 0.f;
   const bool fin = isfinite(lse);
   const float lse2 = fin ? lse * kLog2e : 0.f;
-  const float rowadd = -dl + (fin ? p.z_loss_weight * lse : 0.f);
+  const float rowadd = -dl + (fin ? p.z_loss_weight * lse + gl : 0.f);
   const float c1 = p.sm_scale * temp;
   const float tl = temp * kLog2e;
   float acc[D / 4];
@@ -264,10 +265,11 @@ __global__ void __launch_bounds__(NT) dkv_fp32_kernel(Params p) {
           const size_t r = ((size_t)b * p.Hq + h) * p.L + i;
           const float lse = valid ? p.lse[r] : -INFINITY;
           const float dl = valid ? p.delta[r] : 0.f;
+          const float gl = (p.dlse && valid) ? p.dlse[r] : 0.f;
           const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
           const bool fin = isfinite(lse);
           Cq[4 * threadIdx.x + 0] = fin ? lse * kLog2e : 0.f;
-          Cq[4 * threadIdx.x + 1] = -dl + (fin ? p.z_loss_weight * lse : 0.f);
+          Cq[4 * threadIdx.x + 1] = -dl + (fin ? p.z_loss_weight * lse + gl : 0.f);
           Cq[4 * threadIdx.x + 2] = p.sm_scale * temp;
           Cq[4 * threadIdx.x + 3] = temp * kLog2e;
         }

@@ -147,16 +147,17 @@ using namespace capattn;
 // the dQ kernels).
 static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const void* k, const void* v,
                                const float* temp, const int32_t* seg, const int32_t* bounds,
-                               const void* o, const float* lse, const void* dO, void* dq, void* dk,
-                               void* dv, float* delta, float* dtemp, void* workspace,
-                               size_t workspace_bytes, cudaStream_t stream) {
+                               const void* o, const float* lse, const void* dO, const float* dlse,
+                               void* dq, void* dk, void* dv, float* delta, float* dtemp,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   capattn_status st = validate(cfg);
   if (st != CAPATTN_OK) return st;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
     return CAPATTN_ERR_INVALID_ARG;
   st = check_masks(*cfg, seg, bounds);
   if (st != CAPATTN_OK) return st;
-  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, temp, seg, bounds, dtemp};
+  if (dtemp && !temp) return CAPATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, temp, seg, bounds, dtemp, dlse};
   for (const void* ptr : ptrs)
     if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
   st = check_ws(*cfg, workspace, workspace_bytes);
@@ -165,7 +166,7 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
   fill_params(p, *cfg, workspace);
   p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
   p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
-  p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta; p.dtemp = dtemp;
+  p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta; p.dtemp = dtemp; p.dlse = dlse;
   cudaError_t e = cudaSuccess;
   if (dtemp) {
     e = cudaMemsetAsync(dtemp, 0, (size_t)cfg->B * cfg->L * sizeof(float), stream);
@@ -243,8 +244,17 @@ capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void*
                            const void* o, const float* lse, const void* dO, void* dq, void* dk,
                            void* dv, float* delta, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
-  return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, dq, dk, dv, delta, nullptr, workspace,
-                  workspace_bytes, stream);
+  return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, nullptr, dq, dk, dv, delta, nullptr,
+                  workspace, workspace_bytes, stream);
+}
+
+capattn_status capattn_bwd_ex(const capattn_config* cfg, const void* q, const void* k, const void* v,
+                              const float* temp, const int32_t* seg, const int32_t* bounds,
+                              const void* o, const float* lse, const void* dO, const float* dlse,
+                              void* dq, void* dk, void* dv, float* delta, float* dtemp,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, dlse, dq, dk, dv, delta, dtemp,
+                  workspace, workspace_bytes, stream);
 }
 
 capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const void* k,
@@ -254,8 +264,8 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
                                  float* dtemp, void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream) {
   if (!temp || !dtemp) return CAPATTN_ERR_INVALID_ARG;
-  return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, dq, dk, dv, delta, dtemp, workspace,
-                  workspace_bytes, stream);
+  return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, nullptr, dq, dk, dv, delta, dtemp,
+                  workspace, workspace_bytes, stream);
 }
 
 capattn_status capattn_ranker_bounds_from_ids(const int32_t* seg, int32_t B, int32_t L,
@@ -283,6 +293,16 @@ capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint3
   if (bits & kStatusTimeoutBit) return CAPATTN_ERR_DEVICE_TIMEOUT;
   if (bits) return CAPATTN_ERR_DEVICE_DATA;
   return CAPATTN_OK;
+}
+
+capattn_status capattn_check_bounded_wait(void* workspace, uint64_t limit_ns, cudaStream_t stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CAPATTN_ERR_WORKSPACE;
+  if (limit_ns < 1 || limit_ns > 100000000ull) return CAPATTN_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return CAPATTN_ERR_CUDA;
+  return cuda_status(launch_wait_check(static_cast<uint32_t*>(workspace), limit_ns, sms, stream));
 }
 
 capattn_status capattn_visit_map_host(const capattn_config* cfg, const int32_t* seg,

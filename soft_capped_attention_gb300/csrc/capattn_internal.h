@@ -43,6 +43,7 @@ struct Params {
   void* dv;
   float* delta;
   float* dtemp;           // [B, L] gradient of the temperature (accumulated), or null
+  const float* dlse;      // [B, Hq, L] upstream gradient of the LSE, or null
   // workspace pieces
   uint32_t* status;
   int4* rowinfo;          // [B, L] (lo, hi, e, 0)
@@ -105,6 +106,7 @@ cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_bf16(const Params& p, cudaStream_t s);
+cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, int ctas, cudaStream_t s);
 cudaError_t launch_ranker_bounds(const int32_t* seg, int B, int L, int32_t history_id,
                                  int32_t candidate_id, int32_t* bounds, uint32_t* status,
                                  cudaStream_t s);

@@ -79,17 +79,18 @@ __device__ __forceinline__ void mbar_poll(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// sets the timeout bit in *status and in *abort) when the limit is reached or
-// another thread of the CTA already gave up.
+// sets the timeout bit in *status and in *abort) when the limit (limit_ns of
+// the global timer) is reached or another thread of the CTA already gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         atomicOr(status, kStatusTimeoutBit);
         *abort_flag = 1;
         return false;
@@ -102,8 +103,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 // warp-collective tcgen05 instructions must not let a late timeout in one lane
 // split the warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* status,
-                                               volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, status, abort_flag);
+                                               volatile int* abort_flag,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, status, abort_flag, limit_ns);
   return __all_sync(0xFFFFFFFFu, ok);
 }
 

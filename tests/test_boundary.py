@@ -97,6 +97,14 @@ def test_compute_calls_reject_bad_arguments_before_launch(lib):
     assert st == 1  # null dq
 
 
+def test_bounded_wait_check_rejects_bad_arguments(lib):
+    # checked on the host before any CUDA call
+    assert lib.capattn_check_bounded_wait(None, 1000, None) == 5
+    assert lib.capattn_check_bounded_wait(ctypes.c_void_p(128), 1000, None) == 5
+    assert lib.capattn_check_bounded_wait(ctypes.c_void_p(256), 0, None) == 1
+    assert lib.capattn_check_bounded_wait(ctypes.c_void_p(256), 100000001, None) == 1
+
+
 def _oracle_cfg(causal, window_len):
     return orc.OracleConfig(sm_scale=1.0, causal=causal, window_len=window_len)
 

@@ -219,6 +219,67 @@ def test_wide_cap_window_uses_running_max():
     compare(run_gpu(inp, ap, torch.bfloat16), run_oracle(inp, ap), torch.bfloat16)
 
 
+# Temperatures that are negative on some rows and exactly zero on others: a
+# negative temperature makes the row's smallest capped score its largest logit
+# (the forward's running max then tracks the raw minimum), and temperature 0 is
+# a uniform softmax over the live keys.
+NONPOS_CASES = [
+    # (dtype, D, L, cap, mask, want_ml, z)
+    ("bf16", 128, 300, "tanh", "causal", False, 0.0),
+    ("bf16", 128, 300, "tanh", "causal", True, 0.0),
+    ("bf16", 128, 513, "alsc", "window", False, 1e-3),
+    ("bf16", 128, 513, "alsc", "window", True, 1e-3),
+    ("bf16", 128, 260, "soft_sign", "packed", False, 0.0),
+    ("bf16", 128, 260, "none", "full", True, 0.0),
+    ("bf16", 128, 400, "alsc", "ranker", False, 0.0),
+    ("fp32", 64, 200, "tanh", "causal", True, 0.0),
+    ("fp32", 128, 131, "alsc", "window", True, 1e-3),
+    ("fp32", 64, 150, "none", "full", True, 0.0),
+]
+
+
+@pytest.mark.parametrize("case", NONPOS_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_nonpositive_temperature_matches_oracle(case):
+    dname, D, L, cap, mask, want_ml, z = case
+    dtype = torch.bfloat16 if dname == "bf16" else torch.float32
+    inp = make_case(2, L, 4, 2, D, dtype, mask, True, seed=L + 13)
+    rng = np.random.default_rng(L)
+    inp["temp"] = rng.choice(np.array([-1.3, -0.4, 0.0, 0.8], np.float32), size=(2, L))
+    ap = params(cap, mask, z)
+    got = run_gpu(inp, ap, dtype, want_ml=want_ml)
+    ref = run_oracle(inp, ap)
+    compare(got, ref, dtype)
+    if want_ml:
+        live = np.isfinite(ref["LSE"])
+        tol = 1e-4 if dtype == torch.float32 else 1e-3
+        np.testing.assert_allclose(got["m"][live], ref["m"][live], atol=tol)
+        np.testing.assert_allclose(got["l"][live], ref["l"][live], rtol=5e-3)
+    # rows with temperature 0: P uniform over live keys, so LSE = ln(#live)
+    zero = inp["temp"] == 0.0
+    counts = np.stack([orc.mask_matrix(L, oracle_cfg_of(ap), None if inp["seg"] is None else inp["seg"][b],
+                                       None if inp["bounds"] is None else inp["bounds"][b]).sum(axis=1)
+                       for b in range(2)])
+    for h in range(4):
+        sel = zero & (counts > 0)
+        np.testing.assert_allclose(got["LSE"][:, h][sel], np.log(counts[sel]), atol=1e-3)
+
+
+def oracle_cfg_of(ap):
+    from parity_utils import oracle_cfg
+    return oracle_cfg(ap)
+
+
+def test_dtemp_nonpositive_temperature_bf16():
+    from parity_utils import rel_fro
+    inp = make_case(2, 300, 4, 2, 128, torch.bfloat16, "causal", True, seed=301)
+    inp["temp"] = np.random.default_rng(3).choice(np.array([-1.3, -0.4, 0.0, 0.8], np.float32),
+                                                  size=(2, 300))
+    ap = params("tanh", "causal", 0.0)
+    got = _run_dtemp(inp, ap, torch.bfloat16)
+    ref, _ = _oracle_dtemp(inp, ap)
+    assert rel_fro(got["dtemp"], ref) <= 2e-2, rel_fro(got["dtemp"], ref)
+
+
 # ---------------------------------------------------------------------------
 # Temperature gradient (capattn_bwd_dtemp) against the oracle's definition.
 # ---------------------------------------------------------------------------
@@ -289,6 +350,72 @@ def test_autograd_temperature_gradient():
     ref, _ = _oracle_dtemp(inp, ap)
     from parity_utils import rel_fro
     assert rel_fro(temp.grad.cpu().numpy(), ref) <= 2e-2
+
+
+# ---------------------------------------------------------------------------
+# Upstream gradient of the returned LSE (capattn_bwd_ex dlse).
+# ---------------------------------------------------------------------------
+
+LSE_GRAD_CASES = [
+    # (dtype, D, B, L, Hq, Hkv, cap, mask, z, dtemp)
+    ("bf16", 128, 2, 300, 4, 2, "tanh", "causal", 0.0, False),
+    ("bf16", 128, 1, 513, 4, 1, "alsc", "window", 1e-3, True),
+    ("bf16", 128, 2, 400, 4, 2, "soft_sign", "ranker", 0.0, True),
+    ("fp32", 64, 2, 200, 4, 2, "tanh", "causal", 0.01, True),
+    ("fp32", 128, 1, 131, 2, 1, "none", "packed", 0.0, False),
+]
+
+
+@pytest.mark.parametrize("case", LSE_GRAD_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_lse_gradient_matches_oracle(case):
+    from parity_utils import oracle_cfg, rel_fro
+    dname, D, B, L, Hq, Hkv, cap, mask, z, want_dt = case
+    dtype = torch.bfloat16 if dname == "bf16" else torch.float32
+    inp = make_case(B, L, Hq, Hkv, D, dtype, mask, True, seed=L + 99)
+    dlse = np.random.default_rng(L).standard_normal((B, Hq, L)).astype(np.float32)
+    ap = params(cap, mask, z)
+    q, k, v, do = (to_dev(inp[n], dtype) for n in ("q", "k", "v", "do"))
+    temp, seg, bounds = to_dev(inp["temp"]), to_dev(inp["seg"]), to_dev(inp["bounds"])
+    cfg = ca.make_config(ap, B, L, Hq, Hkv, D, dtype)
+    ws = ca.new_workspace(cfg, q.device)
+    o, lse, _, _ = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws)
+    dq, dk, dv, _, dtemp = ca.capattn_bwd_ex(q, k, v, o, lse, do, ap, temp, seg, bounds,
+                                             dlse=to_dev(dlse), want_dtemp=want_dt, workspace=ws)
+    assert ca.capattn_device_status(ws) == (0, 0)
+    oc = oracle_cfg(ap)
+    O, LSE, _, _ = orc.forward(inp["q"], inp["k"], inp["v"], inp["temp"], inp["seg"], inp["bounds"], oc)
+    ref = orc.backward(inp["q"], inp["k"], inp["v"], inp["temp"], inp["seg"], inp["bounds"], O, LSE,
+                       inp["do"], oc, dLSE=dlse.astype(np.float64))
+    for got, r in zip((dq, dk, dv), ref[:3]):
+        g = got.float().cpu().numpy()
+        if dtype == torch.float32:
+            assert np.max(np.abs(g - r)) <= 1e-4
+        else:
+            assert rel_fro(g, r) <= 2e-2, rel_fro(g, r)
+    if want_dt:
+        rdt = orc.backward_dtemp(inp["q"], inp["k"], inp["v"], inp["temp"], inp["seg"], inp["bounds"],
+                                 O, LSE, inp["do"], oc, dLSE=dlse.astype(np.float64))
+        assert rel_fro(dtemp.cpu().numpy(), rdt) <= 2e-2
+
+
+def test_autograd_passes_the_lse_gradient():
+    inp = make_case(1, 300, 4, 2, 128, torch.bfloat16, "causal", True, seed=8)
+    ap = params("tanh", "causal", 0.0)
+    q, k, v, do = (to_dev(inp[n], torch.bfloat16) for n in ("q", "k", "v", "do"))
+    temp = to_dev(inp["temp"])
+    dlse = torch.randn(1, 4, 300, device="cuda")
+    qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o, lse = ca.CapAttnFunction.apply(qq, kk, vv, ap, temp, None, None)
+    ((o.float() * do.float()).sum() + (lse * dlse).sum()).backward()
+    o2, lse2, _, _ = ca.capattn_fwd(q, k, v, ap, temp)
+    dq, dk, dv, _, _ = ca.capattn_bwd_ex(q, k, v, o2, lse2, do, ap, temp, dlse=dlse)
+    assert torch.equal(qq.grad, dq) and torch.equal(kk.grad, dk) and torch.equal(vv.grad, dv)
+    # a loss of the lse alone (no gradient reaches o)
+    qq.grad = kk.grad = vv.grad = None
+    o, lse = ca.CapAttnFunction.apply(qq, kk, vv, ap, temp, None, None)
+    (lse * dlse).sum().backward()
+    dq0, dk0, dv0, _, _ = ca.capattn_bwd_ex(q, k, v, o2, lse2, torch.zeros_like(do), ap, temp, dlse=dlse)
+    assert torch.equal(qq.grad, dq0) and torch.equal(kk.grad, dk0) and torch.equal(vv.grad, dv0)
 
 
 # ---------------------------------------------------------------------------

@@ -174,6 +174,60 @@ def test_gradients_match_finite_differences(method, cap, alpha, beta, mask, z):
 
 
 @pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
+@pytest.mark.parametrize("mask", [1, 3])
+def test_lse_gradient_matches_finite_differences(method, cap, alpha, beta, mask):
+    # an upstream gradient of the returned LSE: L = sum O dO + sum LSE dLSE (+ z-loss)
+    mk = MASKS[mask]
+    rng = np.random.default_rng(23 + mask)
+    B, L, Hq, Hkv, D = 1, 7, 2, 1, 3
+    q, k, v, do, t, sg, bd = _inputs(rng, B, L, Hq, Hkv, D, seg=mk["seg"], bounds=mk["bounds"],
+                                     scale=1.5)
+    dlse = rng.standard_normal((B, Hq, L))
+    cfg = orc.OracleConfig(sm_scale=0.7, cap_method=method, cap=cap, alpha=alpha, beta=beta,
+                           causal=mk["causal"], window_len=mk["window_len"], z_loss_weight=0.05)
+    O, LSE, _, _ = orc.forward(q, k, v, t, sg, bd, cfg)
+    grads = orc.backward(q, k, v, t, sg, bd, O, LSE, do, cfg, dLSE=dlse)[:3]
+    dtemp = orc.backward_dtemp(q, k, v, t, sg, bd, O, LSE, do, cfg, dLSE=dlse)
+    h = 1e-6
+    for x, gx in zip((q, k, v, t), (*grads, dtemp)):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            x0 = x[idx]
+            x[idx] = x0 + h
+            lp = orc.loss(q, k, v, t, sg, bd, do, cfg, dLSE=dlse)
+            x[idx] = x0 - h
+            lm = orc.loss(q, k, v, t, sg, bd, do, cfg, dLSE=dlse)
+            x[idx] = x0
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(gx - fd) / max(np.linalg.norm(fd), 1e-30)
+        assert err < 1e-6, err
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_lse_gradient_matches_torch_logsumexp(causal):
+    # no cap, temperature 1: LSE = logsumexp of the scaled scores; float64 autograd
+    rng = np.random.default_rng(29)
+    B, L, H, D = 1, 19, 2, 8
+    q, k, v, do, _, _, _ = _inputs(rng, B, L, H, H, D, temp=False)
+    dlse = rng.standard_normal((B, H, L))
+    cfg = orc.OracleConfig(sm_scale=0.4, causal=causal)
+    O, LSE, _, _ = orc.forward(q, k, v, None, None, None, cfg)
+    dQ, dK, dV, _ = orc.backward(q, k, v, None, None, None, O, LSE, do, cfg, dLSE=dlse)
+    tq, tk, tv = (torch.tensor(x).permute(0, 2, 1, 3).requires_grad_(True) for x in (q, k, v))
+    sc = 0.4 * tq @ tk.transpose(-1, -2)
+    if causal:
+        sc = sc.masked_fill(torch.ones(L, L, dtype=torch.bool).triu(1), float("-inf"))
+    lse = torch.logsumexp(sc, dim=-1)
+    out = torch.softmax(sc, dim=-1) @ tv
+    ((out * torch.tensor(do).permute(0, 2, 1, 3)).sum() + (lse * torch.tensor(dlse)).sum()).backward()
+    np.testing.assert_allclose(dQ, tq.grad.permute(0, 2, 1, 3).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dK, tk.grad.permute(0, 2, 1, 3).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dV, tv.grad.permute(0, 2, 1, 3).numpy(), atol=1e-11)
+
+
+@pytest.mark.parametrize("method,cap,alpha,beta", CAPS)
 def test_gradients_match_finite_differences_nonpositive_temperature(method, cap, alpha, beta):
     rng = np.random.default_rng(17)
     B, L, Hq, Hkv, D = 1, 7, 2, 1, 3
