@@ -634,19 +634,23 @@ __device__ __forceinline__ void dq_step(const uint32_t (&s)[64], uint32_t dp_bas
 
 // dQ: one CTA per (batch, query head, 128-query tile), looping over the KV tiles
 // of its visit map.  Per step j (M = queries, N = keys, K-dim = head dim):
-//   S = Q K_j^T and dP = dO V_j^T   (SS MMAs, N = 128, separate commits)
+//   S = Q K_j^T and dP = dO V_j^T   (SS MMAs, N = 128, separately committed)
 //   dQ += dX K_j                    (TS MMAs, 16 keys per chunk)
-// TMEM: S [0, 128), dP [128, 256), dQ [256, 384).  The elementwise warpgroups
-// own 64 key columns each, copy their S columns to registers and release them
-// (S of step j + 1 then runs during step j's elementwise work), and pack dX over
-// their dP columns chunk by chunk.
+// TMEM: S [0, 128), dP of even steps [128, 256), dP of odd steps [256, 384),
+// dQ [384, 512).  K and V have their own two-stage rings: V_j is read only by
+// dP_j, so its stage is free as soon as dP_j has run, and dP of step j + 2 is
+// computed (into the buffer step j used) right after step j's accumulation
+// MMAs; it is ready long before step j + 2 starts.  S of step j + 1 goes into
+// the S buffer once the elementwise warps have copied step j's S to registers
+// (at the start of step j) and K_{j+1} has landed.  The elementwise warpgroups
+// own 64 key columns each and pack dX over the step's dP columns chunk by chunk.
 template <int METHOD, bool DT>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
              const __grid_constant__ CUtensorMap mdq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[20];
+  __shared__ __align__(8) uint64_t bars[24];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float dxch[2][BT];   // half-row sums of O * dO (delta), one per warpgroup
@@ -663,27 +667,35 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   const uint32_t sKV = base + 2 * TILE;  // stage s: K at sKV + s*2*TILE, V at + TILE
 
   const uint32_t bar_q = smem_u32(&bars[0]);
-  const uint32_t bar_full = smem_u32(&bars[1]);    // + s*8
-  const uint32_t bar_empty = smem_u32(&bars[3]);   // + s*8
-  const uint32_t bar_s = smem_u32(&bars[5]);
-  const uint32_t bar_dp = smem_u32(&bars[6]);
-  const uint32_t bar_sfree = smem_u32(&bars[7]);
-  const uint32_t bar_chunk = smem_u32(&bars[8]);   // + c*8: chunk c packed by both warpgroups
-  const uint32_t bar_final = smem_u32(&bars[16]);
-  const uint32_t bar_dx = smem_u32(&bars[17]);     // both warpgroups wrote their delta halves
+  const uint32_t bar_kfull = smem_u32(&bars[1]);   // + s*8: K of stage s landed
+  const uint32_t bar_vfull = smem_u32(&bars[3]);   // + s*8: V of stage s landed
+  const uint32_t bar_kempty = smem_u32(&bars[5]);  // + s*8: K of stage s no longer read
+  const uint32_t bar_vempty = smem_u32(&bars[7]);  // + s*8: V of stage s no longer read
+  const uint32_t bar_s = smem_u32(&bars[9]);       // S of the step complete
+  const uint32_t bar_sfree = smem_u32(&bars[10]);  // S copied to registers (8 warps)
+  const uint32_t bar_dp = smem_u32(&bars[11]);     // + x*8: dP in buffer x complete
+  // + (4 * (j & 1) + c) * 8: chunk c of step j packed by both warpgroups.  The
+  // elementwise warps may run a step ahead of the issuer (dP of the next step is
+  // ready early), so even and odd steps use separate barriers: a barrier then
+  // never completes a phase the issuer has not waited for yet.
+  const uint32_t bar_chunk = smem_u32(&bars[13]);
+  const uint32_t bar_final = smem_u32(&bars[21]);
+  const uint32_t bar_dx = smem_u32(&bars[22]);     // both warpgroups wrote their delta halves
 
   const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar_q, 1);
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_vfull + 8 * s, 1);
+      mbar_init(bar_kempty + 8 * s, 1);
+      mbar_init(bar_vempty + 8 * s, 1);
+      mbar_init(bar_dp + 8 * s, 1);
     }
     mbar_init(bar_s, 1);
-    mbar_init(bar_dp, 1);
     mbar_init(bar_sfree, 8);
-    for (int c = 0; c < 4; ++c) mbar_init(bar_chunk + 8 * c, 8);
+    for (int c = 0; c < 8; ++c) mbar_init(bar_chunk + 8 * c, 8);
     mbar_init(bar_final, 1);
     mbar_init(bar_dx, 8);
     fence_mbar_init();
@@ -716,26 +728,40 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tma_load_4d(sO + SLAB, &mdo, bar_q, 64, h, q0, b);
       }
       __syncwarp();
+      // V of step j as soon as dP of step j - 2 has read its stage, then K of
+      // step j once step j - 2's accumulation MMAs have
       TileIter it(map, p.wk);
       int t, j = 0;
       while (!__any_sync(0xFFFFFFFFu, abort_flag != 0) && it.next(t)) {
         const int s = j % NSTAGE, u = j / NSTAGE;
-        if (u > 0 && !mbar_wait_warp(bar_empty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
+        const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
+        if (u > 0 && !mbar_wait_warp(bar_vempty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
         if (leader) {
-          const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
-          mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
-          tma_load_4d(sK, &mk, bar_full + 8 * s, 0, g, t * BT, b);
-          tma_load_4d(sK + SLAB, &mk, bar_full + 8 * s, 64, g, t * BT, b);
-          tma_load_4d(sV, &mv, bar_full + 8 * s, 0, g, t * BT, b);
-          tma_load_4d(sV + SLAB, &mv, bar_full + 8 * s, 64, g, t * BT, b);
+          mbar_expect_tx(bar_vfull + 8 * s, TILE);
+          tma_load_4d(sV, &mv, bar_vfull + 8 * s, 0, g, t * BT, b);
+          tma_load_4d(sV + SLAB, &mv, bar_vfull + 8 * s, 64, g, t * BT, b);
+        }
+        __syncwarp();
+        if (u > 0 && !mbar_wait_warp(bar_kempty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) {
+          ++j;  // V of this step is in flight: drained below
+          break;
+        }
+        if (leader) {
+          mbar_expect_tx(bar_kfull + 8 * s, TILE);
+          tma_load_4d(sK, &mk, bar_kfull + 8 * s, 0, g, t * BT, b);
+          tma_load_4d(sK + SLAB, &mk, bar_kfull + 8 * s, 64, g, t * BT, b);
         }
         __syncwarp();
         ++j;
       }
       if (leader) {
+        // (on an early exit the last step's K may not have been issued; its
+        // barrier then never completes and the bounded wait just runs out)
         drain_wait(bar_q, 0);
-        for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj)
-          drain_wait(bar_full + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+        for (int jj = (j > NSTAGE ? j - NSTAGE : 0); jj < j; ++jj) {
+          drain_wait(bar_vfull + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+          drain_wait(bar_kfull + 8 * (jj % NSTAGE), (jj / NSTAGE) & 1);
+        }
       }
       __syncwarp();
     }
@@ -747,44 +773,56 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       const uint64_t dQ = smem_desc(sQ, 16, 1024), dO = smem_desc(sO, 16, 1024);
       const uint64_t dKV = smem_desc(sKV, 16, 1024);        // K / V stages, K-major
       const uint64_t dKVmn = smem_desc(sKV, SLAB, 1024);    // the same, MN-major
-      bool ok = mbar_wait_warp(bar_q, 0, p.status, &abort_flag) &&
-                mbar_wait_warp(bar_full, 0, p.status, &abort_flag);
-      if (ok) {
+      // S of step j into the S buffer (step j - 1's S has been copied out)
+      auto issue_s = [&](int j) -> bool {
+        if (!mbar_wait_warp(bar_kfull + 8 * (j % NSTAGE), (j / NSTAGE) & 1, p.status, &abort_flag))
+          return false;
         tc_fence_after();
         if (leader) {
-          issue_scores(tmem, dQ, dKV);                          // S  = Q K^T
+          issue_scores(tmem, dQ, desc_add(dKV, (uint32_t)((j % NSTAGE) * 2 * TILE)));
           mma_commit(bar_s);
-          issue_scores(tmem + 128u, dO, desc_add(dKV, TILE));   // dP = dO V^T
-          mma_commit(bar_dp);
         }
         __syncwarp();
-      }
+        return true;
+      };
+      // dP of step j into buffer j & 1 (step j - 2's accumulation MMAs, which
+      // read that buffer, were issued before); V's stage is then free
+      auto issue_dp = [&](int j) -> bool {
+        if (!mbar_wait_warp(bar_vfull + 8 * (j % NSTAGE), (j / NSTAGE) & 1, p.status, &abort_flag))
+          return false;
+        tc_fence_after();
+        if (leader) {
+          issue_scores(tmem + 128u + 128u * (uint32_t)(j & 1), dO,
+                       desc_add(dKV, (uint32_t)((j % NSTAGE) * 2 * TILE + TILE)));
+          mma_commit(bar_dp + 8 * (j & 1));
+          mma_commit(bar_vempty + 8 * (j % NSTAGE));
+        }
+        __syncwarp();
+        return true;
+      };
+      bool ok = mbar_wait_warp(bar_q, 0, p.status, &abort_flag);
+      tc_fence_after();
+      ok = ok && issue_s(0) && issue_dp(0) && (n < 2 || issue_dp(1));
       for (int j = 0; ok && j < n; ++j) {
         const uint32_t so = (uint32_t)((j % NSTAGE) * 2 * TILE);
-        const uint32_t son = (uint32_t)(((j + 1) % NSTAGE) * 2 * TILE);
-        const bool more = j + 1 < n;
-        if (!mbar_wait_warp(bar_sfree, j & 1, p.status, &abort_flag)) break;
-        if (more) {
-          if (!mbar_wait_warp(bar_full + 8 * ((j + 1) % NSTAGE), ((j + 1) / NSTAGE) & 1, p.status,
-                              &abort_flag))
-            break;
-          tc_fence_after();
-          if (leader) {
-            issue_scores(tmem, dQ, desc_add(dKV, son));
-            mma_commit(bar_s);
-          }
-          __syncwarp();
+        const uint32_t xo = 128u + 128u * (uint32_t)(j & 1);
+        // S of step j + 1 once step j's S is out of TMEM and K_{j+1} has landed
+        // (the elementwise warps need it first; this step's accumulation MMAs
+        // can follow later)
+        if (j + 1 < n) {
+          if (!mbar_wait_warp(bar_sfree, j & 1, p.status, &abort_flag) || !issue_s(j + 1)) break;
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          if (ok && !mbar_wait_warp(bar_chunk + 8 * c, j & 1, p.status, &abort_flag)) ok = false;
+          if (ok && !mbar_wait_warp(bar_chunk + 8 * (4 * (j & 1) + c), (j >> 1) & 1, p.status, &abort_flag))
+            ok = false;
           if (ok) {
             tc_fence_after();
             if (leader) {
 #pragma unroll
               for (int w = 0; w < 2; ++w) {
                 const uint32_t k0c = (uint32_t)(64 * w + 16 * c);
-                mma_ts(tmem + 256u, tmem + 128u + k0c, desc_add(dKVmn, so + k0c * 128), idesc_acc,
+                mma_ts(tmem + 384u, tmem + xo + k0c, desc_add(dKVmn, so + k0c * 128), idesc_acc,
                        (j == 0 && c == 0 && w == 0) ? 0u : 1u);     // dQ += dX K
               }
             }
@@ -792,14 +830,9 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
           }
         }
         if (!ok) break;
-        if (leader) {
-          mma_commit(bar_empty + 8 * (j % NSTAGE));
-          if (more) {
-            issue_scores(tmem + 128u, dO, desc_add(dKV, son + TILE));
-            mma_commit(bar_dp);
-          }
-        }
+        if (leader) mma_commit(bar_kempty + 8 * (j % NSTAGE));
         __syncwarp();
+        if (j + 2 < n && !issue_dp(j + 2)) break;
       }
       if (leader) mma_commit(bar_final);
       __syncwarp();
@@ -811,7 +844,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const int i = q0 + r;
     const bool valid = i < p.L;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t s_cols = lane_base + 64u * wg, dp_cols = lane_base + 128u + 64u * wg;
+    const uint32_t s_cols = lane_base + 64u * wg;
     const int4 ri = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
     const float temp = (p.temp && valid) ? p.temp[(size_t)b * p.L + i] : 1.f;
     const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
@@ -917,22 +950,24 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         for (int e = 0; e < 64; e += 2) am = fmax3_abs(am, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
         poly = __all_sync(0xFFFFFFFFu, tf.ok && am * fabsf(xf.in) <= kTanhPolyMaxU);
       }
-      if (!mbar_wait_warp(bar_dp, j & 1, p.status, &abort_flag)) {
+      if (!mbar_wait_warp(bar_dp + 8 * (j & 1), (j >> 1) & 1, p.status, &abort_flag)) {
         aborted = true;
         break;
       }
       tc_fence_after();
       const int j0 = k0 + 64 * wg;
+      const uint32_t dp_cols = lane_base + 128u + 128u * (uint32_t)(j & 1) + 64u * wg;
+      const uint32_t chunk_bars = bar_chunk + 32u * (uint32_t)(j & 1);
       if (full) {
         if (poly)
-          dq_step<METHOD, false, true, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
+          dq_step<METHOD, false, true, DT>(sv, dp_cols, rc, ri, j0, xf, tf, chunk_bars, lane, dr, dacc);
         else
-          dq_step<METHOD, false, false, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
+          dq_step<METHOD, false, false, DT>(sv, dp_cols, rc, ri, j0, xf, tf, chunk_bars, lane, dr, dacc);
       } else {
         if (poly)
-          dq_step<METHOD, true, true, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
+          dq_step<METHOD, true, true, DT>(sv, dp_cols, rc, ri, j0, xf, tf, chunk_bars, lane, dr, dacc);
         else
-          dq_step<METHOD, true, false, DT>(sv, dp_cols, rc, ri, j0, xf, tf, bar_chunk, lane, dr, dacc);
+          dq_step<METHOD, true, false, DT>(sv, dp_cols, rc, ri, j0, xf, tf, chunk_bars, lane, dr, dacc);
       }
     }
     bool have = false;
@@ -954,7 +989,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     for (int c = 0; c < 2; ++c) {
       uint32_t v[32];
       if (have) {
-        tmem_ld32(lane_base + 256u + 64 * wg + 32 * c, v);
+        tmem_ld32(lane_base + 384u + 64 * wg + 32 * c, v);
         tmem_wait_ld();
       } else {
 #pragma unroll
