@@ -1,7 +1,7 @@
 """Benchmark: soft-capped attention forward + backward on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl capattn|reference]
-                    [--workload 2] [--no-cpu-baseline]
+                    [--workload 2] [--no-cpu-baseline] [--no-e2e] [--no-per-workload]
 
 A step is one forward (capattn_fwd) and one backward (capattn_bwd) over the
 workload's batch of synthetic seeded inputs.  The default workload is
@@ -13,10 +13,19 @@ oracle from the seeded masks and stored in tests/golden/pair_counts.json).
 
 Timing: inputs resident in HBM; an L2 flush (a 512 MB write) runs before every
 timed step, outside the events; each step is bracketed by CUDA events on the
-stream the kernels run on.  `value` = total FLOPs / summed step time.  `e2e`
-repeats the step through the same C ABI with pinned host buffers: host-to-
-device copies of Q, K, V, dO, the forward, the backward and device-to-host
-copies of O, LSE, dQ, dK, dV all inside the timed region.
+stream the kernels run on; exactly K steps are timed.  `value` = total FLOPs /
+summed step time.  Clock samples (nvidia-smi) cover an untimed soak of about a
+second of the same step right before the timed steps, and the timed steps.
+`e2e` repeats the step through the same C ABI with pinned host buffers:
+host-to-device copies of Q, K, V, dO (+ temperature, segments, bounds), the
+forward, the backward and device-to-host copies of O, LSE, dQ, dK, dV, all
+inside the timed region (dO's copy overlaps the forward and O / LSE leave
+during the backward, on a second stream).
+
+`per_workload` (single process only) measures every workload of the table the
+same way (fwd / bwd split from a pass with every kernel bracketed by events),
+with the fp64 oracle's forward and backward seconds on one (batch, KV head)
+plane of each on the host cores.
 
 Multi-GPU: each rank runs an independent replica of the workload (the path
 shards over (batch, KV head) without any exchange), timing is the max over
@@ -55,6 +64,7 @@ METRIC = "capped-attention fwd+bwd TFLOP/s (mask-aware) and % of GB300 BF16 peak
 # does Q K^T and P V; the dK/dV kernel recomputes S and does dP, dV, dK; the dQ
 # kernel's own product is dQ (its S and dP recomputations are not counted).
 KERNEL_FLOPS_PER_PAIR_D = {"fwd": 4, "dkv": 8, "dq": 2}
+SOAK_SECONDS = 1.0
 
 
 def dist_env():
@@ -84,6 +94,20 @@ def read_peak():
         return float(pk["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
     except Exception:
         return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def config_of(w, idx: int, world: int, dtemp: bool = False) -> dict:
+    """The workload's description, identical in both arms."""
+    N = pairs_of(idx)
+    return {"workload": w.name, "B": w.B, "L": w.L, "Lk": w.key_len, "Hq": w.Hq, "Hkv": w.Hkv,
+            "D": w.D, "causal": w.causal, "window_len": w.window_len,
+            "cap": [w.cap_method, w.cap, w.alpha, w.beta], "z_loss_weight": w.z_loss_weight,
+            "temperature": None if w.temp_range is None else list(w.temp_range),
+            "packed_documents": None if w.doc_len_range is None else list(w.doc_len_range),
+            "ranker_bounds": None if w.ranker_hu_range is None else
+            {"hu": list(w.ranker_hu_range), "candidates": list(w.ranker_cand_range)},
+            "unmasked_pairs": N, "flops_per_step": 14.0 * w.D * N, "dtemp": dtemp,
+            "parallelism": f"replicas x{world}"}
 
 
 class ClockSampler:
@@ -124,6 +148,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
         mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        pw = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         for s in self.samples:
@@ -132,7 +157,8 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(self.samples)}
+                "samples": len(self.samples), "power_w_max": max(pw) if pw else None,
+                "window": f"an untimed soak of ~{SOAK_SECONDS:.0f} s of the same step, then the timed steps"}
 
 
 def kernel_source_hash() -> str:
@@ -161,106 +187,252 @@ def traffic_for(kernel: str, workload: str):
 # capattn arm
 # ---------------------------------------------------------------------------
 
-def run_capattn(args, rank, world, local_rank):
-    from soft_capped_attention_gb300 import capattn as ca
+class Run:
+    """One workload's inputs resident on the device and its forward + backward step."""
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = WORKLOADS[args.workload]
-    inp = make_inputs(w, seed=args.workload)
-    dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    ap = ca.params_from_workload(w)
-    host = {n: torch.from_numpy(inp[n]).to(dtype).contiguous() for n in ("q", "k", "v", "do")}
-    aux = {n: (None if inp[n] is None else torch.from_numpy(inp[n]).contiguous())
-           for n in ("temp", "seg", "bounds")}
-    d = {n: t.to(dev) for n, t in host.items()}
-    da = {n: (None if t is None else t.to(dev)) for n, t in aux.items()}
-    cfg = ca.make_config(ap, w.B, w.L, w.Hq, w.Hkv, w.D, dtype, Lk=w.key_len)
-    ws = ca.new_workspace(cfg, dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    use_dtemp = args.dtemp and aux["temp"] is not None
-    if args.dtemp and not use_dtemp:
-        raise SystemExit("--dtemp needs a workload with a temperature")
+    def __init__(self, idx: int, dev, dtemp: bool = False):
+        from soft_capped_attention_gb300 import capattn as ca
+        self.ca = ca
+        self.idx = idx
+        self.w = w = WORKLOADS[idx]
+        self.inp = inp = make_inputs(w, seed=idx)
+        self.dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.ap = ca.params_from_workload(w)
+        self.host = {n: torch.from_numpy(inp[n]).to(self.dtype).contiguous() for n in ("q", "k", "v", "do")}
+        self.aux = {n: (None if inp[n] is None else torch.from_numpy(inp[n]).contiguous())
+                    for n in ("temp", "seg", "bounds")}
+        self.d = {n: t.to(dev) for n, t in self.host.items()}
+        self.da = {n: (None if t is None else t.to(dev)) for n, t in self.aux.items()}
+        self.cfg = ca.make_config(self.ap, w.B, w.L, w.Hq, w.Hkv, w.D, self.dtype, Lk=w.key_len)
+        self.ws = ca.new_workspace(self.cfg, dev)
+        self.dev = dev
+        self.dtemp = dtemp and self.aux["temp"] is not None
+        if dtemp and not self.dtemp:
+            raise SystemExit("--dtemp needs a workload with a temperature")
+        self.N = pairs_of(idx)
+        self.flops = 14.0 * w.D * self.N
 
-    def bwd(*a, **kw):
-        if use_dtemp:
-            return ca.capattn_bwd_dtemp(*a, **kw)[:3]
-        return ca.capattn_bwd(*a, **kw)[:3]
+    def bwd(self, q, k, v, o, lse, do, temp, seg, bounds):
+        ca = self.ca
+        if self.dtemp:
+            return ca.capattn_bwd_dtemp(q, k, v, o, lse, do, self.ap, temp, seg, bounds,
+                                        workspace=self.ws)[:3]
+        return ca.capattn_bwd(q, k, v, o, lse, do, self.ap, temp, seg, bounds, workspace=self.ws)[:3]
 
-    def step(split=False):
-        o, lse, _, _ = ca.capattn_fwd(d["q"], d["k"], d["v"], ap, da["temp"], da["seg"],
-                                      da["bounds"], workspace=ws)
+    def step(self, stream=None, split=False):
+        d, da = self.d, self.da
+        o, lse, _, _ = self.ca.capattn_fwd(d["q"], d["k"], d["v"], self.ap, da["temp"], da["seg"],
+                                           da["bounds"], workspace=self.ws)
         ev_mid = None
         if split:
             ev_mid = torch.cuda.Event(enable_timing=True)
             ev_mid.record(stream)
-        bwd(d["q"], d["k"], d["v"], o, lse, d["do"], ap, da["temp"], da["seg"],
-                       da["bounds"], workspace=ws)
+        self.bwd(d["q"], d["k"], d["v"], o, lse, d["do"], da["temp"], da["seg"], da["bounds"])
         return ev_mid
+
+
+def breakdown_pass(run: Run, steps: int, flush, stream):
+    """Every library kernel bracketed by events and a mark between forward and
+    backward: per-kernel milliseconds and launches, and the fwd / bwd split."""
+    ca = run.ca
+    ca.capattn_profile_select(None)
+    ca.capattn_profile_enable(True)
+    ca.capattn_profile_read(reset=True)
+    split = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e1 = run.step(stream, split=True)
+        e2.record(stream)
+        split.append((e0, e1, e2))
+    torch.cuda.synchronize()
+    prof = ca.capattn_profile_read(reset=True)
+    ca.capattn_profile_enable(False)
+    fw = sum(a.elapsed_time(b) for a, b, _ in split)
+    bw = sum(b.elapsed_time(c) for _, b, c in split)
+    kern_ms = {k: v[0] for k, v in prof.items() if v[1] > 0}
+    launches = {k: v[1] for k, v in prof.items()}
+    dom = max(KERNEL_FLOPS_PER_PAIR_D, key=lambda k: kern_ms.get(k, 0.0))
+    return fw, bw, kern_ms, launches, dom
+
+
+def timed_steps(run: Run, steps: int, flush, stream):
+    """Exactly `steps` steps, each bracketed by events; returns summed milliseconds."""
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run.step(stream)
+        e2.record(stream)
+        times.append((e0, e2))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in times)
+
+
+def check_status(run: Run):
+    st, bits = run.ca.capattn_device_status(run.ws)
+    if st != 0:
+        raise RuntimeError(f"{run.w.name}: device status {st} (bits {bits})")
+
+
+def e2e_measure(run: Run, args, world, dev, stream, flush):
+    """The step from pinned host buffers: inputs copied in and results copied out
+    inside the timed region (dO's copy overlaps the forward on a second
+    stream; O and LSE leave during the backward)."""
+    ca, w = run.ca, run.w
+    ph = {n: t.pin_memory() for n, t in run.host.items()}
+    pa = {n: (None if t is None else t.pin_memory()) for n, t in run.aux.items()}
+    out_h = {"o": torch.empty_like(ph["q"]).pin_memory(),
+             "lse": torch.empty(w.B, w.Hq, w.L, dtype=torch.float32).pin_memory(),
+             "dq": torch.empty_like(ph["q"]).pin_memory(),
+             "dk": torch.empty_like(ph["k"]).pin_memory(),
+             "dv": torch.empty_like(ph["v"]).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in ph.values()) + \
+        sum(t.numel() * t.element_size() for t in pa.values() if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+    dbuf = {n: torch.empty_like(t, device=dev) for n, t in ph.items()}
+    dabuf = {n: (None if t is None else torch.empty_like(t, device=dev)) for n, t in pa.items()}
+    side = torch.cuda.Stream(dev)
+
+    def e2e_step():
+        start = torch.cuda.Event()
+        start.record(stream)
+        side.wait_event(start)
+        with torch.cuda.stream(side):
+            dbuf["do"].copy_(ph["do"], non_blocking=True)
+        ev_do = torch.cuda.Event()
+        ev_do.record(side)
+        for n in ("q", "k", "v"):
+            dbuf[n].copy_(ph[n], non_blocking=True)
+        for n in pa:
+            if pa[n] is not None:
+                dabuf[n].copy_(pa[n], non_blocking=True)
+        o, lse, _, _ = ca.capattn_fwd(dbuf["q"], dbuf["k"], dbuf["v"], run.ap, dabuf["temp"],
+                                      dabuf["seg"], dabuf["bounds"], workspace=run.ws)
+        ev_fwd = torch.cuda.Event()
+        ev_fwd.record(stream)
+        side.wait_event(ev_fwd)
+        with torch.cuda.stream(side):
+            out_h["o"].copy_(o, non_blocking=True)
+            out_h["lse"].copy_(lse, non_blocking=True)
+        stream.wait_event(ev_do)
+        dq, dk, dv = run.bwd(dbuf["q"], dbuf["k"], dbuf["v"], o, lse, dbuf["do"], dabuf["temp"],
+                             dabuf["seg"], dabuf["bounds"])
+        out_h["dq"].copy_(dq, non_blocking=True)
+        out_h["dk"].copy_(dk, non_blocking=True)
+        out_h["dv"].copy_(dv, non_blocking=True)
+        ev_side = torch.cuda.Event()
+        ev_side.record(side)
+        stream.wait_event(ev_side)
+        o.record_stream(side)
+        lse.record_stream(side)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    etot = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b_ = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b_.record(stream)
+        b_.synchronize()
+        etot += a.elapsed_time(b_)
+    if world > 1:
+        etot = max_over_ranks([etot], dev)[0]
+    check_status(run)
+    return {"value": round(run.flops * args.steps * world / (etot * 1e-3) / 1e12, 3),
+            "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(etot / args.steps, 4),
+            "overlap": "dO's copy overlaps the forward and O / LSE leave during the backward (second stream)"}
+
+
+def per_workload_measure(args, dev, stream, flush, headline: dict):
+    """Every workload of the table, the headline's numbers reused."""
+    peak, _ = read_peak()
+    out = {}
+    for idx in sorted(WORKLOADS):
+        if idx == args.workload:
+            out[WORKLOADS[idx].name] = headline
+            continue
+        run = Run(idx, dev)
+        steps = max(3, args.per_workload_steps)
+        for _ in range(3):
+            flush.zero_()
+            run.step(stream)
+        torch.cuda.synchronize()
+        check_status(run)
+        fw, bw, kern_ms, launches, dom = breakdown_pass(run, steps, flush, stream)
+        tot = timed_steps(run, steps, flush, stream)
+        check_status(run)
+        D, N = run.w.D, run.N
+        value = run.flops * steps / (tot * 1e-3) / 1e12
+        out[run.w.name] = {
+            "workload": idx, "dtype": run.w.dtype, "unmasked_pairs": N, "steps": steps,
+            "fwd_bwd_tflops": round(value, 3), "frac_of_peak": round(value / peak, 4),
+            "fwd_tflops": round(4.0 * D * N * steps / (fw * 1e-3) / 1e12, 3),
+            "bwd_tflops": round(10.0 * D * N * steps / (bw * 1e-3) / 1e12, 3),
+            "ms_per_step": round(tot / steps, 4), "dominant_kernel": dom,
+            "kernel_ms_per_launch": {k: round(kern_ms[k] / max(launches[k], 1), 4) for k in kern_ms}}
+        del run
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_capattn(args, rank, world, local_rank):
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    run = Run(args.workload, dev, dtemp=args.dtemp)
+    ca, w = run.ca, run.w
+    use_dtemp = run.dtemp
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        run.step(stream)
     torch.cuda.synchronize()
-    st, bits = ca.capattn_device_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status {st} (bits {bits}) after warm-up")
+    check_status(run)
 
-    N = pairs_of(args.workload)
-    D = w.D
-    flops_step = 14.0 * D * N
+    D, N = w.D, run.N
+    flops_step = run.flops
 
     # Breakdown pass (not the headline): every kernel bracketed by events and a
     # mark between forward and backward.  Each recorded event costs the stream a
     # few microseconds, so the headline run below records only the events of the
     # kernel its roofline names.
-    ca.capattn_profile_select(None)
-    ca.capattn_profile_enable(True)
-    ca.capattn_profile_read(reset=True)
-    split = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e2 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        e1 = step(split=True)
-        e2.record(stream)
-        split.append((e0, e1, e2))
-    torch.cuda.synchronize()
-    prof_all = ca.capattn_profile_read(reset=True)
-    fw = sum(a.elapsed_time(b) for a, b, _ in split)
-    bw = sum(b.elapsed_time(c) for _, b, c in split)
-    kern_ms_all = {k: v[0] for k, v in prof_all.items() if v[1] > 0}
-    launches_all = {k: v[1] for k, v in prof_all.items()}
-    dom = max(KERNEL_FLOPS_PER_PAIR_D, key=lambda k: kern_ms_all.get(k, 0.0))
+    fw, bw, kern_ms_all, launches_all, dom = breakdown_pass(run, args.steps, flush, stream)
     total_kernel_ms = sum(kern_ms_all.values())
 
-    # Headline run: step events plus the events of the roofline kernel only.
+    # Headline run: step events plus the events of the roofline kernel only,
+    # after an untimed soak of the same step under the clock sampler.
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ca.capattn_profile_select([dom])
-    ca.capattn_profile_read(reset=True)
-    times_total = []
+    step_ms_est = (fw + bw) / max(args.steps, 1)
+    soak = max(1, int(SOAK_SECONDS / max(step_ms_est * 1e-3 + 1e-4, 1e-6)))
     with ClockSampler(local_rank) as clk:
-        time.sleep(0.05)
-        for _ in range(args.steps):
+        for _ in range(soak):
             flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e2 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            step()
-            e2.record(stream)
-            times_total.append((e0, e2))
-        torch.cuda.synchronize()
-        time.sleep(0.05)
-    prof = ca.capattn_profile_read(reset=True)
-    ca.capattn_profile_enable(False)
-    ca.capattn_profile_select(None)
+            run.step(stream)
+        ca.capattn_profile_select([dom])
+        ca.capattn_profile_enable(True)
+        ca.capattn_profile_read(reset=True)
+        tot = timed_steps(run, args.steps, flush, stream)
+        prof = ca.capattn_profile_read(reset=True)
+        ca.capattn_profile_enable(False)
+        ca.capattn_profile_select(None)
+    check_status(run)
     if world > 1:
         torch.distributed.barrier()
-    tot = sum(e0.elapsed_time(e2) for e0, e2 in times_total)
     ms_step = tot / args.steps
     if world > 1:
         tot, fw, bw = max_over_ranks([tot, fw, bw], dev)
@@ -287,83 +459,38 @@ def run_capattn(args, rank, world, local_rank):
                 "breakdown": "kernel_ms_per_launch / kernel_share from a separate pass with every "
                              "kernel bracketed by events"}
 
-    # e2e through the C ABI with pinned host buffers
-    e2e = None
-    if not args.no_e2e:
-        ph = {n: t.pin_memory() for n, t in host.items()}
-        pa = {n: (None if t is None else t.pin_memory()) for n, t in aux.items()}
-        out_h = {"o": torch.empty_like(ph["q"]).pin_memory(),
-                 "lse": torch.empty(w.B, w.Hq, w.L, dtype=torch.float32).pin_memory(),
-                 "dq": torch.empty_like(ph["q"]).pin_memory(),
-                 "dk": torch.empty_like(ph["k"]).pin_memory(),
-                 "dv": torch.empty_like(ph["v"]).pin_memory()}
-        h2d = sum(t.numel() * t.element_size() for t in ph.values()) + \
-            sum(t.numel() * t.element_size() for t in pa.values() if t is not None)
-        d2h = sum(t.numel() * t.element_size() for t in out_h.values())
-        dbuf = {n: torch.empty_like(t, device=dev) for n, t in ph.items()}
-        dabuf = {n: (None if t is None else torch.empty_like(t, device=dev)) for n, t in pa.items()}
+    e2e = None if args.no_e2e else e2e_measure(run, args, world, dev, stream, flush)
 
-        def e2e_step():
-            for n in ph:
-                dbuf[n].copy_(ph[n], non_blocking=True)
-            for n in pa:
-                if pa[n] is not None:
-                    dabuf[n].copy_(pa[n], non_blocking=True)
-            o, lse, _, _ = ca.capattn_fwd(dbuf["q"], dbuf["k"], dbuf["v"], ap, dabuf["temp"],
-                                          dabuf["seg"], dabuf["bounds"], workspace=ws)
-            dq, dk, dv = bwd(dbuf["q"], dbuf["k"], dbuf["v"], o, lse, dbuf["do"], ap,
-                                           dabuf["temp"], dabuf["seg"], dabuf["bounds"],
-                                           workspace=ws)
-            out_h["o"].copy_(o, non_blocking=True)
-            out_h["lse"].copy_(lse, non_blocking=True)
-            out_h["dq"].copy_(dq, non_blocking=True)
-            out_h["dk"].copy_(dk, non_blocking=True)
-            out_h["dv"].copy_(dv, non_blocking=True)
-
-        for _ in range(max(args.warmup, 3)):
-            e2e_step()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        etot = 0.0
-        for _ in range(args.steps):
-            flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b_ = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            e2e_step()
-            b_.record(stream)
-            b_.synchronize()
-            etot += a.elapsed_time(b_)
-        if world > 1:
-            t = torch.tensor([etot], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            etot = float(t.item())
-        e2e = {"value": round(flops_step * args.steps * world / (etot * 1e-3) / 1e12, 3),
-               "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(etot / args.steps, 4)}
+    headline = {"workload": args.workload, "dtype": w.dtype, "unmasked_pairs": N,
+                "steps": args.steps, "fwd_bwd_tflops": round(value / world, 3),
+                "frac_of_peak": round(value / world / peak, 4), "fwd_tflops": round(fwd_tf / world, 3),
+                "bwd_tflops": round(bwd_tf / world, 3), "ms_per_step": round(ms_step, 4),
+                "dominant_kernel": dom, "kernel_ms_per_launch": roofline["kernel_ms_per_launch"]}
+    per_wl = None
+    if world == 1 and not args.no_per_workload:
+        del run
+        torch.cuda.empty_cache()
+        per_wl = per_workload_measure(args, dev, stream, flush, headline)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.workload, args.cpu_seconds)
+        cpu = cpu_baseline(WORKLOADS[args.workload], args.workload, args.cpu_seconds)
+        if per_wl is not None:
+            for idx in sorted(WORKLOADS):
+                per_wl[WORKLOADS[idx].name]["cpu_oracle"] = oracle_fwd_bwd_plane(idx)
 
     clocks = clk.summary()
     line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded normal Q, K, V, dO; seeded masks)",
-            "config": {"workload": w.name, "B": w.B, "L": w.L, "Lk": w.key_len, "Hq": w.Hq, "Hkv": w.Hkv,
-                       "D": w.D, "causal": w.causal, "window_len": w.window_len,
-                       "cap": [w.cap_method, w.cap, w.alpha, w.beta],
-                       "z_loss_weight": w.z_loss_weight, "unmasked_pairs": N,
-                       "dtemp": use_dtemp,
-                       "flops_per_step": flops_step, "l2": "flushed before every timed step",
-                       "parallelism": f"replicas x{world}"},
+            "config": config_of(w, args.workload, world, use_dtemp),
+            "l2": "flushed before every timed step",
             "fwd_tflops": round(fwd_tf, 3), "bwd_tflops": round(bwd_tf, 3),
             "fwd_bwd_split": "from the breakdown pass (events around every kernel)",
             "frac_of_peak": round(value / peak, 4), "peak_tflops": peak, "peak_source": peak_src,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-            "clocks": clocks}
+            "clocks": clocks, "per_workload": per_wl}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -375,14 +502,26 @@ def run_capattn(args, rank, world, local_rank):
 _ORACLE_INPUTS = {}
 
 
+def _oracle_inputs(w, idx):
+    if idx not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS.clear()
+        _ORACLE_INPUTS[idx] = make_inputs(w, seed=idx)
+    return _ORACLE_INPUTS[idx]
+
+
+def _plane_pairs(w, inp, cfg, b):
+    from oracle import capattn_oracle as orc
+    return orc.pair_count(w.L, cfg, None if inp["seg"] is None else inp["seg"][b:b + 1],
+                          None if inp["bounds"] is None else inp["bounds"][b:b + 1], B=1,
+                          Lk=w.key_len)
+
+
 def oracle_sample(w, idx, seconds: float, start: int = 0):
     """Runs the oracle forward + backward on whole (batch, KV head) planes of the
     workload, starting at plane `start`, until `seconds` elapse (at least one
     plane); returns (FLOPs counted mask-aware, seconds, planes)."""
     from oracle import capattn_oracle as orc
-    if idx not in _ORACLE_INPUTS:
-        _ORACLE_INPUTS[idx] = make_inputs(w, seed=idx)
-    inp = _ORACLE_INPUTS[idx]
+    inp = _oracle_inputs(w, idx)
     cfg = orc.config_from_workload(w)
     flops = 0.0
     t0 = time.perf_counter()
@@ -390,17 +529,37 @@ def oracle_sample(w, idx, seconds: float, start: int = 0):
     nplanes = w.B * w.Hkv
     for pidx in range(start, start + nplanes):
         b, g = divmod(pidx % nplanes, w.Hkv)
-        if True:
-            orc.backward_kv_head(inp["q"], inp["k"], inp["v"], inp["temp"], inp["seg"],
-                                 inp["bounds"], inp["do"], cfg, b, g)
-            n_head = orc.pair_count(w.L, cfg, None if inp["seg"] is None else inp["seg"][b:b + 1],
-                                    None if inp["bounds"] is None else inp["bounds"][b:b + 1], B=1,
-                                    Lk=w.key_len)
-            flops += 14.0 * w.D * n_head * w.G
-            planes += 1
-            if time.perf_counter() - t0 >= seconds:
-                return flops, time.perf_counter() - t0, planes
+        orc.backward_kv_head(inp["q"], inp["k"], inp["v"], inp["temp"], inp["seg"],
+                             inp["bounds"], inp["do"], cfg, b, g)
+        flops += 14.0 * w.D * _plane_pairs(w, inp, cfg, b) * w.G
+        planes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
     return flops, time.perf_counter() - t0, planes
+
+
+def oracle_fwd_bwd_plane(idx):
+    """The oracle's forward and backward seconds, timed apart, on plane (b=0,
+    KV head 0) of workload idx (its G query heads), and the TFLOP/s they give."""
+    from oracle import capattn_oracle as orc
+    w = WORKLOADS[idx]
+    inp = _oracle_inputs(w, idx)
+    cfg = orc.config_from_workload(w)
+    G = w.G
+    sl = lambda x: None if x is None else x[0:1]
+    q, do = inp["q"][0:1, :, 0:G], inp["do"][0:1, :, 0:G]
+    k, v = inp["k"][0:1, :, 0:1], inp["v"][0:1, :, 0:1]
+    t0 = time.perf_counter()
+    O, LSE, _, _ = orc.forward(q, k, v, sl(inp["temp"]), sl(inp["seg"]), sl(inp["bounds"]), cfg)
+    t1 = time.perf_counter()
+    orc.backward(q, k, v, sl(inp["temp"]), sl(inp["seg"]), sl(inp["bounds"]), O, LSE, do, cfg)
+    t2 = time.perf_counter()
+    n = _plane_pairs(w, inp, cfg, 0) * G
+    return {"fwd_s": round(t1 - t0, 4), "bwd_s": round(t2 - t1, 4),
+            "fwd_tflops": round(4.0 * w.D * n / (t1 - t0) / 1e12, 6),
+            "bwd_tflops": round(10.0 * w.D * n / (t2 - t1) / 1e12, 6),
+            "cores": len(os.sched_getaffinity(0)),
+            "sample": f"plane (batch 0, KV head 0) with its {G} query head(s), fp64"}
 
 
 def cpu_baseline(w, idx, seconds):
@@ -432,7 +591,7 @@ def run_reference(args, rank, world):
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded normal Q, K, V, dO; seeded masks)", "impl": "reference",
-            "config": {"workload": w.name, "B": w.B, "L": w.L, "Lk": w.key_len, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D},
+            "config": config_of(w, args.workload, world, args.dtemp and w.temp_range is not None),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle",
                              "sample": f"each step: one (batch, KV head) plane of {w.name}, "
@@ -452,6 +611,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--per-workload-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--dtemp", action="store_true",
                     help="also compute the temperature gradient (workloads with a temperature)")
