@@ -114,7 +114,10 @@ capattn_status capattn_validate_config(const capattn_config* cfg);
 
 /*
  * Bytes of device workspace needed by capattn_fwd (pass CAPATTN_PASS_FWD) or
- * capattn_bwd (CAPATTN_PASS_BWD) for this configuration; 0 if cfg is invalid.
+ * capattn_bwd / capattn_bwd_dtemp / capattn_bwd_ex (CAPATTN_PASS_BWD) for this
+ * configuration; 0 if cfg is invalid.  The backward needs more: it also holds
+ * the per-(head, row) partial sums of the temperature gradient (8 bytes per
+ * (b, query head, row)).  A workspace sized for the backward serves both.
  * The workspace must be 256-byte aligned.  Its first word is the device status.
  */
 size_t capattn_workspace_bytes(const capattn_config* cfg, int pass);
@@ -164,9 +167,10 @@ capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void*
  * keys j of dT[b,h,i,j] * c[b,h,i,j], with dT = P (dP - delta + z LSE) the
  * gradient of the tempered logit (0 for masked pairs).
  * temp and dtemp [B,L] float32 (device) are required (CAPATTN_ERR_INVALID_ARG
- * if either is null); dtemp is overwritten (zeroed on `stream`, then the
- * per-head sums are added with float32 atomics, so their order, and the last
- * bits, vary from run to run).  Everything else is as in capattn_bwd.
+ * if either is null); dtemp is overwritten.  The dQ kernels leave per-(head,
+ * row) partial sums in the workspace and a final pass adds them over the heads
+ * in a fixed order, so dtemp is the same bit for bit on every run.  Everything
+ * else is as in capattn_bwd.
  */
 capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const void* k,
                                  const void* v, const float* temp, const int32_t* seg,

@@ -976,10 +976,11 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       tc_fence_after();
     }
     if constexpr (DT) {
-      // this warpgroup's part of sum over the row's keys of dT c (all heads add in)
+      // this warpgroup's part of sum over the row's keys of dT c, one slot per
+      // (head, row, warpgroup); the slots are added in a fixed order afterwards
       float a0, a1;
       f2_split(dacc, a0, a1);
-      if (valid && !aborted) atomicAdd(p.dtemp + (size_t)b * p.L + i, a0 + a1);
+      if (valid) p.dtemp_part[2 * rr + wg] = aborted ? 0.f : a0 + a1;
     }
     // Warpgroup wg writes dQ columns [64 wg, 64 wg + 64) through slab wg of
     // the Q tile's shared memory (free once every MMA has completed) and one

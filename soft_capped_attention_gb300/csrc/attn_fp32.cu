@@ -210,10 +210,14 @@ __global__ void __launch_bounds__(NT) dq_fp32_kernel(Params p) {
     }
   }
   if (p.dtemp) {
-    // the four threads of a row add their columns; every query head adds in
+    // the four threads of a row add their columns; one slot pair per (head,
+    // row), added over the heads in a fixed order afterwards
     dta += __shfl_xor_sync(0xFFFFFFFFu, dta, 1);
     dta += __shfl_xor_sync(0xFFFFFFFFu, dta, 2);
-    if (valid && ln.sub == 0) atomicAdd(p.dtemp + (size_t)b * p.L + i, dta);
+    if (valid && ln.sub == 0) {
+      p.dtemp_part[2 * r] = dta;
+      p.dtemp_part[2 * r + 1] = 0.f;
+    }
   }
   if (valid) {
     float* dq = static_cast<float*>(p.dq) + ((size_t)(b * p.L + i) * p.Hq + h) * D;

@@ -27,6 +27,8 @@ WorkspaceLayout workspace_layout(const capattn_config& c, int bq, int bk) {
   w.kmap_off = align256(w.qmap_off + sizeof(uint32_t) * (size_t)c.B * nq * wk);
   w.qfull_off = align256(w.kmap_off + sizeof(uint32_t) * (size_t)c.B * nk * wq);
   w.total = align256(w.qfull_off + sizeof(int2) * (size_t)c.B * nq);
+  w.dtemp_part_off = w.total;
+  w.total_bwd = align256(w.dtemp_part_off + sizeof(float) * 2 * (size_t)c.B * c.Hq * c.L);
   return w;
 }
 
@@ -103,11 +105,13 @@ static void fill_params(Params& p, const capattn_config& c, void* ws) {
   p.qmap = reinterpret_cast<uint32_t*>(base + w.qmap_off);
   p.kmap = reinterpret_cast<uint32_t*>(base + w.kmap_off);
   p.qfull = reinterpret_cast<int2*>(base + w.qfull_off);
+  p.dtemp_part = reinterpret_cast<float*>(base + w.dtemp_part_off);  // backward workspace only
 }
 
-static capattn_status check_ws(const capattn_config& c, void* ws, size_t bytes) {
+static capattn_status check_ws(const capattn_config& c, void* ws, size_t bytes, int pass) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return CAPATTN_ERR_WORKSPACE;
-  if (bytes < workspace_layout(c, tile_q(c), tile_kv(c)).total) return CAPATTN_ERR_WORKSPACE;
+  const WorkspaceLayout w = workspace_layout(c, tile_q(c), tile_kv(c));
+  if (bytes < (pass == CAPATTN_PASS_BWD ? w.total_bwd : w.total)) return CAPATTN_ERR_WORKSPACE;
   return CAPATTN_OK;
 }
 
@@ -160,19 +164,14 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, delta, temp, seg, bounds, dtemp, dlse};
   for (const void* ptr : ptrs)
     if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
-  st = check_ws(*cfg, workspace, workspace_bytes);
+  st = check_ws(*cfg, workspace, workspace_bytes, CAPATTN_PASS_BWD);
   if (st != CAPATTN_OK) return st;
   Params p;
   fill_params(p, *cfg, workspace);
   p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
   p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
   p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta; p.dtemp = dtemp; p.dlse = dlse;
-  cudaError_t e = cudaSuccess;
-  if (dtemp) {
-    e = cudaMemsetAsync(dtemp, 0, (size_t)cfg->B * cfg->L * sizeof(float), stream);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
-  e = launch_prepass(p, true, stream);
+  cudaError_t e = launch_prepass(p, true, stream);
   if (e != cudaSuccess) return cuda_status(e);
   // bf16: the dQ kernel computes delta itself; fp32: a separate pass
   if (cfg->dtype != CAPATTN_BF16) {
@@ -180,6 +179,10 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
     if (e != cudaSuccess) return cuda_status(e);
   }
   e = (cfg->dtype == CAPATTN_BF16) ? launch_bwd_bf16(p, stream) : launch_bwd_fp32(p, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  // dtemp: the dQ kernels leave per-(head, row) partial sums; they are added in
+  // a fixed order, so the result does not depend on scheduling
+  if (dtemp) e = launch_dtemp_reduce(p, stream);
   return cuda_status(e);
 }
 
@@ -204,7 +207,8 @@ capattn_status capattn_validate_config(const capattn_config* cfg) { return valid
 size_t capattn_workspace_bytes(const capattn_config* cfg, int pass) {
   if (validate(cfg) != CAPATTN_OK) return 0;
   if (pass != CAPATTN_PASS_FWD && pass != CAPATTN_PASS_BWD) return 0;
-  return workspace_layout(*cfg, tile_q(*cfg), tile_kv(*cfg)).total;
+  const WorkspaceLayout w = workspace_layout(*cfg, tile_q(*cfg), tile_kv(*cfg));
+  return pass == CAPATTN_PASS_BWD ? w.total_bwd : w.total;
 }
 
 capattn_status capattn_tile_sizes(const capattn_config* cfg, int32_t* block_q, int32_t* block_kv) {
@@ -227,7 +231,7 @@ capattn_status capattn_fwd(const capattn_config* cfg, const void* q, const void*
   const void* ptrs[] = {q, k, v, o, lse, temp, seg, bounds, m, l};
   for (const void* ptr : ptrs)
     if (ptr && !aligned16(ptr)) return CAPATTN_ERR_INVALID_ARG;
-  st = check_ws(*cfg, workspace, workspace_bytes);
+  st = check_ws(*cfg, workspace, workspace_bytes, CAPATTN_PASS_FWD);
   if (st != CAPATTN_OK) return st;
   Params p;
   fill_params(p, *cfg, workspace);
@@ -353,7 +357,7 @@ capattn_status capattn_visit_map_device(const capattn_config* cfg, const int32_t
     return CAPATTN_ERR_INVALID_ARG;
   st = check_masks(*cfg, seg, bounds);
   if (st != CAPATTN_OK) return st;
-  st = check_ws(*cfg, workspace, workspace_bytes);
+  st = check_ws(*cfg, workspace, workspace_bytes, CAPATTN_PASS_FWD);
   if (st != CAPATTN_OK) return st;
   Params p;
   fill_params(p, *cfg, workspace);

@@ -42,7 +42,8 @@ struct Params {
   void* dk;
   void* dv;
   float* delta;
-  float* dtemp;           // [B, L] gradient of the temperature (accumulated), or null
+  float* dtemp;           // [B, L] gradient of the temperature, or null
+  float* dtemp_part;      // [B, Hq, L, 2] per-head partial sums of dtemp (backward workspace)
   const float* dlse;      // [B, Hq, L] upstream gradient of the LSE, or null
   // workspace pieces
   uint32_t* status;
@@ -60,8 +61,10 @@ struct Params {
   CapConsts cap;
 };
 
+// `total` is what the forward needs; the backward also holds the per-head
+// partial sums of the temperature gradient after it (`total_bwd`).
 struct WorkspaceLayout {
-  size_t status_off, rowinfo_off, qmap_off, kmap_off, qfull_off, total;
+  size_t status_off, rowinfo_off, qmap_off, kmap_off, qfull_off, total, dtemp_part_off, total_bwd;
 };
 
 WorkspaceLayout workspace_layout(const capattn_config& c, int block_q, int block_kv);
@@ -106,6 +109,7 @@ cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_bf16(const Params& p, cudaStream_t s);
+cudaError_t launch_dtemp_reduce(const Params& p, cudaStream_t s);
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, int ctas, cudaStream_t s);
 cudaError_t launch_ranker_bounds(const int32_t* seg, int B, int L, int32_t history_id,
                                  int32_t candidate_id, int32_t* bounds, uint32_t* status,

@@ -153,6 +153,32 @@ cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ dtemp
+// dtemp[b, i] = sum over query heads h of the two partial sums the dQ kernels
+// left for (b, h, i), always added in the order h = 0, 1, ... (deterministic).
+__global__ void dtemp_reduce_kernel(Params p) {
+  pdl_trigger();
+  pdl_wait();
+  const long long bi = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (bi >= (long long)p.B * p.L) return;
+  const int b = (int)(bi / p.L), i = (int)(bi % p.L);
+  const float2* part = reinterpret_cast<const float2*>(p.dtemp_part);
+  float acc = 0.f;
+  for (int h = 0; h < p.Hq; ++h) {
+    const float2 v = part[((size_t)b * p.Hq + h) * p.L + i];
+    acc += v.x + v.y;
+  }
+  p.dtemp[bi] = acc;
+}
+
+cudaError_t launch_dtemp_reduce(const Params& p, cudaStream_t s) {
+  const long long n = (long long)p.B * p.L;
+  const unsigned grid = (unsigned)((n + 255) / 256);
+  const cudaError_t e = launch_pdl(dtemp_reduce_kernel, dim3(grid), dim3(256), 0, s, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // One CTA per batch row: the hull [first, last + 1) of the positions carrying
 // each of the two ids (empty (0, 0) when absent), and whether each run fills its
 // hull (count == length).

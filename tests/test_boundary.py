@@ -97,6 +97,19 @@ def test_compute_calls_reject_bad_arguments_before_launch(lib):
     assert st == 1  # null dq
 
 
+def test_backward_workspace_holds_the_temperature_partials(lib):
+    c = _cfg(B=3, L=300, Hq=4, Hkv=2)
+    fwd = lib.capattn_workspace_bytes(ctypes.byref(c), 0)
+    bwd = lib.capattn_workspace_bytes(ctypes.byref(c), 1)
+    extra = 8 * 3 * 4 * 300  # two float partial sums per (b, query head, row)
+    assert bwd == fwd + ((extra + 255) // 256) * 256
+    # a forward-sized workspace is refused by the backward before any launch
+    p16 = ctypes.c_void_p(16)
+    st = lib.capattn_bwd(ctypes.byref(c), p16, p16, p16, None, None, None, *([p16] * 7),
+                         ctypes.c_void_p(256), fwd, None)
+    assert st == 5
+
+
 def test_bounded_wait_check_rejects_bad_arguments(lib):
     # checked on the host before any CUDA call
     assert lib.capattn_check_bounded_wait(None, 1000, None) == 5

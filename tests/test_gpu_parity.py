@@ -332,6 +332,26 @@ def test_dtemp_bf16_matches_oracle(case):
     assert rel_fro(got["dQ"], plain["dQ"]) < 1e-3
 
 
+@pytest.mark.parametrize("dname", ["bf16", "fp32"])
+def test_dtemp_is_deterministic(dname):
+    # per-(head, row) partial sums added in a fixed order: identical bits on
+    # every run (and dQ / dK / dV, which use no atomics, too)
+    dtype = torch.bfloat16 if dname == "bf16" else torch.float32
+    D = 128 if dname == "bf16" else 64
+    inp = make_case(2, 700, 8, 2, D, dtype, "causal", True, seed=5)
+    ap = params("tanh", "causal", 0.01)
+    q, k, v, do = (to_dev(inp[n], dtype) for n in ("q", "k", "v", "do"))
+    temp = to_dev(inp["temp"])
+    cfg = ca.make_config(ap, 2, 700, 8, 2, D, dtype)
+    ws = ca.new_workspace(cfg, q.device)
+    o, lse, _, _ = ca.capattn_fwd(q, k, v, ap, temp, workspace=ws)
+    runs = [ca.capattn_bwd_dtemp(q, k, v, o, lse, do, ap, temp, workspace=ws) for _ in range(4)]
+    assert ca.capattn_device_status(ws) == (0, 0)
+    for r in runs[1:]:
+        for a, b in zip(r, runs[0]):
+            assert torch.equal(a, b)
+
+
 def test_dtemp_fp32_matches_oracle():
     inp = make_case(1, 130, 2, 1, 64, torch.float32, "causal", True, seed=77)
     ap = params("tanh", "causal", 0.02)
