@@ -191,17 +191,21 @@ def _config(q, k, ap: AttnParams) -> CapattnConfig:
 
 
 def capattn_fwd(q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None, workspace=None,
-                want_ml=False, stream=None):
+                want_ml=False, stream=None, out=None):
     """Forward.  q [B,L,Hq,D], k/v [B,Lk,Hkv,D] (bf16 or fp32, contiguous, on the GPU).
-    Returns (o, lse, m, l); m and l are None unless want_ml."""
+    Returns (o, lse, m, l); m and l are None unless want_ml.  out: optional
+    preallocated (o, lse, m, l) to write into (m, l may be None)."""
     cfg = _config(q, k, ap)
     B, L, Hq = cfg.B, cfg.L, cfg.Hq
     if workspace is None:
         workspace = new_workspace(cfg, q.device)
-    o = torch.empty_like(q)
-    lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
-    m = torch.empty_like(lse) if want_ml else None
-    l = torch.empty_like(lse) if want_ml else None
+    if out is not None:
+        o, lse, m, l = out
+    else:
+        o = torch.empty_like(q)
+        lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+        m = torch.empty_like(lse) if want_ml else None
+        l = torch.empty_like(lse) if want_ml else None
     st = lib().capattn_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(temp), _ptr(seg),
                            _ptr(bounds), _ptr(o), _ptr(lse), _ptr(m), _ptr(l), _ptr(workspace),
                            workspace.numel(), _stream(stream))
@@ -210,16 +214,20 @@ def capattn_fwd(q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None, works
 
 
 def capattn_bwd(q, k, v, o, lse, do, ap: AttnParams, temp=None, seg=None, bounds=None,
-                workspace=None, stream=None):
-    """Backward.  Returns (dq, dk, dv, delta)."""
+                workspace=None, stream=None, out=None):
+    """Backward.  Returns (dq, dk, dv, delta).  out: optional preallocated
+    (dq, dk, dv, delta) to write into."""
     cfg = _config(q, k, ap)
     B, L, Hq = cfg.B, cfg.L, cfg.Hq
     if workspace is None:
         workspace = new_workspace(cfg, q.device)
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
-    delta = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
+    if out is not None:
+        dq, dk, dv, delta = out
+    else:
+        dq = torch.empty_like(q)
+        dk = torch.empty_like(k)
+        dv = torch.empty_like(v)
+        delta = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device)
     st = lib().capattn_bwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(temp), _ptr(seg),
                            _ptr(bounds), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
                            _ptr(dv), _ptr(delta), _ptr(workspace), workspace.numel(),

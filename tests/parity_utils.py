@@ -26,16 +26,61 @@ def to_dev(x, dtype=None):
     return t.cuda()
 
 
+# Guard bands (a stand-in for a memory checker): every output buffer sits
+# between two 4 KB bands of a sentinel byte, and one band follows the
+# workspace; a write outside a buffer shows up as a changed band.
+GUARD_BYTES = 4096
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """A tensor of the given shape and dtype inside a byte buffer with guard bands."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        esz = torch.tensor([], dtype=dtype).element_size()
+        n = int(np.prod(shape)) * esz
+        self.buf = torch.full((GUARD_BYTES + n + GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8,
+                              device=device)
+        self.n = n
+        self.tensor = self.buf[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+
+    def intact(self) -> bool:
+        head = self.buf[:GUARD_BYTES]
+        tail = self.buf[GUARD_BYTES + self.n:]
+        return bool((head == GUARD_BYTE).all()) and bool((tail == GUARD_BYTE).all())
+
+
 def run_gpu(inp, ap, dtype, want_ml=False):
+    """Forward and backward through the binding with every output guarded; the
+    inputs must come back unchanged and no guard band may be touched."""
     q, k, v, do = (to_dev(inp[n], dtype) for n in ("q", "k", "v", "do"))
     temp, seg, bounds = to_dev(inp.get("temp")), to_dev(inp.get("seg")), to_dev(inp.get("bounds"))
+    inputs = [t for t in (q, k, v, do, temp, seg, bounds) if t is not None]
+    before = [t.clone() for t in inputs]
     B, L, Hq, D = q.shape
-    cfg = ca.make_config(ap, B, L, Hq, k.shape[2], D, dtype, Lk=k.shape[1])
-    ws = ca.new_workspace(cfg, q.device)
-    o, lse, m, l = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws, want_ml=want_ml)
-    dq, dk, dv, delta = ca.capattn_bwd(q, k, v, o, lse, do, ap, temp, seg, bounds, workspace=ws)
-    st, bits = ca.capattn_device_status(ws)
+    Lk, Hkv = k.shape[1], k.shape[2]
+    cfg = ca.make_config(ap, B, L, Hq, Hkv, D, dtype, Lk=Lk)
+    ws_bytes = max(ca.workspace_bytes(cfg, ca.PASS_FWD), ca.workspace_bytes(cfg, ca.PASS_BWD))
+    ws_g = Guarded((ws_bytes,), torch.uint8)
+    ws_g.tensor.zero_()
+    assert ws_g.tensor.data_ptr() % 256 == 0
+    g = {"O": Guarded((B, L, Hq, D), dtype), "LSE": Guarded((B, Hq, L), torch.float32),
+         "m": Guarded((B, Hq, L), torch.float32) if want_ml else None,
+         "l": Guarded((B, Hq, L), torch.float32) if want_ml else None,
+         "dQ": Guarded((B, L, Hq, D), dtype), "dK": Guarded((B, Lk, Hkv, D), dtype),
+         "dV": Guarded((B, Lk, Hkv, D), dtype), "delta": Guarded((B, Hq, L), torch.float32)}
+    t = {n: (None if x is None else x.tensor) for n, x in g.items()}
+    o, lse, m, l = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws_g.tensor,
+                                  out=(t["O"], t["LSE"], t["m"], t["l"]))
+    dq, dk, dv, delta = ca.capattn_bwd(q, k, v, o, lse, do, ap, temp, seg, bounds, workspace=ws_g.tensor,
+                                       out=(t["dQ"], t["dK"], t["dV"], t["delta"]))
+    st, bits = ca.capattn_device_status(ws_g.tensor)
     assert st == 0, f"device status {st} bits {bits}"
+    torch.cuda.synchronize()
+    for name, x in list(g.items()) + [("workspace", ws_g)]:
+        assert x is None or x.intact(), f"guard band of {name} overwritten"
+    for a, b in zip(inputs, before):
+        assert torch.equal(a, b), "an input was modified"
     out = {"O": o, "LSE": lse, "dQ": dq, "dK": dk, "dV": dv, "delta": delta, "m": m, "l": l}
     return {k2: (None if v2 is None else v2.float().cpu().numpy()) for k2, v2 in out.items()}
 

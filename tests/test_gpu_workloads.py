@@ -1,7 +1,8 @@
 """GPU parity at the five workloads' full sizes, in the launch configuration the
-benchmark times.  The CUDA path runs the whole batch; the oracle recomputes
-whole (batch, KV head) planes (forward and backward of every query head of the
-group) and those planes are compared: O max-abs, LSE max-abs on live rows with
+benchmark times.  The CUDA path runs the whole batch once; the oracle recomputes
+six whole (batch, KV head) planes per workload (forward and backward of every
+query head of the group), chosen at the extremes of the workload's masks, and
+those planes are compared: O max-abs, LSE max-abs on live rows with
 -inf identical, dQ / dK / dV relative Frobenius error per plane.  Across the
 whole batch, every output is also checked for finiteness and fully masked rows
 for exact zeros."""
@@ -19,9 +20,32 @@ from parity_utils import TOL_BF16_GRAD, TOL_BF16_LSE, TOL_BF16_O, rel_fro, to_de
 pytestmark = pytest.mark.gpu
 
 
-def _planes(w):
-    last = (w.B - 1, w.Hkv - 1)
-    return [(0, 0), last] if last != (0, 0) else [(0, 0)]
+def _planes(w, inp, limit=6):
+    """(batch, KV head) planes to recompute: the first and last, the batch rows
+    at the extremes of the workload's random structure (ranker: smallest and
+    largest history end hu, hu closest to and farthest past a 128-key tile
+    boundary, the most candidates; packed documents: the rows with the most and
+    the fewest documents), then seeded random planes up to `limit`."""
+    planes = [(0, 0), (w.B - 1, w.Hkv - 1)]
+    rows = []
+    if inp["bounds"] is not None:
+        hu = inp["bounds"][:, 1].astype(np.int64)
+        nc = inp["bounds"][:, 3].astype(np.int64) - inp["bounds"][:, 2]
+        rows += [int(np.argmin(hu)), int(np.argmax(hu)), int(np.argmin(hu % 128)),
+                 int(np.argmax(hu % 128)), int(np.argmax(nc))]
+    if inp["seg"] is not None:
+        ndocs = inp["seg"].max(axis=1) + 1
+        rows += [int(np.argmax(ndocs)), int(np.argmin(ndocs))]
+    for i, b in enumerate(rows):
+        planes.append((b, i % w.Hkv))
+    rng = np.random.default_rng(w.B * 1000 + w.L)
+    while len(set(planes)) < min(limit, w.B * w.Hkv):
+        planes.append((int(rng.integers(w.B)), int(rng.integers(w.Hkv))))
+    out = []
+    for p in planes:
+        if p not in out:
+            out.append(p)
+    return out[:limit]
 
 
 @pytest.mark.parametrize("idx", [2, 3, 4, 5, 6])
@@ -45,7 +69,7 @@ def test_full_size_workload_matches_oracle_on_sampled_planes(idx):
         assert (o_rows == 0).all()
     cfg_o = orc.config_from_workload(w)
     G = w.G
-    for b, g in _planes(w):
+    for b, g in _planes(w, inp):
         dQr, dKr, dVr, Or, LSEr = orc.backward_kv_head(inp["q"], inp["k"], inp["v"], inp["temp"],
                                                        inp["seg"], inp["bounds"], inp["do"],
                                                        cfg_o, b, g)
