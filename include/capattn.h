@@ -69,7 +69,7 @@ extern "C" {
 typedef enum capattn_status {
   CAPATTN_OK = 0,
   CAPATTN_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment or parameter */
-  CAPATTN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. bf16 with D != 128) */
+  CAPATTN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head dim D other than 64 or 128) */
   CAPATTN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
   CAPATTN_ERR_DEVICE_TIMEOUT = 4,/* a kernel gave up on a bounded wait (device status) */
   CAPATTN_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than capattn_workspace_bytes */

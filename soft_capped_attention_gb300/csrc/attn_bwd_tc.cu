@@ -43,13 +43,15 @@ namespace capattn {
 
 namespace {
 
-constexpr int HD = 128;
 constexpr int BT = 128;                       // tile rows (queries and keys)
 constexpr int SLAB = 128 * 64 * 2;
-constexpr int TILE = 2 * SLAB;
+// A 128-row tile of head dim HD (64 or 128) is HD / 64 slabs.
+template <int HD>
+constexpr int tile_bytes() { return (HD / 64) * SLAB; }
 constexpr int NSTAGE = 2;
 constexpr int NTHREADS = 320;
-constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
+template <int HD>
+constexpr int smem_bytes() { return 2 * tile_bytes<HD>() + NSTAGE * 2 * tile_bytes<HD>() + 1024; }
 
 // 32 fp32 values of row r as bf16 into 16-byte chunks q0 .. q0 + 3 of a
 // swizzled [128][64] bf16 slab (the layout the TMA store reads).
@@ -109,6 +111,7 @@ __device__ __forceinline__ ColRaw load_col_raw(const Params& p, int b, int h, in
 // ======================================================================= dK / dV
 // Score MMAs of a whole step: D[128 x 128] = A[128 x 128] B^T, both K-major,
 // from the tiles' descriptors.
+template <int HD>
 __device__ __forceinline__ void issue_scores(uint32_t d, uint64_t dA, uint64_t dB) {
   constexpr uint32_t idesc = idesc_bf16(BT, BT, 0, 0);
 #pragma unroll
@@ -244,12 +247,14 @@ __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_ba
 // j + 1 while step j's elementwise work runs), and packs P^T / dX^T over its dP^T
 // columns chunk by chunk; dP^T of step j + 1 is issued once every chunk's MMAs
 // are.
-template <int METHOD>
+template <int METHOD, int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
               const __grid_constant__ CUtensorMap mdk, const __grid_constant__ CUtensorMap mdv,
               const Params p) {
+  constexpr int TILE = tile_bytes<HD>();
+  constexpr int NSLAB = HD / 64;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[26];
   __shared__ uint32_t tmem_slot;
@@ -321,10 +326,10 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         tma_prefetch_desc(&mdk);
         tma_prefetch_desc(&mdv);
         mbar_expect_tx(bar_kv, 2 * TILE);
-        tma_load_4d(sK, &mk, bar_kv, 0, g, k0, b);
-        tma_load_4d(sK + SLAB, &mk, bar_kv, 64, g, k0, b);
-        tma_load_4d(sV, &mv, bar_kv, 0, g, k0, b);
-        tma_load_4d(sV + SLAB, &mv, bar_kv, 64, g, k0, b);
+        for (int sl = 0; sl < NSLAB; ++sl) {
+          tma_load_4d(sK + sl * SLAB, &mk, bar_kv, 64 * sl, g, k0, b);
+          tma_load_4d(sV + sl * SLAB, &mv, bar_kv, 64 * sl, g, k0, b);
+        }
       }
       __syncwarp();
       StepIter st(map, p.wq, p.G);
@@ -336,10 +341,10 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (leader) {
           const uint32_t sQ = sQD + s * 2 * TILE, sO = sQ + TILE;
           mbar_expect_tx(bar_full + 8 * s, 2 * TILE);
-          tma_load_4d(sQ, &mq, bar_full + 8 * s, 0, h, qt * BT, b);
-          tma_load_4d(sQ + SLAB, &mq, bar_full + 8 * s, 64, h, qt * BT, b);
-          tma_load_4d(sO, &mdo, bar_full + 8 * s, 0, h, qt * BT, b);
-          tma_load_4d(sO + SLAB, &mdo, bar_full + 8 * s, 64, h, qt * BT, b);
+          for (int sl = 0; sl < NSLAB; ++sl) {
+            tma_load_4d(sQ + sl * SLAB, &mq, bar_full + 8 * s, 64 * sl, h, qt * BT, b);
+            tma_load_4d(sO + sl * SLAB, &mdo, bar_full + 8 * s, 64 * sl, h, qt * BT, b);
+          }
         }
         __syncwarp();
         ++j;
@@ -364,9 +369,9 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (ok) {
         tc_fence_after();
         if (leader) {
-          issue_scores(tmem, dK, dQD);                          // S^T  = K Q^T
+          issue_scores<HD>(tmem, dK, dQD);                          // S^T  = K Q^T
           mma_commit(bar_s);
-          issue_scores(tmem + 128u, dV, desc_add(dQD, TILE));   // dP^T = V dO^T
+          issue_scores<HD>(tmem + 128u, dV, desc_add(dQD, TILE));   // dP^T = V dO^T
           mma_commit(bar_dp);
         }
         __syncwarp();
@@ -382,7 +387,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             break;
           tc_fence_after();
           if (leader) {
-            issue_scores(tmem, dK, desc_add(dQD, son));
+            issue_scores<HD>(tmem, dK, desc_add(dQD, son));
             mma_commit(bar_s);
           }
           __syncwarp();
@@ -410,7 +415,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (leader) {
           mma_commit(bar_empty + 8 * (j % NSTAGE));
           if (more) {
-            issue_scores(tmem + 128u, dV, desc_add(dQD, son + TILE));
+            issue_scores<HD>(tmem + 128u, dV, desc_add(dQD, son + TILE));
             mma_commit(bar_dp);
           }
         }
@@ -548,7 +553,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const uint32_t oslab = wg == 0 ? sV : sK;
     const uint32_t acc = lane_base + (wg == 0 ? 256u : 384u);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < HD / 32; ++c) {
       uint32_t v[32];
       if (have) {
         tmem_ld32(acc + c * 32, v);
@@ -563,8 +568,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     named_bar_sync(1 + wg, 128);  // the warpgroup's rows are in shared memory
     if (tid == 0) {
       const CUtensorMap* mo = wg == 0 ? &mdv : &mdk;
-      tma_store_4d(mo, oslab, 0, g, k0, b);
-      tma_store_4d(mo, oslab + SLAB, 64, g, k0, b);
+      for (int sl = 0; sl < NSLAB; ++sl) tma_store_4d(mo, oslab + sl * SLAB, 64 * sl, g, k0, b);
       bulk_commit();
       bulk_wait_read0();
     }
@@ -644,11 +648,13 @@ __device__ __forceinline__ void dq_step(const uint32_t (&s)[64], uint32_t dp_bas
 // the S buffer once the elementwise warps have copied step j's S to registers
 // (at the start of step j) and K_{j+1} has landed.  The elementwise warpgroups
 // own 64 key columns each and pack dX over the step's dP columns chunk by chunk.
-template <int METHOD, bool DT>
+template <int METHOD, bool DT, int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
              const __grid_constant__ CUtensorMap mdq, const Params p) {
+  constexpr int TILE = tile_bytes<HD>();
+  constexpr int NSLAB = HD / 64;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[24];
   __shared__ uint32_t tmem_slot;
@@ -722,10 +728,10 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tma_prefetch_desc(&mv);
         tma_prefetch_desc(&mdq);
         mbar_expect_tx(bar_q, 2 * TILE);
-        tma_load_4d(sQ, &mq, bar_q, 0, h, q0, b);
-        tma_load_4d(sQ + SLAB, &mq, bar_q, 64, h, q0, b);
-        tma_load_4d(sO, &mdo, bar_q, 0, h, q0, b);
-        tma_load_4d(sO + SLAB, &mdo, bar_q, 64, h, q0, b);
+        for (int sl = 0; sl < NSLAB; ++sl) {
+          tma_load_4d(sQ + sl * SLAB, &mq, bar_q, 64 * sl, h, q0, b);
+          tma_load_4d(sO + sl * SLAB, &mdo, bar_q, 64 * sl, h, q0, b);
+        }
       }
       __syncwarp();
       // V of step j as soon as dP of step j - 2 has read its stage, then K of
@@ -738,8 +744,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         if (u > 0 && !mbar_wait_warp(bar_vempty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) break;
         if (leader) {
           mbar_expect_tx(bar_vfull + 8 * s, TILE);
-          tma_load_4d(sV, &mv, bar_vfull + 8 * s, 0, g, t * BT, b);
-          tma_load_4d(sV + SLAB, &mv, bar_vfull + 8 * s, 64, g, t * BT, b);
+          for (int sl = 0; sl < NSLAB; ++sl)
+            tma_load_4d(sV + sl * SLAB, &mv, bar_vfull + 8 * s, 64 * sl, g, t * BT, b);
         }
         __syncwarp();
         if (u > 0 && !mbar_wait_warp(bar_kempty + 8 * s, (u - 1) & 1, p.status, &abort_flag)) {
@@ -748,8 +754,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         }
         if (leader) {
           mbar_expect_tx(bar_kfull + 8 * s, TILE);
-          tma_load_4d(sK, &mk, bar_kfull + 8 * s, 0, g, t * BT, b);
-          tma_load_4d(sK + SLAB, &mk, bar_kfull + 8 * s, 64, g, t * BT, b);
+          for (int sl = 0; sl < NSLAB; ++sl)
+            tma_load_4d(sK + sl * SLAB, &mk, bar_kfull + 8 * s, 64 * sl, g, t * BT, b);
         }
         __syncwarp();
         ++j;
@@ -779,7 +785,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
           return false;
         tc_fence_after();
         if (leader) {
-          issue_scores(tmem, dQ, desc_add(dKV, (uint32_t)((j % NSTAGE) * 2 * TILE)));
+          issue_scores<HD>(tmem, dQ, desc_add(dKV, (uint32_t)((j % NSTAGE) * 2 * TILE)));
           mma_commit(bar_s);
         }
         __syncwarp();
@@ -792,7 +798,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
           return false;
         tc_fence_after();
         if (leader) {
-          issue_scores(tmem + 128u + 128u * (uint32_t)(j & 1), dO,
+          issue_scores<HD>(tmem + 128u + 128u * (uint32_t)(j & 1), dO,
                        desc_add(dKV, (uint32_t)((j % NSTAGE) * 2 * TILE + TILE)));
           mma_commit(bar_dp + 8 * (j & 1));
           mma_commit(bar_vempty + 8 * (j % NSTAGE));
@@ -862,20 +868,22 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       float dpart = 0.f;
       if (n > 0) {
         // O is loaded first, so that its latency overlaps the wait for the tiles
-        uint4 orow_g[8];
+        constexpr int NCH = HD / 8;       // 16-byte chunks (8 bf16) of a row; each warpgroup takes half
+        uint4 orow_g[NCH / 2];
         if (valid) {
           const uint4* og = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(p.o) + ((size_t)(b * p.L + i) * p.Hq + h) * HD + 64 * wg);
+              static_cast<const __nv_bfloat16*>(p.o) + ((size_t)(b * p.L + i) * p.Hq + h) * HD + (HD / 2) * wg);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) orow_g[c] = og[c];
+          for (int c = 0; c < NCH / 2; ++c) orow_g[c] = og[c];
         }
         if (!mbar_wait_warp(bar_q, 0, p.status, &abort_flag)) aborted = true;
         if (valid && !aborted) {
-          const uint8_t* orow = smem_raw + (sO - smem_u32(smem_raw)) + wg * SLAB + r * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < NCH / 2; ++c) {
+            const int gc = (NCH / 2) * wg + c;   // chunk of the row: slab gc / 8, chunk gc % 8
+            const uint8_t* orow = smem_raw + (sO - smem_u32(smem_raw)) + (gc >> 3) * SLAB + r * 128;
             const uint4 a = orow_g[c];
-            const uint4 d = *reinterpret_cast<const uint4*>(orow + ((c ^ (r & 7)) << 4));
+            const uint4 d = *reinterpret_cast<const uint4*>(orow + (((gc & 7) ^ (r & 7)) << 4));
             const uint32_t av[4] = {a.x, a.y, a.z, a.w}, dv4[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -985,25 +993,37 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     // Warpgroup wg writes dQ columns [64 wg, 64 wg + 64) through slab wg of
     // the Q tile's shared memory (free once every MMA has completed) and one
     // TMA store (rows past L are clipped).
-    const uint32_t oslab = sQ + (uint32_t)wg * SLAB;
+    // HD = 128: warpgroup wg fills slab wg; HD = 64: the two warpgroups fill
+    // the two halves (16-byte chunks [0, 4) and [4, 8)) of the one slab.
+    const uint32_t oslab = sQ + (HD == 128 ? (uint32_t)wg * SLAB : 0u);
+    const int chunk0 = HD == 128 ? 0 : 4 * wg;
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < HD / 64; ++c) {
       uint32_t v[32];
       if (have) {
-        tmem_ld32(lane_base + 384u + 64 * wg + 32 * c, v);
+        tmem_ld32(lane_base + 384u + (HD / 2) * wg + 32 * c, v);
         tmem_wait_ld();
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = 0u;
       }
-      st_row32_swz(oslab, r, 4 * c, v);
+      st_row32_swz(oslab, r, chunk0 + 4 * c, v);
     }
     fence_async_smem();
-    named_bar_sync(1 + wg, 128);  // the warpgroup's rows are in shared memory
-    if (warp == 2 + 4 * wg && lane == 0) {
-      tma_store_4d(&mdq, oslab, 64 * wg, h, q0, b);
-      bulk_commit();
-      bulk_wait_read0();
+    if constexpr (HD == 128) {
+      named_bar_sync(1 + wg, 128);  // the warpgroup's rows are in shared memory
+      if (warp == 2 + 4 * wg && lane == 0) {
+        tma_store_4d(&mdq, oslab, 64 * wg, h, q0, b);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+    } else {
+      named_bar_sync(1, 256);       // both warpgroups' halves are in shared memory
+      if (warp == 2 && lane == 0) {
+        tma_store_4d(&mdq, oslab, 0, h, q0, b);
+        bulk_commit();
+        bulk_wait_read0();
+      }
     }
   }
   __syncwarp();  // warps 0 and 1 reach the CTA barrier converged
@@ -1017,38 +1037,44 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
   }
 }
 
+template <int METHOD, int HD>
+cudaError_t launch_bwd_hd(const Params& p, cudaStream_t s) {
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BT);
+  if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.Lk, p.Hkv, HD, BT);
+  if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.Lk, p.Hkv, HD, BT);
+  if (e == cudaSuccess) e = make_bhld_map(&mdo, p.dO, p.B, p.L, p.Hq, HD, BT);
+  if (e == cudaSuccess) e = make_bhld_map(&mdq, p.dq, p.B, p.L, p.Hq, HD, BT);
+  if (e == cudaSuccess) e = make_bhld_map(&mdk, p.dk, p.B, p.Lk, p.Hkv, HD, BT);
+  if (e == cudaSuccess) e = make_bhld_map(&mdv, p.dv, p.B, p.Lk, p.Hkv, HD, BT);
+  if (e != cudaSuccess) return e;
+  constexpr int SMEM_BYTES = smem_bytes<HD>();
+  // dQ first: it also computes delta, which the dK/dV kernel reads.
+  auto kdq = p.dtemp ? dq_tc_kernel<METHOD, true, HD> : dq_tc_kernel<METHOD, false, HD>;
+  e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  prof_begin(CAPATTN_KERNEL_DQ, s);
+  prof_count(CAPATTN_KERNEL_DQ, 1);
+  e = launch_pdl(kdq, dim3(p.Hq * p.B, p.nq), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdq, p);
+  if (e != cudaSuccess) return e;
+  prof_end(CAPATTN_KERNEL_DQ, s);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto kdkv = dkv_tc_kernel<METHOD, HD>;
+  e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  prof_begin(CAPATTN_KERNEL_DKV, s);
+  prof_count(CAPATTN_KERNEL_DKV, 1);
+  e = launch_pdl(kdkv, dim3(p.Hkv * p.B, p.nk), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdk, mdv, p);
+  if (e != cudaSuccess) return e;
+  prof_end(CAPATTN_KERNEL_DKV, s);
+  return cudaGetLastError();
+}
+
 template <int METHOD>
 struct BwdTcLaunch {
   static cudaError_t run(const Params& p, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
-    cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.Lk, p.Hkv, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.Lk, p.Hkv, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mdo, p.dO, p.B, p.L, p.Hq, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mdq, p.dq, p.B, p.L, p.Hq, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mdk, p.dk, p.B, p.Lk, p.Hkv, HD, BT);
-    if (e == cudaSuccess) e = make_bhld_map(&mdv, p.dv, p.B, p.Lk, p.Hkv, HD, BT);
-    if (e != cudaSuccess) return e;
-    // dQ first: it also computes delta, which the dK/dV kernel reads.
-    auto kdq = p.dtemp ? dq_tc_kernel<METHOD, true> : dq_tc_kernel<METHOD, false>;
-    e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    prof_begin(CAPATTN_KERNEL_DQ, s);
-    prof_count(CAPATTN_KERNEL_DQ, 1);
-    e = launch_pdl(kdq, dim3(p.Hq * p.B, p.nq), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdq, p);
-    if (e != cudaSuccess) return e;
-    prof_end(CAPATTN_KERNEL_DQ, s);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    auto kdkv = dkv_tc_kernel<METHOD>;
-    e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    prof_begin(CAPATTN_KERNEL_DKV, s);
-    prof_count(CAPATTN_KERNEL_DKV, 1);
-    e = launch_pdl(kdkv, dim3(p.Hkv * p.B, p.nk), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdk, mdv, p);
-    if (e != cudaSuccess) return e;
-    prof_end(CAPATTN_KERNEL_DKV, s);
-    return cudaGetLastError();
+    return p.D == 64 ? launch_bwd_hd<METHOD, 64>(p, s) : launch_bwd_hd<METHOD, 128>(p, s);
   }
 };
 

@@ -47,11 +47,13 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int HD = 128;
 constexpr int NSTAGE = 2;
 constexpr int SLAB = 128 * 64 * 2;          // one [128][64] bf16 box
-constexpr int TILE = 2 * SLAB;               // 128 x 128 bf16
-constexpr int SMEM_BYTES = 2 * TILE + NSTAGE * 2 * TILE + 1024;
+// A 128-row tile of head dim HD (64 or 128) is HD / 64 slabs.
+template <int HD>
+constexpr int tile_bytes() { return (HD / 64) * SLAB; }
+template <int HD>
+constexpr int smem_bytes() { return 2 * tile_bytes<HD>() + NSTAGE * 2 * tile_bytes<HD>() + 1024; }
 constexpr int NTHREADS = 576;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // Capped logits of a row lie in a window [x_hi - W, x_hi] (log2 units) known
@@ -99,6 +101,7 @@ __device__ __forceinline__ int count_union(const uint32_t* a, const uint32_t* c,
 }
 
 // S = Q K^T from the tiles' K-major descriptors.
+template <int HD>
 __device__ __forceinline__ void issue_s(uint32_t d, uint64_t dQ, uint64_t dK) {
   constexpr uint32_t idesc = idesc_bf16(BM, BN, 0, 0);
 #pragma unroll
@@ -109,7 +112,8 @@ __device__ __forceinline__ void issue_s(uint32_t d, uint64_t dQ, uint64_t dK) {
 }
 
 // O += P V with P (bf16) in TMEM (key columns [0, 64) packed at pt + [0, 32),
-// [64, 128) at pt + [64, 96)) and V's MN-major descriptor.
+// [64, 128) at pt + [64, 96)) and V's MN-major descriptor (N = HD).
+template <int HD>
 __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t pt, uint64_t dV, uint32_t acc0) {
   constexpr uint32_t idesc = idesc_bf16(BM, HD, 0, 1);
 #pragma unroll
@@ -252,11 +256,13 @@ __device__ __forceinline__ float p_dispatch(bool full_any, bool poly, const uint
   return p_chunk<METHOD, true, 8>(v, pk, xf, mul, addm, live);
 }
 
-template <int METHOD>
+template <int METHOD, int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
               const Params p) {
+  constexpr int TILE = tile_bytes<HD>();
+  constexpr int NSLAB = HD / 64;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[16];
   __shared__ uint32_t tmem_slot;
@@ -354,10 +360,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         tma_prefetch_desc(&mv);
         tma_prefetch_desc(&mo);
         mbar_expect_tx(bar_q, 2 * TILE);
-        tma_load_4d(sQ0, &mq, bar_q, 0, h, qt0 * BM, b);
-        tma_load_4d(sQ0 + SLAB, &mq, bar_q, 64, h, qt0 * BM, b);
-        tma_load_4d(sQ1, &mq, bar_q, 0, h, qt0 * BM + BM, b);
-        tma_load_4d(sQ1 + SLAB, &mq, bar_q, 64, h, qt0 * BM + BM, b);
+        for (int sl = 0; sl < NSLAB; ++sl) {
+          tma_load_4d(sQ0 + sl * SLAB, &mq, bar_q, 64 * sl, h, qt0 * BM, b);
+          tma_load_4d(sQ1 + sl * SLAB, &mq, bar_q, 64 * sl, h, qt0 * BM + BM, b);
+        }
       }
       __syncwarp();
       PairIter it(map0, map1, p.wk);
@@ -369,11 +375,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (leader) {
           const uint32_t sK = sKV + s * 2 * TILE, sV = sK + TILE;
           mbar_expect_tx(bar_kfull + 8 * s, TILE);
-          tma_load_4d(sK, &mk, bar_kfull + 8 * s, 0, g, t * BN, b);
-          tma_load_4d(sK + SLAB, &mk, bar_kfull + 8 * s, 64, g, t * BN, b);
+          for (int sl = 0; sl < NSLAB; ++sl)
+            tma_load_4d(sK + sl * SLAB, &mk, bar_kfull + 8 * s, 64 * sl, g, t * BN, b);
           mbar_expect_tx(bar_vfull + 8 * s, TILE);
-          tma_load_4d(sV, &mv, bar_vfull + 8 * s, 0, g, t * BN, b);
-          tma_load_4d(sV + SLAB, &mv, bar_vfull + 8 * s, 64, g, t * BN, b);
+          for (int sl = 0; sl < NSLAB; ++sl)
+            tma_load_4d(sV + sl * SLAB, &mv, bar_vfull + 8 * s, 64 * sl, g, t * BN, b);
         }
         __syncwarp();
         ++j;
@@ -407,8 +413,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (ok) {
         tc_fence_after();
         if (leader) {
-          if (c0) { issue_s(tmem, dQ0, dKV); mma_commit(bar_sfull); }
-          if (c1) { issue_s(tmem + 128u, dQ1, dKV); mma_commit(bar_sfull + 8); }
+          if (c0) { issue_s<HD>(tmem, dQ0, dKV); mma_commit(bar_sfull); }
+          if (c1) { issue_s<HD>(tmem + 128u, dQ1, dKV); mma_commit(bar_sfull + 8); }
         }
         __syncwarp();
       }
@@ -424,27 +430,27 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           if (!mbar_wait_warp(bar_pfull, pc0 & 1, p.status, &abort_flag)) break;
           ++pc0;
           tc_fence_after();
-          if (leader) issue_pv(tmem + 256u, tmem, desc_add(dKVmn, vo), started0);
+          if (leader) issue_pv<HD>(tmem + 256u, tmem, desc_add(dKVmn, vo), started0);
           __syncwarp();
           started0 = 1;
         }
         if (more) {
           if (!mbar_wait_warp(bar_kfull + 8 * s1, ((j + 1) / NSTAGE) & 1, p.status, &abort_flag)) break;
           tc_fence_after();
-          if (n0 && leader) { issue_s(tmem, dQ0, desc_add(dKV, ko)); mma_commit(bar_sfull); }
+          if (n0 && leader) { issue_s<HD>(tmem, dQ0, desc_add(dKV, ko)); mma_commit(bar_sfull); }
           __syncwarp();
         }
         if (c1) {
           if (!mbar_wait_warp(bar_pfull + 8, pc1 & 1, p.status, &abort_flag)) break;
           ++pc1;
           tc_fence_after();
-          if (leader) issue_pv(tmem + 384u, tmem + 128u, desc_add(dKVmn, vo), started1);
+          if (leader) issue_pv<HD>(tmem + 384u, tmem + 128u, desc_add(dKVmn, vo), started1);
           __syncwarp();
           started1 = 1;
         }
         if (leader) {
           mma_commit(bar_empty + 8 * s);
-          if (more && n1) { issue_s(tmem + 128u, dQ1, desc_add(dKV, ko)); mma_commit(bar_sfull + 8); }
+          if (more && n1) { issue_s<HD>(tmem + 128u, dQ1, desc_add(dKV, ko)); mma_commit(bar_sfull + 8); }
         }
         __syncwarp();
         c0 = n0;
@@ -460,7 +466,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int quarter = warp & 3;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_base = tmem + lane_off + (uint32_t)tsel * 128u + 64u * (uint32_t)half;
-    const uint32_t o_base = tmem + lane_off + 256u + (uint32_t)tsel * 128u + 64u * (uint32_t)half;
+    // this half's HD / 2 columns of the tile's O
+    const uint32_t o_base = tmem + lane_off + 256u + (uint32_t)tsel * 128u + (uint32_t)(HD / 2) * half;
     const uint32_t my_sfull = bar_sfull + 8 * tsel, my_pfull = bar_pfull + 8 * tsel;
     const uint32_t my_xch = bar_xch + 8 * tsel;
     const int4 ri = valid ? p.rowinfo[(size_t)b * p.L + i] : make_int4(0, 0, -1, 0);
@@ -535,7 +542,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       // ---- O rescale of this half's 64 columns (PV of the previous live tile is complete)
       if (cnt > 0 && __any_sync(0xFFFFFFFFu, resc)) {
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < HD / 64; ++c) {
           uint32_t o[32];
           tmem_ld32(o_base + c * 32, o);
           tmem_wait_ld();
@@ -617,9 +624,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     // half's slab of the tile's Q is free and takes the rows' 64 bf16 values in
     // the swizzled layout; one TMA store per (tile, half) writes the slab (rows
     // past L are clipped by the tensor map).
-    const uint32_t oslab = (tsel ? sQ1 : sQ0) + (uint32_t)half * SLAB;
+    // HD = 128: each half fills its own slab; HD = 64: the two halves fill the
+    // two halves (16-byte chunks [0, 4) and [4, 8)) of the tile's one slab.
+    const uint32_t tile_smem = tsel ? sQ1 : sQ0;
+    const uint32_t oslab = tile_smem + (HD == 128 ? (uint32_t)half * SLAB : 0u);
+    const int chunk0 = HD == 128 ? 0 : 4 * half;
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < HD / 64; ++c) {
       uint32_t o[32];
       if (have_o) {
         tmem_ld32(o_base + c * 32, o);
@@ -634,14 +645,23 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        st_swz_chunk(oslab, r, 4 * c + e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        st_swz_chunk(oslab, r, chunk0 + 4 * c + e, pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
     }
     fence_async_smem();
-    named_bar_sync(1 + (sw >> 2), 128);  // the four warps of this (tile, half)
-    if ((sw & 3) == 0 && lane == 0 && (tsel == 0 || has1)) {
-      tma_store_4d(&mo, oslab, 64 * half, h, (qt0 + tsel) * BM, b);
-      bulk_commit();
-      bulk_wait_read0();
+    if constexpr (HD == 128) {
+      named_bar_sync(1 + (sw >> 2), 128);  // the four warps of this (tile, half)
+      if ((sw & 3) == 0 && lane == 0 && (tsel == 0 || has1)) {
+        tma_store_4d(&mo, oslab, 64 * half, h, (qt0 + tsel) * BM, b);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+    } else {
+      named_bar_sync(1 + tsel, 256);       // the eight warps of this tile
+      if ((sw & 7) == 0 && lane == 0 && (tsel == 0 || has1)) {
+        tma_store_4d(&mo, tile_smem, 0, h, (qt0 + tsel) * BM, b);
+        bulk_commit();
+        bulk_wait_read0();
+      }
     }
     if (valid && half == 0) {
       const size_t rr = ((size_t)b * p.Hq + h) * p.L + i;
@@ -663,24 +683,30 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   }
 }
 
+template <int METHOD, int HD>
+cudaError_t launch_fwd_hd(const Params& p, cudaStream_t s) {
+  CUtensorMap mq, mk, mv, mo;
+  cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BM);
+  if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.Lk, p.Hkv, HD, BN);
+  if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.Lk, p.Hkv, HD, BN);
+  if (e == cudaSuccess) e = make_bhld_map(&mo, p.o, p.B, p.L, p.Hq, HD, BM);
+  if (e != cudaSuccess) return e;
+  auto kern = fwd_tc_kernel<METHOD, HD>;
+  constexpr int SMEM_BYTES = smem_bytes<HD>();
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  prof_begin(CAPATTN_KERNEL_FWD, s);
+  prof_count(CAPATTN_KERNEL_FWD, 1);
+  e = launch_pdl(kern, dim3(p.Hq * p.B, (p.nq + 1) / 2), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mo, p);
+  if (e != cudaSuccess) return e;
+  prof_end(CAPATTN_KERNEL_FWD, s);
+  return cudaGetLastError();
+}
+
 template <int METHOD>
 struct FwdTcLaunch {
   static cudaError_t run(const Params& p, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, mo;
-    cudaError_t e = make_bhld_map(&mq, p.q, p.B, p.L, p.Hq, HD, BM);
-    if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.Lk, p.Hkv, HD, BN);
-    if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.Lk, p.Hkv, HD, BN);
-    if (e == cudaSuccess) e = make_bhld_map(&mo, p.o, p.B, p.L, p.Hq, HD, BM);
-    if (e != cudaSuccess) return e;
-    auto kern = fwd_tc_kernel<METHOD>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    prof_begin(CAPATTN_KERNEL_FWD, s);
-    prof_count(CAPATTN_KERNEL_FWD, 1);
-    e = launch_pdl(kern, dim3(p.Hq * p.B, (p.nq + 1) / 2), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mo, p);
-    if (e != cudaSuccess) return e;
-    prof_end(CAPATTN_KERNEL_FWD, s);
-    return cudaGetLastError();
+    return p.D == 64 ? launch_fwd_hd<METHOD, 64>(p, s) : launch_fwd_hd<METHOD, 128>(p, s);
   }
 };
 

@@ -58,8 +58,7 @@ static capattn_status validate(const capattn_config* c) {
   // 64-bit across planes; keep one plane comfortably inside int32.
   if ((int64_t)c->L * c->Hq * c->D >= (1ll << 31)) return CAPATTN_ERR_UNSUPPORTED;
   if ((int64_t)key_len(*c) * c->Hkv * c->D >= (1ll << 31)) return CAPATTN_ERR_UNSUPPORTED;
-  if (c->dtype == CAPATTN_BF16 && c->D != 128) return CAPATTN_ERR_UNSUPPORTED;
-  if (c->dtype == CAPATTN_FP32 && c->D != 64 && c->D != 128) return CAPATTN_ERR_UNSUPPORTED;
+  if (c->D != 64 && c->D != 128) return CAPATTN_ERR_UNSUPPORTED;
   return CAPATTN_OK;
 }
 

@@ -53,7 +53,8 @@ def test_validation_codes(lib):
     assert v(_cfg()) == 0
     assert v(_cfg(Hq=3)) == 1                 # Hq not a multiple of Hkv
     assert v(_cfg(L=0)) == 1
-    assert v(_cfg(D=64)) == 2                 # bf16 needs D = 128
+    assert v(_cfg(D=64)) == 0                 # bf16: D = 64 or 128
+    assert v(_cfg(D=96)) == 2
     assert v(_cfg(D=64, dtype=torch.float32)) == 0
     assert v(_cfg(D=96, dtype=torch.float32)) == 2
     c = _cfg()

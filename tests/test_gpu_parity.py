@@ -86,6 +86,60 @@ def test_bf16_matches_oracle(case):
     compare(got, ref, torch.bfloat16)
 
 
+# bf16 with head dim 64 (the tcgen05 kernels' D = 64 instantiation).  The first
+# case is the shape mosaic_backward.py's test_mosaic_backward_correctness
+# draws: B=1, L=128, H=4, H_kv=2, D=64, ALSC cap 30, alpha 4, beta 0.5, and a
+# per-query temperature (there drawn from U[0.8, 1.2], here U[0.5, 1.5]).
+D64_CASES = [
+    # (B, L, Hq, Hkv, cap, (cap, alpha, beta) or None, mask, temp, z)
+    (1, 128, 4, 2, "alsc", (30.0, 4.0, 0.5), "full", True, 0.0),
+    (2, 300, 4, 2, "tanh", None, "causal", False, 0.0),
+    (1, 513, 4, 1, "alsc", None, "window", True, 1e-4),
+    (2, 384, 2, 2, "soft_sign", None, "packed", False, 0.0),
+    (2, 400, 4, 2, "alsc", None, "ranker", False, 0.01),
+    (1, 257, 2, 1, "none", None, "window_nc", True, 0.0),
+    # (L = 1 would leave a single live key per row, where dP - delta cancels
+    # exactly and dQ, dK are zero: no relative error is defined there)
+    (1, 2, 2, 1, "tanh", None, "causal", False, 0.0),
+]
+
+
+@pytest.mark.parametrize("case", D64_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_bf16_head_dim_64_matches_oracle(case):
+    B, L, Hq, Hkv, cap, cparams, mask, temp, z = case
+    inp = make_case(B, L, Hq, Hkv, 64, torch.bfloat16, mask, temp, seed=L * 5 + Hq)
+    ap = params(cap, mask, z)
+    if cparams is not None:
+        ap = ca.AttnParams(sm_scale=0.125, cap_method=cap, cap=cparams[0], alpha=cparams[1],
+                           beta=cparams[2], causal=ap.causal, window_len=ap.window_len,
+                           z_loss_weight=z)
+    got = run_gpu(inp, ap, torch.bfloat16, want_ml=(L == 300))
+    ref = run_oracle(inp, ap)
+    compare(got, ref, torch.bfloat16)
+    np.testing.assert_allclose(got["delta"], ref["delta"], atol=5e-2)
+
+
+def test_bf16_head_dim_64_dtemp_and_lse_gradient():
+    from parity_utils import oracle_cfg, rel_fro
+    inp = make_case(2, 300, 4, 2, 64, torch.bfloat16, "causal", True, seed=64)
+    ap = params("tanh", "causal", 0.01)
+    dlse = np.random.default_rng(64).standard_normal((2, 4, 300)).astype(np.float32)
+    q, k, v, do = (to_dev(inp[n], torch.bfloat16) for n in ("q", "k", "v", "do"))
+    temp = to_dev(inp["temp"])
+    o, lse, _, _ = ca.capattn_fwd(q, k, v, ap, temp)
+    dq, dk, dv, _, dtemp = ca.capattn_bwd_ex(q, k, v, o, lse, do, ap, temp, dlse=to_dev(dlse),
+                                             want_dtemp=True)
+    oc = oracle_cfg(ap)
+    O, LSE, _, _ = orc.forward(inp["q"], inp["k"], inp["v"], inp["temp"], None, None, oc)
+    ref = orc.backward(inp["q"], inp["k"], inp["v"], inp["temp"], None, None, O, LSE, inp["do"], oc,
+                       dLSE=dlse.astype(np.float64))
+    for got, r in zip((dq, dk, dv), ref[:3]):
+        assert rel_fro(got.float().cpu().numpy(), r) <= 2e-2
+    rdt = orc.backward_dtemp(inp["q"], inp["k"], inp["v"], inp["temp"], None, None, O, LSE, inp["do"],
+                             oc, dLSE=dlse.astype(np.float64))
+    assert rel_fro(dtemp.cpu().numpy(), rdt) <= 2e-2
+
+
 FP32_CASES = [
     (1, 128, 2, 2, 64, "none", "full", False, 0.0),
     (2, 200, 4, 2, 64, "tanh", "causal", True, 0.0),
