@@ -64,7 +64,7 @@ METRIC = "capped-attention fwd+bwd TFLOP/s (mask-aware) and % of GB300 BF16 peak
 # does Q K^T and P V; the dK/dV kernel recomputes S and does dP, dV, dK; the dQ
 # kernel's own product is dQ (its S and dP recomputations are not counted).
 KERNEL_FLOPS_PER_PAIR_D = {"fwd": 4, "dkv": 8, "dq": 2}
-SOAK_SECONDS = 1.0
+SOAK_SECONDS = 1.0  # default of --soak-seconds
 
 
 def dist_env():
@@ -158,7 +158,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
                 "samples": len(self.samples), "power_w_max": max(pw) if pw else None,
-                "window": f"an untimed soak of ~{SOAK_SECONDS:.0f} s of the same step, then the timed steps"}
+                "window": "an untimed soak of the same step (--soak-seconds), then the timed steps"}
 
 
 def kernel_source_hash() -> str:
@@ -418,7 +418,7 @@ def run_capattn(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     step_ms_est = (fw + bw) / max(args.steps, 1)
-    soak = max(1, int(SOAK_SECONDS / max(step_ms_est * 1e-3 + 1e-4, 1e-6)))
+    soak = int(args.soak_seconds / max(step_ms_est * 1e-3 + 1e-4, 1e-6)) if args.soak_seconds > 0 else 0
     with ClockSampler(local_rank) as clk:
         for _ in range(soak):
             flush.zero_()
@@ -614,6 +614,8 @@ def main():
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--per-workload-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--soak-seconds", type=float, default=SOAK_SECONDS,
+                    help="untimed run of the step under the clock sampler before the timed steps")
     ap.add_argument("--dtemp", action="store_true",
                     help="also compute the temperature gradient (workloads with a temperature)")
     args = ap.parse_args()
