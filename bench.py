@@ -3,7 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl capattn|reference]
                     [--workload 2] [--no-cpu-baseline] [--no-e2e] [--no-per-workload]
 
-A step is one forward (capattn_fwd) and one backward (capattn_bwd) over the
+A step is one forward (capattn_fwd) and one backward (capattn_bwd_ex, reusing
+the spans and visit maps the forward left in the shared workspace) over the
 workload's batch of synthetic seeded inputs.  The default workload is
 causal_tanh: B=2, Hq=Hkv=16, L=2048, D=128, bf16, causal, tanh cap 50.
 
@@ -213,11 +214,11 @@ class Run:
         self.flops = 14.0 * w.D * self.N
 
     def bwd(self, q, k, v, o, lse, do, temp, seg, bounds):
-        ca = self.ca
-        if self.dtemp:
-            return ca.capattn_bwd_dtemp(q, k, v, o, lse, do, self.ap, temp, seg, bounds,
-                                        workspace=self.ws)[:3]
-        return ca.capattn_bwd(q, k, v, o, lse, do, self.ap, temp, seg, bounds, workspace=self.ws)[:3]
+        """The backward of the forward just run on self.ws with the same inputs:
+        it reuses that forward's spans and visit maps."""
+        return self.ca.capattn_bwd_ex(q, k, v, o, lse, do, self.ap, temp, seg, bounds,
+                                      want_dtemp=self.dtemp, workspace=self.ws,
+                                      reuse_fwd_maps=True)[:3]
 
     def step(self, stream=None, split=False):
         d, da = self.d, self.da

@@ -86,6 +86,8 @@ enum { CAPATTN_BF16 = 0, CAPATTN_FP32 = 1 };
 /* Which pass a workspace size or visit map refers to. */
 enum { CAPATTN_PASS_FWD = 0, CAPATTN_PASS_BWD = 1 };
 enum { CAPATTN_VISIT_Q_TILES = 0, CAPATTN_VISIT_KV_TILES = 1 };
+/* flags of capattn_bwd_ex */
+enum { CAPATTN_BWD_REUSE_FWD_MAPS = 1 };
 
 /*
  * Configuration (the pages' KernelConfig: cap method and parameters, sm_scale,
@@ -181,7 +183,8 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
 
 /*
  * The backward with every optional input and output; capattn_bwd is this call
- * with dlse = dtemp = NULL, capattn_bwd_dtemp with dlse = NULL.
+ * with dlse = dtemp = NULL and flags = 0, capattn_bwd_dtemp with dlse = NULL
+ * and flags = 0.
  * dlse [B,Hq,L] float32 (device, nullable): an upstream gradient of the lse
  * that capattn_fwd returns.  Since d lse_i / d t_ij = P_ij, it adds
  * dlse_i * P_ij to dT (the same form as the z-loss term of
@@ -189,13 +192,23 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
  * gets that part of the gradient in dq, dk, dv (and dtemp).  Rows that are
  * fully masked ignore it.  dtemp [B,L] float32 (nullable) as in
  * capattn_bwd_dtemp; it needs temp (CAPATTN_ERR_INVALID_ARG otherwise).
+ * flags: 0 or CAPATTN_BWD_REUSE_FWD_MAPS (other bits: CAPATTN_ERR_INVALID_ARG).
+ * With CAPATTN_BWD_REUSE_FWD_MAPS the backward does not rebuild the per-row
+ * live spans and the block visit maps: it uses the ones capattn_fwd left in
+ * this workspace.  The caller guarantees that the last capattn_fwd on this
+ * workspace ran with the same cfg, seg and bounds (same contents), and that
+ * nothing but backward calls with those same arguments has used the workspace
+ * since (they leave the maps as they were).  A call that breaks this gets wrong gradients,
+ * not an error.  It also skips the device checks of seg and bounds, which
+ * that capattn_fwd already reported in the status word.
  * Everything else is as in capattn_bwd.
  */
 capattn_status capattn_bwd_ex(const capattn_config* cfg, const void* q, const void* k, const void* v,
                               const float* temp, const int32_t* seg, const int32_t* bounds,
                               const void* o, const float* lse, const void* dO, const float* dlse,
                               void* dq, void* dk, void* dv, float* delta, float* dtemp,
-                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                              uint32_t flags, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
 
 /*
  * Synchronises `stream`, reads and clears the device status word at the start

@@ -25,6 +25,7 @@ CAP_METHODS = {"none": 0, "tanh": 1, "soft_sign": 2, "alsc": 3}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 PASS_FWD, PASS_BWD = 0, 1
 VISIT_Q_TILES, VISIT_KV_TILES = 0, 1
+BWD_REUSE_FWD_MAPS = 1
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
                 4: "device wait timeout", 5: "workspace missing, misaligned or too small",
                 6: "invalid device data (segment ids or ranker bounds)",
@@ -75,7 +76,7 @@ def lib() -> ctypes.CDLL:
         h.capattn_bwd_dtemp.restype = ctypes.c_int
         h.capattn_bwd_dtemp.argtypes = [cfgp] + [vp] * 14 + [vp, sz, vp]
         h.capattn_bwd_ex.restype = ctypes.c_int
-        h.capattn_bwd_ex.argtypes = [cfgp] + [vp] * 15 + [vp, sz, vp]
+        h.capattn_bwd_ex.argtypes = [cfgp] + [vp] * 15 + [ctypes.c_uint32, vp, sz, vp]
         h.capattn_ranker_bounds_from_ids.restype = ctypes.c_int
         h.capattn_ranker_bounds_from_ids.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                      ctypes.c_int32, vp, vp, vp]
@@ -259,11 +260,15 @@ def capattn_bwd_dtemp(q, k, v, o, lse, do, ap: AttnParams, temp, seg=None, bound
 
 
 def capattn_bwd_ex(q, k, v, o, lse, do, ap: AttnParams, temp=None, seg=None, bounds=None, dlse=None,
-                   want_dtemp=False, workspace=None, stream=None):
+                   want_dtemp=False, workspace=None, stream=None, reuse_fwd_maps=False):
     """Backward with an optional upstream LSE gradient dlse [B,Hq,L] (fp32) and,
-    with want_dtemp, the temperature gradient.  Returns (dq, dk, dv, delta, dtemp)."""
+    with want_dtemp, the temperature gradient.  Returns (dq, dk, dv, delta, dtemp).
+    reuse_fwd_maps: use the spans and visit maps that capattn_fwd left in
+    `workspace` for the same inputs instead of rebuilding them."""
     if want_dtemp and temp is None:
         raise ValueError("the temperature gradient needs the temperature tensor")
+    if reuse_fwd_maps and workspace is None:
+        raise ValueError("reusing the forward's maps needs the forward's workspace")
     cfg = _config(q, k, ap)
     B, L, Hq = cfg.B, cfg.L, cfg.Hq
     if workspace is None:
@@ -275,7 +280,8 @@ def capattn_bwd_ex(q, k, v, o, lse, do, ap: AttnParams, temp=None, seg=None, bou
     dtemp = torch.empty(B, L, dtype=torch.float32, device=q.device) if want_dtemp else None
     st = lib().capattn_bwd_ex(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(temp), _ptr(seg),
                               _ptr(bounds), _ptr(o), _ptr(lse), _ptr(do), _ptr(dlse), _ptr(dq),
-                              _ptr(dk), _ptr(dv), _ptr(delta), _ptr(dtemp), _ptr(workspace),
+                              _ptr(dk), _ptr(dv), _ptr(delta), _ptr(dtemp),
+                              BWD_REUSE_FWD_MAPS if reuse_fwd_maps else 0, _ptr(workspace),
                               workspace.numel(), _stream(stream))
     _check(st, "capattn_bwd_ex")
     return dq, dk, dv, delta, dtemp
@@ -383,15 +389,18 @@ def capattn_profile_read(reset: bool = True) -> dict:
 
 
 class CapAttnFunction(torch.autograd.Function):
-    """Autograd wrapper: forward saves (o, lse); backward calls capattn_bwd_ex.
-    Gradients flow to q, k, v and, when it requires grad, to the temperature;
-    a loss that uses the returned lse contributes through its gradient dlse
-    (d lse_i / d t_ij = P_ij).  Segment ids and bounds are inputs only."""
+    """Autograd wrapper: forward saves (o, lse) and its workspace, whose spans
+    and visit maps the backward (capattn_bwd_ex) reuses.  Gradients flow to q,
+    k, v and, when it requires grad, to the temperature; a loss that uses the
+    returned lse contributes through its gradient dlse (d lse_i / d t_ij =
+    P_ij).  Segment ids and bounds are inputs only."""
 
     @staticmethod
     def forward(ctx, q, k, v, ap: AttnParams, temp=None, seg=None, bounds=None):
-        o, lse, _, _ = capattn_fwd(q, k, v, ap, temp, seg, bounds)
+        ws = new_workspace(_config(q, k, ap), q.device)
+        o, lse, _, _ = capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws)
         ctx.save_for_backward(q, k, v, o, lse, temp, seg, bounds)
+        ctx.ws = ws
         ctx.ap = ap
         ctx.set_materialize_grads(False)
         return o, lse
@@ -404,7 +413,8 @@ class CapAttnFunction(torch.autograd.Function):
         if dlse is not None:
             dlse = dlse.to(torch.float32).contiguous()
         dq, dk, dv, _, dtemp = capattn_bwd_ex(q, k, v, o, lse, do, ctx.ap, temp, seg, bounds,
-                                              dlse=dlse, want_dtemp=want_dtemp)
+                                              dlse=dlse, want_dtemp=want_dtemp, workspace=ctx.ws,
+                                              reuse_fwd_maps=True)
         return dq, dk, dv, None, dtemp, None, None
 
 

@@ -771,6 +771,19 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
       }
       __syncwarp();
     }
+    // Key-tile visit map for the dK/dV kernel (launched after this grid
+    // completes): query tile qt's bit in the word of every KV tile it visits.
+    // One head per (b, qt) writes; rowmap_kernel cleared the words.
+    if (h == 0) {
+      for (int w = lane; w < p.wk; w += 32) {
+        uint32_t bits = map[w];
+        while (bits) {
+          const int kt = 32 * w + __ffs(bits) - 1;
+          bits &= bits - 1u;
+          atomicOr(&p.kmap[((size_t)b * p.nk + kt) * p.wq + (qt >> 5)], 1u << (qt & 31));
+        }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (n > 0) {

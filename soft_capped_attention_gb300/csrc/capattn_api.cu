@@ -146,17 +146,18 @@ static void host_spans(const capattn_config& c, const int32_t* seg, const int32_
 
 using namespace capattn;
 
-// Backward with an optional temperature gradient (zeroed here, accumulated by
-// the dQ kernels).
+// Backward with the optional LSE gradient and temperature gradient.
 static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const void* k, const void* v,
                                const float* temp, const int32_t* seg, const int32_t* bounds,
                                const void* o, const float* lse, const void* dO, const float* dlse,
                                void* dq, void* dk, void* dv, float* delta, float* dtemp,
-                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                               uint32_t flags, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
   capattn_status st = validate(cfg);
   if (st != CAPATTN_OK) return st;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !delta)
     return CAPATTN_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)CAPATTN_BWD_REUSE_FWD_MAPS) return CAPATTN_ERR_INVALID_ARG;
   st = check_masks(*cfg, seg, bounds);
   if (st != CAPATTN_OK) return st;
   if (dtemp && !temp) return CAPATTN_ERR_INVALID_ARG;
@@ -170,7 +171,11 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
   p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
   p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
   p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta; p.dtemp = dtemp; p.dlse = dlse;
-  cudaError_t e = launch_prepass(p, true, stream);
+  // Spans and query-tile maps: from the forward (same workspace, same inputs)
+  // or rebuilt.  Key-tile map: the bf16 dQ kernel ORs it together from the
+  // query-tile maps into the words rowmap_kernel cleared; fp32 runs kmap_kernel.
+  const bool reuse = (flags & CAPATTN_BWD_REUSE_FWD_MAPS) != 0;
+  cudaError_t e = launch_prepass(p, !reuse, cfg->dtype != CAPATTN_BF16, stream);
   if (e != cudaSuccess) return cuda_status(e);
   // bf16: the dQ kernel computes delta itself; fp32: a separate pass
   if (cfg->dtype != CAPATTN_BF16) {
@@ -236,7 +241,7 @@ capattn_status capattn_fwd(const capattn_config* cfg, const void* q, const void*
   fill_params(p, *cfg, workspace);
   p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
   p.o = o; p.lse = lse; p.m = m; p.l = l;
-  cudaError_t e = launch_prepass(p, false, stream);
+  cudaError_t e = launch_prepass(p, true, false, stream);
   if (e != cudaSuccess) return cuda_status(e);
   e = (cfg->dtype == CAPATTN_BF16) ? launch_fwd_bf16(p, stream) : launch_fwd_fp32(p, stream);
   return cuda_status(e);
@@ -248,16 +253,17 @@ capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void*
                            void* dv, float* delta, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
   return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, nullptr, dq, dk, dv, delta, nullptr,
-                  workspace, workspace_bytes, stream);
+                  0u, workspace, workspace_bytes, stream);
 }
 
 capattn_status capattn_bwd_ex(const capattn_config* cfg, const void* q, const void* k, const void* v,
                               const float* temp, const int32_t* seg, const int32_t* bounds,
                               const void* o, const float* lse, const void* dO, const float* dlse,
                               void* dq, void* dk, void* dv, float* delta, float* dtemp,
-                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                              uint32_t flags, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
   return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, dlse, dq, dk, dv, delta, dtemp,
-                  workspace, workspace_bytes, stream);
+                  flags, workspace, workspace_bytes, stream);
 }
 
 capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const void* k,
@@ -268,7 +274,7 @@ capattn_status capattn_bwd_dtemp(const capattn_config* cfg, const void* q, const
                                  cudaStream_t stream) {
   if (!temp || !dtemp) return CAPATTN_ERR_INVALID_ARG;
   return bwd_impl(cfg, q, k, v, temp, seg, bounds, o, lse, dO, nullptr, dq, dk, dv, delta, dtemp,
-                  workspace, workspace_bytes, stream);
+                  0u, workspace, workspace_bytes, stream);
 }
 
 capattn_status capattn_ranker_bounds_from_ids(const int32_t* seg, int32_t B, int32_t L,
@@ -365,7 +371,7 @@ capattn_status capattn_visit_map_device(const capattn_config* cfg, const int32_t
   const size_t need = which == CAPATTN_VISIT_Q_TILES ? (size_t)p.B * p.nq * p.wk
                                                      : (size_t)p.B * p.nk * p.wq;
   if (!out || out_words < need) return CAPATTN_ERR_INVALID_ARG;
-  cudaError_t e = launch_prepass(p, true, stream);
+  cudaError_t e = launch_prepass(p, true, true, stream);
   if (e != cudaSuccess) return cuda_status(e);
   e = cudaMemcpyAsync(out, which == CAPATTN_VISIT_Q_TILES ? p.qmap : p.kmap,
                       need * sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream);

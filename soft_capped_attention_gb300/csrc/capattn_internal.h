@@ -103,7 +103,10 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 #endif
 
 // Launchers.  Each returns cudaGetLastError() after the launch.
-cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s);
+// build_rows: rowmap_kernel (spans, query-tile maps, fully covered ranges;
+// clears the key-tile map); build_kmap: kmap_kernel (key-tile map from the
+// query-tile map, whole words).
+cudaError_t launch_prepass(const Params& p, bool build_rows, bool build_kmap, cudaStream_t s);
 cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);

@@ -23,6 +23,10 @@ __device__ __forceinline__ void set_bit_range(uint32_t* bm, int a, int c) {
 // the KV tiles its rows touch, and the range of KV tiles every row covers
 // completely (the tiles in which no pair needs a mask test); a tile with rows
 // past L has no fully covered KV tile.
+// The CTA of every 32nd query tile also clears the word of the key-tile map
+// that holds the bits of query tiles [qt, qt + 32), for every KV tile: the
+// bf16 dQ kernel ORs each query tile's bits into that map later (kmap_kernel
+// instead writes whole words).
 __global__ void rowmap_kernel(Params p) {
   extern __shared__ uint32_t bm[];
   __shared__ int full_lo, full_hi;
@@ -30,6 +34,9 @@ __global__ void rowmap_kernel(Params p) {
   pdl_wait();
   const int qt = blockIdx.x, b = blockIdx.y;
   for (int w = threadIdx.x; w < p.wk; w += blockDim.x) bm[w] = 0u;
+  if ((qt & 31) == 0)
+    for (int kt = threadIdx.x; kt < p.nk; kt += blockDim.x)
+      p.kmap[((size_t)b * p.nk + kt) * p.wq + (qt >> 5)] = 0u;
   if (threadIdx.x == 0) {
     full_lo = 0;
     full_hi = p.nk;
@@ -97,12 +104,16 @@ __global__ void kmap_kernel(Params p) {
   }
 }
 
-cudaError_t launch_prepass(const Params& p, bool build_kmap, cudaStream_t s) {
+cudaError_t launch_prepass(const Params& p, bool build_rows, bool build_kmap, cudaStream_t s) {
+  if (!build_rows && !build_kmap) return cudaSuccess;
   prof_begin(CAPATTN_KERNEL_PREPASS, s);
-  prof_count(CAPATTN_KERNEL_PREPASS, build_kmap ? 2 : 1);
-  dim3 g1(p.nq, p.B);
-  cudaError_t e = launch_pdl(rowmap_kernel, g1, dim3(128), p.wk * sizeof(uint32_t), s, p);
-  if (e != cudaSuccess) return e;
+  prof_count(CAPATTN_KERNEL_PREPASS, (build_rows ? 1 : 0) + (build_kmap ? 1 : 0));
+  cudaError_t e = cudaSuccess;
+  if (build_rows) {
+    dim3 g1(p.nq, p.B);
+    e = launch_pdl(rowmap_kernel, g1, dim3(128), p.wk * sizeof(uint32_t), s, p);
+    if (e != cudaSuccess) return e;
+  }
   if (build_kmap) {
     dim3 g3(p.nk, p.B);
     e = launch_pdl(kmap_kernel, g3, dim3(32), 0, s, p);

@@ -111,6 +111,18 @@ def test_backward_workspace_holds_the_temperature_partials(lib):
     assert st == 5
 
 
+def test_backward_flags_are_checked_on_the_host(lib):
+    c = _cfg()
+    p16 = ctypes.c_void_p(16)
+    bwd = lib.capattn_workspace_bytes(ctypes.byref(c), 1)
+    # unknown flag bits: rejected before any launch (the pointers are never touched)
+    for flags in (2, 0x80000000, 3):
+        st = lib.capattn_bwd_ex(ctypes.byref(c), p16, p16, p16, None, None, None, *([p16] * 3),
+                                None, *([p16] * 4), None, flags, ctypes.c_void_p(256), bwd, None)
+        assert st == 1, flags
+    assert ca.BWD_REUSE_FWD_MAPS == 1
+
+
 def test_bounded_wait_check_rejects_bad_arguments(lib):
     # checked on the host before any CUDA call
     assert lib.capattn_check_bounded_wait(None, 1000, None) == 5

@@ -493,6 +493,56 @@ def test_autograd_passes_the_lse_gradient():
 
 
 # ---------------------------------------------------------------------------
+# Backward reusing the forward's spans and visit maps (CAPATTN_BWD_REUSE_FWD_MAPS).
+# ---------------------------------------------------------------------------
+
+REUSE_CASES = [
+    # (dtype, D, B, L, Hq, Hkv, cap, mask)
+    ("bf16", 128, 2, 700, 4, 2, "tanh", "packed"),
+    ("bf16", 128, 2, 400, 4, 2, "soft_sign", "ranker"),
+    ("bf16", 64, 1, 4200, 2, 1, "alsc", "window"),
+    ("bf16", 128, 1, 4200, 2, 2, "tanh", "causal"),
+    ("fp32", 64, 2, 300, 4, 2, "tanh", "packed"),
+]
+
+
+@pytest.mark.parametrize("case", REUSE_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_backward_reusing_the_forward_maps_is_bit_identical(case):
+    """The forward runs on a workspace whose bytes were all 0xFF (only the
+    status word zeroed), so maps that the forward failed to write would show;
+    the backward that reuses its maps, twice in a row, must give the same bits
+    as a backward that rebuilds them on a fresh workspace."""
+    dname, D, B, L, Hq, Hkv, cap, mask = case
+    dtype = torch.bfloat16 if dname == "bf16" else torch.float32
+    inp = make_case(B, L, Hq, Hkv, D, dtype, mask, True, seed=L + 5)
+    ap = params(cap, mask, 1e-3)
+    q, k, v, do = (to_dev(inp[n], dtype) for n in ("q", "k", "v", "do"))
+    temp, seg, bounds = to_dev(inp["temp"]), to_dev(inp["seg"]), to_dev(inp["bounds"])
+    cfg = ca.make_config(ap, B, L, Hq, Hkv, D, dtype)
+    ws = ca.new_workspace(cfg, q.device)
+    ws.fill_(0xFF)
+    ws[:4].zero_()
+    o, lse, _, _ = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws)
+    dlse = torch.randn(B, Hq, L, device="cuda")
+    ref = ca.capattn_bwd_ex(q, k, v, o, lse, do, ap, temp, seg, bounds, dlse=dlse, want_dtemp=True)
+    for _ in range(2):
+        got = ca.capattn_bwd_ex(q, k, v, o, lse, do, ap, temp, seg, bounds, dlse=dlse,
+                                want_dtemp=True, workspace=ws, reuse_fwd_maps=True)
+        for name, a, b in zip(("dq", "dk", "dv", "delta", "dtemp"), got, ref):
+            assert torch.equal(a, b), name
+    assert ca.capattn_device_status(ws) == (0, 0)
+
+
+def test_reuse_needs_the_forward_workspace():
+    inp = make_case(1, 200, 2, 2, 128, torch.bfloat16, "causal", False, seed=3)
+    ap = params("tanh", "causal", 0.0)
+    q, k, v, do = (to_dev(inp[n], torch.bfloat16) for n in ("q", "k", "v", "do"))
+    o, lse, _, _ = ca.capattn_fwd(q, k, v, ap)
+    with pytest.raises(ValueError):
+        ca.capattn_bwd_ex(q, k, v, o, lse, do, ap, reuse_fwd_maps=True)
+
+
+# ---------------------------------------------------------------------------
 # Ranker bounds from history / candidate segment ids (bit-exact).
 # ---------------------------------------------------------------------------
 
