@@ -84,7 +84,7 @@ enum { CAPATTN_CAP_NONE = 0, CAPATTN_CAP_TANH = 1, CAPATTN_CAP_SOFT_SIGN = 2, CA
 enum { CAPATTN_BF16 = 0, CAPATTN_FP32 = 1 };
 
 /* Which pass a workspace size or visit map refers to. */
-enum { CAPATTN_PASS_FWD = 0, CAPATTN_PASS_BWD = 1 };
+enum { CAPATTN_PASS_FWD = 0, CAPATTN_PASS_BWD = 1, CAPATTN_PASS_BWD_NO_POOL = 2 };
 enum { CAPATTN_VISIT_Q_TILES = 0, CAPATTN_VISIT_KV_TILES = 1 };
 /* flags of capattn_bwd_ex */
 enum { CAPATTN_BWD_REUSE_FWD_MAPS = 1 };
@@ -119,8 +119,15 @@ capattn_status capattn_validate_config(const capattn_config* cfg);
  * capattn_bwd / capattn_bwd_dtemp / capattn_bwd_ex (CAPATTN_PASS_BWD) for this
  * configuration; 0 if cfg is invalid.  The backward needs more: it also holds
  * the per-(head, row) partial sums of the temperature gradient (8 bytes per
- * (b, query head, row)).  A workspace sized for the backward serves both.
- * The workspace must be 256-byte aligned.  Its first word is the device status.
+ * (b, query head, row)) and, for bf16, a pool for the stored-dX backward:
+ * 32 KB per (b, query head, query tile, key tile of the tile's band), the band
+ * being the key tiles the causal / window masks of cfg leave a query tile
+ * (all of them without those masks).  The pool is left out, and that backward
+ * not used, when it would exceed 4 GiB.  CAPATTN_PASS_BWD_NO_POOL gives the
+ * backward's size without the pool (the smallest workspace a backward takes;
+ * it then recomputes dX for dQ).  A workspace sized for the backward serves
+ * both passes.  The workspace must be 256-byte aligned.  Its first word is the
+ * device status.
  */
 size_t capattn_workspace_bytes(const capattn_config* cfg, int pass);
 
@@ -154,6 +161,14 @@ capattn_status capattn_fwd(const capattn_config* cfg, const void* q, const void*
  * Outputs (device): dq [B,L,Hq,D], dk and dv [B,Lk,Hkv,D] (input element type,
  * fully overwritten); delta [B,Hq,L] float32 = rowsum(o * dO).
  * workspace: device, >= capattn_workspace_bytes(cfg, CAPATTN_PASS_BWD).
+ * bf16 takes one of two kernel sequences.  With the dX pool (the workspace
+ * holds it) and no temperature gradient: delta, then dK/dV, which also writes
+ * each visited tile's dX to the pool, then dQ as a GEMM over the stored tiles
+ * (the scores and dX are computed once per tile pair).  Otherwise (a smaller
+ * workspace, or a temperature gradient): a dQ
+ * kernel that recomputes the scores and dX and also writes delta, then dK/dV.
+ * capattn_workspace_bytes(cfg, CAPATTN_PASS_BWD_NO_POOL) is the size without the pool.
+ * The two agree to rounding (delta and dQ are summed in different orders).
  */
 capattn_status capattn_bwd(const capattn_config* cfg, const void* q, const void* k, const void* v,
                            const float* temp, const int32_t* seg, const int32_t* bounds,
@@ -215,7 +230,10 @@ capattn_status capattn_bwd_ex(const capattn_config* cfg, const void* q, const vo
  * of `workspace`.  Returns CAPATTN_OK, CAPATTN_ERR_DEVICE_TIMEOUT or
  * CAPATTN_ERR_DEVICE_DATA; *raw_bits (nullable) receives the raw bits
  * (1 = wait timeout, 2 = decreasing segment ids, 4 = ranker bounds out of range,
- * 8 = history / candidate ids not contiguous, from capattn_ranker_bounds_from_ids).
+ * 8 = history / candidate ids not contiguous, from capattn_ranker_bounds_from_ids,
+ * 16 = a visited (query tile, key tile) pair outside the causal / window band of
+ * the configuration, which the stored-dX backward has no slot for: an internal
+ * inconsistency, never expected).
  */
 capattn_status capattn_device_status(void* workspace, cudaStream_t stream, uint32_t* raw_bits);
 

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libcapattn.so")
 
 CAP_METHODS = {"none": 0, "tanh": 1, "soft_sign": 2, "alsc": 3}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
-PASS_FWD, PASS_BWD = 0, 1
+PASS_FWD, PASS_BWD, PASS_BWD_NO_POOL = 0, 1, 2
 VISIT_Q_TILES, VISIT_KV_TILES = 0, 1
 BWD_REUSE_FWD_MAPS = 1
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",

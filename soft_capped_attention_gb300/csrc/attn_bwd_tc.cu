@@ -35,6 +35,7 @@
 
 #include "cap_math.cuh"
 #include "capattn_internal.h"
+#include "row_span.h"
 #include "softmax_elem.cuh"
 #include "tc_common.cuh"
 #include "tma_maps.h"
@@ -52,6 +53,7 @@ constexpr int NSTAGE = 2;
 constexpr int NTHREADS = 320;
 template <int HD>
 constexpr int smem_bytes() { return 2 * tile_bytes<HD>() + NSTAGE * 2 * tile_bytes<HD>() + 1024; }
+
 
 // 32 fp32 values of row r as bf16 into 16-byte chunks q0 .. q0 + 3 of a
 // swizzled [128][64] bf16 slab (the layout the TMA store reads).
@@ -208,10 +210,18 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_
 // loaded while chunk C is computed; the packed P^T and dX^T of chunk C overwrite
 // its dP columns ([16 C, 16 C + 8) and [16 C + 8, 16 C + 16) of the warpgroup's
 // range) and the chunk is handed to the MMA issuer.
+// Stored-dX backward (dxo != kNoDx): after chunk C's hand-off (whose release
+// would otherwise wait for the store), the thread writes its 16 dX values of
+// the chunk, 32 bytes, at 32-byte unit dxo + 128 C of the pool.  The pool
+// keeps each tile in the layout of a 32-byte-swizzled MN-major MMA operand:
+// eight blocks of 16 query columns, each 128 key rows of 32 bytes, with the
+// two 16-byte halves of rows 4..7 of every 8 swapped (the swizzle).  A warp's
+// store then covers 1 KB of consecutive bytes.
+constexpr uint32_t kNoDx = 0xFFFFFFFFu;
 template <int METHOD, bool MASKED, bool POLY>
 __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair* cp,
                                          const int4* ci, int jrow, const Xf& xf, const TanhFold& tf,
-                                         uint32_t bar_chunk0, int lane) {
+                                         uint32_t bar_chunk0, int lane, char* pool, uint32_t dxo) {
   uint32_t da[16], db[16], pk[8], xk[8];
   tmem_ld16(dp_base, da);
   tmem_wait_ld();
@@ -227,6 +237,13 @@ __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_ba
     tc_fence_before();                                                                    \
     __syncwarp();                                                                         \
     if (lane == 0) mbar_arrive(bar_chunk0 + 8 * C);                                       \
+    if (dxo != kNoDx) {                                                                   \
+      const bool sw = (lane >> 2) & 1;                                                    \
+      st_global_v8(pool + 32 * (size_t)(dxo + 128u * C), sw ? xk[4] : xk[0],               \
+                   sw ? xk[5] : xk[1], sw ? xk[6] : xk[2], sw ? xk[7] : xk[3],            \
+                   sw ? xk[0] : xk[4], sw ? xk[1] : xk[5], sw ? xk[2] : xk[6],            \
+                   sw ? xk[3] : xk[7]);                                                   \
+    }                                                                                     \
   }
   CAPATTN_DKV_CHUNK(0, da, db)
   CAPATTN_DKV_CHUNK(1, db, da)
@@ -468,9 +485,26 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const bool have0 = nx.next(nh, nqt);
     const ColRaw r0 = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have0 && tid < 64);
     int2 fr_cur = qfull_of(have0, nqt);
+    int2 hq_cur = make_int2(g * p.G + nh, nqt);  // (query head, query tile) of the step
     const bool have1 = nx.next(nh, nqt);
     ColRaw r1 = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have1 && tid < 64);
     int2 fr_nxt = qfull_of(have1, nqt);
+    int2 hq_nxt = make_int2(g * p.G + nh, nqt);
+    // stored-dX backward: this thread's first 32-byte unit in the step's dX^T
+    // tile (1024 units per tile; at most 4 GiB of pool, so units fit 32 bits):
+    // block 4 wg (query columns 64 wg ..), key row r
+    auto dx_unit = [&](int2 hq) -> uint32_t {
+      if (p.dx_pool == nullptr) return kNoDx;
+      const int lo = p.dx_c >= 0 ? imax32(0, hq.y - p.dx_c) : 0;
+      const int d = kt - lo;
+      if (d < 0 || d >= p.dx_wmax) {
+        atomicOr(p.status, kStatusBandBit);
+        return kNoDx;
+      }
+      const uint32_t slot = ((uint32_t)(b * p.Hq + hq.x) * (uint32_t)p.nq + (uint32_t)hq.y) *
+                                (uint32_t)p.dx_wmax + (uint32_t)d;
+      return slot * 1024u + (uint32_t)(wg * 512 + r);
+    };
     put(0, r0);
     mbar_arrive(bar_cfull + 8 * (2 * wg));
     for (int step = 0; step < n; ++step) {
@@ -491,6 +525,8 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const bool have2 = nx.next(nh, nqt);
       const ColRaw r2 = load_col_raw(p, b, g * p.G + nh, nqt, my_col, have2 && tid < 64);
       const int2 fr2 = qfull_of(have2, nqt);
+      const int2 hq2 = make_int2(g * p.G + nh, nqt);
+      const uint32_t dxo = dx_unit(hq_cur);
       const bool tile_full = (kt >= fr_cur.x) && (kt < fr_cur.y);
       if (!mbar_wait_warp(my_cfull, cu & 1, p.status, &abort_flag)) {
         aborted = true;
@@ -527,19 +563,21 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int4* ci = &coli[cb][64 * wg];
       if (tile_full) {
         if (poly)
-          dkv_step<METHOD, false, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
+          dkv_step<METHOD, false, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
         else
-          dkv_step<METHOD, false, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
+          dkv_step<METHOD, false, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
       } else {
         if (poly)
-          dkv_step<METHOD, true, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
+          dkv_step<METHOD, true, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
         else
-          dkv_step<METHOD, true, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane);
+          dkv_step<METHOD, true, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
       }
       mbar_arrive(my_cfree);
       r1 = r2;
       fr_cur = fr_nxt;
       fr_nxt = fr2;
+      hq_cur = hq_nxt;
+      hq_nxt = hq2;
     }
     // ---------------------------------------------------------- epilogue
     bool have = false;
@@ -1062,17 +1100,24 @@ cudaError_t launch_bwd_hd(const Params& p, cudaStream_t s) {
   if (e == cudaSuccess) e = make_bhld_map(&mdv, p.dv, p.B, p.Lk, p.Hkv, HD, BT);
   if (e != cudaSuccess) return e;
   constexpr int SMEM_BYTES = smem_bytes<HD>();
-  // dQ first: it also computes delta, which the dK/dV kernel reads.
-  auto kdq = p.dtemp ? dq_tc_kernel<METHOD, true, HD> : dq_tc_kernel<METHOD, false, HD>;
-  e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  prof_begin(CAPATTN_KERNEL_DQ, s);
-  prof_count(CAPATTN_KERNEL_DQ, 1);
-  e = launch_pdl(kdq, dim3(p.Hq * p.B, p.nq), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdq, p);
-  if (e != cudaSuccess) return e;
-  prof_end(CAPATTN_KERNEL_DQ, s);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (p.dx_pool) {
+    // stored-dX backward: delta (and the key-tile map), then dK/dV (which also
+    // stores dX), then dQ as a GEMM over the stored tiles
+    e = launch_delta_bf16(p, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    // dQ first: it also computes delta, which the dK/dV kernel reads.
+    auto kdq = p.dtemp ? dq_tc_kernel<METHOD, true, HD> : dq_tc_kernel<METHOD, false, HD>;
+    e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    prof_begin(CAPATTN_KERNEL_DQ, s);
+    prof_count(CAPATTN_KERNEL_DQ, 1);
+    e = launch_pdl(kdq, dim3(p.Hq * p.B, p.nq), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdq, p);
+    if (e != cudaSuccess) return e;
+    prof_end(CAPATTN_KERNEL_DQ, s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   auto kdkv = dkv_tc_kernel<METHOD, HD>;
   e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -1081,7 +1126,9 @@ cudaError_t launch_bwd_hd(const Params& p, cudaStream_t s) {
   e = launch_pdl(kdkv, dim3(p.Hkv * p.B, p.nk), dim3(NTHREADS), SMEM_BYTES, s, mq, mk, mv, mdo, mdk, mdv, p);
   if (e != cudaSuccess) return e;
   prof_end(CAPATTN_KERNEL_DKV, s);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !p.dx_pool) return e;
+  return launch_dq_gemm(p, s);
 }
 
 template <int METHOD>

@@ -29,6 +29,26 @@ WorkspaceLayout workspace_layout(const capattn_config& c, int bq, int bk) {
   w.total = align256(w.qfull_off + sizeof(int2) * (size_t)c.B * nq);
   w.dtemp_part_off = w.total;
   w.total_bwd = align256(w.dtemp_part_off + sizeof(float) * 2 * (size_t)c.B * c.Hq * c.L);
+  // dX pool of the stored-dX backward (bf16 only): per (batch, query head,
+  // query tile) a slot for every key tile of the tile's causal / window band
+  // [kt_lo, kt_hi]; the data-dependent masks only ever remove tiles from it.
+  w.dx_off = w.total_dx = w.total_bwd;
+  w.dx_wmax = 0;
+  w.dx_c = c.window_len > 0 ? (c.window_len - 1 + bk - 1) / bk : -1;
+  if (c.dtype == CAPATTN_BF16 && bq == bk) {
+    int64_t wmax = 0;
+    for (int64_t qt = 0; qt < (int64_t)nq; ++qt) {
+      const int64_t lo = w.dx_c >= 0 ? (qt - w.dx_c > 0 ? qt - w.dx_c : 0) : 0;
+      const int64_t hi = c.causal ? (qt < (int64_t)nk - 1 ? qt : (int64_t)nk - 1) : (int64_t)nk - 1;
+      if (hi - lo + 1 > wmax) wmax = hi - lo + 1;
+    }
+    const double pool = (double)c.B * c.Hq * (double)nq * (double)wmax * (double)kDxTileBytes;
+    if (wmax > 0 && pool <= (double)kDxPoolMaxBytes) {
+      w.dx_wmax = (int32_t)wmax;
+      w.dx_off = (w.total_bwd + 1023) & ~size_t(1023);
+      w.total_dx = w.dx_off + (size_t)pool;
+    }
+  }
   return w;
 }
 
@@ -105,6 +125,9 @@ static void fill_params(Params& p, const capattn_config& c, void* ws) {
   p.kmap = reinterpret_cast<uint32_t*>(base + w.kmap_off);
   p.qfull = reinterpret_cast<int2*>(base + w.qfull_off);
   p.dtemp_part = reinterpret_cast<float*>(base + w.dtemp_part_off);  // backward workspace only
+  p.dx_pool = nullptr;  // set by a backward that takes the stored-dX path
+  p.dx_wmax = w.dx_wmax;
+  p.dx_c = w.dx_c;
 }
 
 static capattn_status check_ws(const capattn_config& c, void* ws, size_t bytes, int pass) {
@@ -112,6 +135,14 @@ static capattn_status check_ws(const capattn_config& c, void* ws, size_t bytes, 
   const WorkspaceLayout w = workspace_layout(c, tile_q(c), tile_kv(c));
   if (bytes < (pass == CAPATTN_PASS_BWD ? w.total_bwd : w.total)) return CAPATTN_ERR_WORKSPACE;
   return CAPATTN_OK;
+}
+
+// Whether a backward takes the stored-dX path: bf16, no temperature gradient
+// (the dQ kernel's per-row sums provide it), and a workspace that holds the pool.
+static bool use_dx_pool(const capattn_config& c, size_t bytes, bool dtemp) {
+  if (c.dtype != CAPATTN_BF16 || dtemp) return false;
+  const WorkspaceLayout w = workspace_layout(c, tile_q(c), tile_kv(c));
+  return w.dx_wmax > 0 && bytes >= w.total_dx;
 }
 
 static capattn_status cuda_status(cudaError_t e) {
@@ -171,9 +202,12 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
   p.q = q; p.k = k; p.v = v; p.temp = temp; p.seg = seg; p.bounds = bounds;
   p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
   p.dO = dO; p.dq = dq; p.dk = dk; p.dv = dv; p.delta = delta; p.dtemp = dtemp; p.dlse = dlse;
+  if (use_dx_pool(*cfg, workspace_bytes, dtemp != nullptr))
+    p.dx_pool = static_cast<char*>(workspace) + workspace_layout(*cfg, p.block_q, p.block_kv).dx_off;
   // Spans and query-tile maps: from the forward (same workspace, same inputs)
-  // or rebuilt.  Key-tile map: the bf16 dQ kernel ORs it together from the
-  // query-tile maps into the words rowmap_kernel cleared; fp32 runs kmap_kernel.
+  // or rebuilt.  Key-tile map: on the bf16 paths the dQ kernel or the delta
+  // kernel ORs it together from the query-tile maps into the words
+  // rowmap_kernel cleared; fp32 runs kmap_kernel.
   const bool reuse = (flags & CAPATTN_BWD_REUSE_FWD_MAPS) != 0;
   cudaError_t e = launch_prepass(p, !reuse, cfg->dtype != CAPATTN_BF16, stream);
   if (e != cudaSuccess) return cuda_status(e);
@@ -210,9 +244,13 @@ capattn_status capattn_validate_config(const capattn_config* cfg) { return valid
 
 size_t capattn_workspace_bytes(const capattn_config* cfg, int pass) {
   if (validate(cfg) != CAPATTN_OK) return 0;
-  if (pass != CAPATTN_PASS_FWD && pass != CAPATTN_PASS_BWD) return 0;
   const WorkspaceLayout w = workspace_layout(*cfg, tile_q(*cfg), tile_kv(*cfg));
-  return pass == CAPATTN_PASS_BWD ? w.total_bwd : w.total;
+  switch (pass) {
+    case CAPATTN_PASS_FWD: return w.total;
+    case CAPATTN_PASS_BWD: return w.total_dx;
+    case CAPATTN_PASS_BWD_NO_POOL: return w.total_bwd;
+  }
+  return 0;
 }
 
 capattn_status capattn_tile_sizes(const capattn_config* cfg, int32_t* block_q, int32_t* block_kv) {

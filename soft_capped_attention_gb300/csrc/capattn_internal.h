@@ -51,6 +51,14 @@ struct Params {
   uint32_t* qmap;         // [B, nq, wk]
   uint32_t* kmap;         // [B, nk, wq]
   int2* qfull;            // [B, nq]: KV tiles [x, y) in which every pair is live
+  // Stored-dX backward (bf16; null otherwise): the dK/dV kernel writes each
+  // step's dX^T tile (128 keys x 128 queries, bf16, key rows of 256 bytes) to
+  // slot ((b Hq + h) nq + qt) dx_wmax + (kt - kt_lo(qt)) of the pool, and the
+  // dQ GEMM kernel reads the tiles back.  kt_lo(qt) = max(0, qt - dx_c) with a
+  // sliding window (dx_c >= 0), else 0; dx_wmax = the widest band of key tiles
+  // a query tile can visit under the configuration's causal / window masks.
+  void* dx_pool;
+  int32_t dx_wmax, dx_c;
   // shapes (L query rows, Lk keys)
   int32_t B, L, Lk, Hq, Hkv, D, G;
   int32_t block_q, block_kv, nq, nk, wq, wk;
@@ -62,10 +70,16 @@ struct Params {
 };
 
 // `total` is what the forward needs; the backward also holds the per-head
-// partial sums of the temperature gradient after it (`total_bwd`).
+// partial sums of the temperature gradient after it (`total_bwd`), and the
+// stored-dX backward its dX pool after that (`total_dx`; equal to total_bwd
+// when that backward does not apply: fp32, or a pool above kDxPoolMaxBytes).
 struct WorkspaceLayout {
   size_t status_off, rowinfo_off, qmap_off, kmap_off, qfull_off, total, dtemp_part_off, total_bwd;
+  size_t dx_off, total_dx;
+  int32_t dx_wmax, dx_c;
 };
+constexpr size_t kDxTileBytes = 128 * 128 * 2;
+constexpr size_t kDxPoolMaxBytes = size_t(4) << 30;
 
 WorkspaceLayout workspace_layout(const capattn_config& c, int block_q, int block_kv);
 
@@ -108,6 +122,11 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // query-tile map, whole words).
 cudaError_t launch_prepass(const Params& p, bool build_rows, bool build_kmap, cudaStream_t s);
 cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s);
+// bf16 delta for the stored-dX backward; also ORs each query tile's bits into
+// the key-tile map (rowmap_kernel cleared it).
+cudaError_t launch_delta_bf16(const Params& p, cudaStream_t s);
+// dQ from the stored dX tiles (bf16, HD = p.D).
+cudaError_t launch_dq_gemm(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);

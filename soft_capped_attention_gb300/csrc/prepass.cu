@@ -164,6 +164,81 @@ cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// bf16, stored-dX backward: one CTA per (query tile, b, query head) of 8 warps,
+// each warp taking 16 of the tile's rows: delta[b, h, i] = sum_d O * dO in fp32.
+// The CTAs of head 0 also OR their query tile's bit into the word of every KV
+// tile the tile visits (the key-tile map for the dK/dV kernel, which runs next;
+// rowmap_kernel cleared those words).
+template <int D>
+__global__ void delta_bf16_kernel(Params p) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int VEC = D / 32;  // bf16 values per lane: 4 or 2
+  constexpr int ROWS = 16;     // rows per warp
+  const int qt = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dO);
+  float acc[ROWS];
+#pragma unroll
+  for (int k = 0; k < ROWS; ++k) {
+    const int i = qt * 128 + warp * ROWS + k;
+    acc[k] = 0.f;
+    if (i < p.L) {
+      const size_t off = (((size_t)b * p.L + i) * p.Hq + h) * D + lane * VEC;
+      if constexpr (VEC == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+        const uint2 c = *reinterpret_cast<const uint2*>(g + off);
+        const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+        const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+        const float2 c0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.x));
+        const float2 c1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.y));
+        acc[k] = fmaf(a0.x, c0.x, fmaf(a0.y, c0.y, fmaf(a1.x, c1.x, a1.y * c1.y)));
+      } else {
+        const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off);
+        const uint32_t c = *reinterpret_cast<const uint32_t*>(g + off);
+        const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+        const float2 c0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c));
+        acc[k] = fmaf(a0.x, c0.x, a0.y * c0.y);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < ROWS; ++k) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], off);
+  }
+  if (lane < ROWS) {
+    float mine = acc[0];
+#pragma unroll
+    for (int k = 1; k < ROWS; ++k) mine = lane == k ? acc[k] : mine;
+    const int i = qt * 128 + warp * ROWS + lane;
+    if (i < p.L) p.delta[((size_t)b * p.Hq + h) * p.L + i] = mine;
+  }
+  if (h == 0 && warp == 0) {
+    const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
+    for (int w = lane; w < p.wk; w += 32) {
+      uint32_t bits = map[w];
+      while (bits) {
+        const int kt = 32 * w + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        atomicOr(&p.kmap[((size_t)b * p.nk + kt) * p.wq + (qt >> 5)], 1u << (qt & 31));
+      }
+    }
+  }
+}
+
+cudaError_t launch_delta_bf16(const Params& p, cudaStream_t s) {
+  prof_begin(CAPATTN_KERNEL_DELTA, s);
+  prof_count(CAPATTN_KERNEL_DELTA, 1);
+  const dim3 grid(p.nq, p.B, p.Hq);
+  const cudaError_t e = p.D == 64 ? launch_pdl(delta_bf16_kernel<64>, grid, dim3(256), 0, s, p)
+                                  : launch_pdl(delta_bf16_kernel<128>, grid, dim3(256), 0, s, p);
+  if (e != cudaSuccess) return e;
+  prof_end(CAPATTN_KERNEL_DELTA, s);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ dtemp
 // dtemp[b, i] = sum over query heads h of the two partial sums the dQ kernels
 // left for (b, h, i), always added in the order h = 0, 1, ... (deterministic).

@@ -134,6 +134,20 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t sr
       "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// One 32-byte global store (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t e, uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+// Contiguous bulk copy global -> shared (both 16-byte aligned, bytes a multiple
+// of 16), completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -263,17 +277,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all >> 4), version 1 at bit 46, swizzle mode at bit 61
-// (2 = 128-byte swizzle).  Tiles live at 1024-byte aligned addresses, so the
+// (2 = 128-byte swizzle, 6 = 32-byte swizzle).  Tiles live at 1024-byte aligned addresses, so the
 // base-offset field stays 0.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                               uint32_t swizzle_mode = 2) {
   uint64_t d = 0;
   d |= (uint64_t)((addr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
-  d |= 2ull << 61;
+  d |= (uint64_t)swizzle_mode << 61;
   return d;
 }
+constexpr uint32_t kSwizzle32B = 6;  // swizzle-mode field value of the 32-byte swizzle
 
 // Instruction descriptor for kind::f16: bf16 A and B, fp32 accumulator,
 // M x N tile, A/B K-major (0) or MN-major (1).

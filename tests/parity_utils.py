@@ -50,9 +50,12 @@ class Guarded:
         return bool((head == GUARD_BYTE).all()) and bool((tail == GUARD_BYTE).all())
 
 
-def run_gpu(inp, ap, dtype, want_ml=False):
+def run_gpu(inp, ap, dtype, want_ml=False, pool=True):
     """Forward and backward through the binding with every output guarded; the
-    inputs must come back unchanged and no guard band may be touched."""
+    inputs must come back unchanged and no guard band may be touched.  pool:
+    a workspace that holds the dX pool (bf16: the stored-dX backward, checked
+    by its launch of the delta kernel) or one without it (the backward that
+    recomputes dX for dQ)."""
     q, k, v, do = (to_dev(inp[n], dtype) for n in ("q", "k", "v", "do"))
     temp, seg, bounds = to_dev(inp.get("temp")), to_dev(inp.get("seg")), to_dev(inp.get("bounds"))
     inputs = [t for t in (q, k, v, do, temp, seg, bounds) if t is not None]
@@ -60,7 +63,8 @@ def run_gpu(inp, ap, dtype, want_ml=False):
     B, L, Hq, D = q.shape
     Lk, Hkv = k.shape[1], k.shape[2]
     cfg = ca.make_config(ap, B, L, Hq, Hkv, D, dtype, Lk=Lk)
-    ws_bytes = max(ca.workspace_bytes(cfg, ca.PASS_FWD), ca.workspace_bytes(cfg, ca.PASS_BWD))
+    ws_bytes = max(ca.workspace_bytes(cfg, ca.PASS_FWD),
+                   ca.workspace_bytes(cfg, ca.PASS_BWD if pool else ca.PASS_BWD_NO_POOL))
     ws_g = Guarded((ws_bytes,), torch.uint8)
     ws_g.tensor.zero_()
     assert ws_g.tensor.data_ptr() % 256 == 0
@@ -72,8 +76,16 @@ def run_gpu(inp, ap, dtype, want_ml=False):
     t = {n: (None if x is None else x.tensor) for n, x in g.items()}
     o, lse, m, l = ca.capattn_fwd(q, k, v, ap, temp, seg, bounds, workspace=ws_g.tensor,
                                   out=(t["O"], t["LSE"], t["m"], t["l"]))
+    ca.capattn_profile_enable(True)
+    ca.capattn_profile_select([])  # launch counts only
+    ca.capattn_profile_read(reset=True)
     dq, dk, dv, delta = ca.capattn_bwd(q, k, v, o, lse, do, ap, temp, seg, bounds, workspace=ws_g.tensor,
                                        out=(t["dQ"], t["dK"], t["dV"], t["delta"]))
+    launches = ca.capattn_profile_read(reset=True)
+    ca.capattn_profile_enable(False)
+    if dtype == torch.bfloat16:
+        stored_dx = ca.workspace_bytes(cfg, ca.PASS_BWD) > ca.workspace_bytes(cfg, ca.PASS_BWD_NO_POOL)
+        assert launches["delta"][1] == (1 if (pool and stored_dx) else 0), launches
     st, bits = ca.capattn_device_status(ws_g.tensor)
     assert st == 0, f"device status {st} bits {bits}"
     torch.cuda.synchronize()

@@ -45,7 +45,8 @@ def _cfg(**kw):
     ap = ca.AttnParams(sm_scale=0.1, cap_method=base.pop("cap_method", "tanh"),
                        cap=base.pop("cap", 5.0), causal=base.pop("causal", True),
                        window_len=base.pop("window_len", 0))
-    return ca.make_config(ap, **base)
+    Lk = base.pop("Lk", 0)
+    return ca.make_config(ap, **base, Lk=Lk)
 
 
 def test_validation_codes(lib):
@@ -101,14 +102,62 @@ def test_compute_calls_reject_bad_arguments_before_launch(lib):
 def test_backward_workspace_holds_the_temperature_partials(lib):
     c = _cfg(B=3, L=300, Hq=4, Hkv=2)
     fwd = lib.capattn_workspace_bytes(ctypes.byref(c), 0)
-    bwd = lib.capattn_workspace_bytes(ctypes.byref(c), 1)
+    no_pool = lib.capattn_workspace_bytes(ctypes.byref(c), 2)
     extra = 8 * 3 * 4 * 300  # two float partial sums per (b, query head, row)
-    assert bwd == fwd + ((extra + 255) // 256) * 256
+    assert no_pool == fwd + ((extra + 255) // 256) * 256
     # a forward-sized workspace is refused by the backward before any launch
     p16 = ctypes.c_void_p(16)
     st = lib.capattn_bwd(ctypes.byref(c), p16, p16, p16, None, None, None, *([p16] * 7),
                          ctypes.c_void_p(256), fwd, None)
     assert st == 5
+    assert lib.capattn_workspace_bytes(ctypes.byref(c), 3) == 0
+
+
+def _band_width(L, Lk, causal, window, tile=128):
+    """Widest set of key tiles that some (query, key) pair of a query tile may
+    see under the causal / window masks alone, by brute force over positions."""
+    nq, nk = -(-L // tile), -(-Lk // tile)
+    widest = 0
+    for qt in range(nq):
+        i = np.arange(qt * tile, min(L, qt * tile + tile))[:, None]
+        seen = 0
+        for kt in range(nk):
+            j = np.arange(kt * tile, min(Lk, kt * tile + tile))[None, :]
+            ok = np.ones((i.size, j.size), bool)
+            if causal:
+                ok &= j <= i
+            if window:
+                ok &= j > i - window
+            seen += bool(ok.any())
+        widest = max(widest, seen)
+    return widest
+
+
+@pytest.mark.parametrize("L,Lk,causal,window", [
+    (300, 0, True, 0), (1000, 0, True, 300), (1000, 0, False, 300), (1000, 0, True, 129),
+    (700, 0, True, 1), (300, 1000, False, 0), (2048, 0, True, 0), (640, 0, False, 0)])
+def test_dx_pool_size_is_the_band_of_the_masks(lib, L, Lk, causal, window):
+    B, Hq = 2, 4
+    c = _cfg(B=B, L=L, Lk=Lk, Hq=Hq, Hkv=2, causal=causal, window_len=window)
+    no_pool = lib.capattn_workspace_bytes(ctypes.byref(c), 2)
+    bwd = lib.capattn_workspace_bytes(ctypes.byref(c), 1)
+    nq = -(-L // 128)
+    pool = B * Hq * nq * _band_width(L, Lk or L, causal, window) * 128 * 128 * 2
+    assert bwd == ((no_pool + 1023) // 1024) * 1024 + pool
+
+
+def test_dx_pool_is_left_out_for_fp32_and_above_4_gib(lib):
+    c = _cfg(dtype=torch.float32, D=64)
+    assert lib.capattn_workspace_bytes(ctypes.byref(c), 1) == lib.capattn_workspace_bytes(ctypes.byref(c), 2)
+    # full attention, 128 x 128 tiles: 64 * 128 * 128 tiles of 32 KB = 32 GiB
+    c = _cfg(B=64, L=16384, Hq=1, Hkv=1, causal=False)
+    assert lib.capattn_workspace_bytes(ctypes.byref(c), 1) == lib.capattn_workspace_bytes(ctypes.byref(c), 2)
+    # just under the cap: 4 GiB exactly is kept
+    c = _cfg(B=8, L=16384, Hq=1, Hkv=1, causal=False)
+    pool = 8 * 128 * 128 * 32768
+    assert pool == 4 << 30
+    no_pool = lib.capattn_workspace_bytes(ctypes.byref(c), 2)
+    assert lib.capattn_workspace_bytes(ctypes.byref(c), 1) == ((no_pool + 1023) // 1024) * 1024 + pool
 
 
 def test_backward_flags_are_checked_on_the_host(lib):
