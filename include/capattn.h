@@ -123,7 +123,7 @@ capattn_status capattn_validate_config(const capattn_config* cfg);
  * 32 KB per (b, query head, query tile, key tile of the tile's band), the band
  * being the key tiles the causal / window masks of cfg leave a query tile
  * (all of them without those masks).  The pool is left out, and that backward
- * not used, when it would exceed 4 GiB.  CAPATTN_PASS_BWD_NO_POOL gives the
+ * not used, when it would exceed 16 GiB.  CAPATTN_PASS_BWD_NO_POOL gives the
  * backward's size without the pool (the smallest workspace a backward takes;
  * it then recomputes dX for dQ).  A workspace sized for the backward serves
  * both passes.  The workspace must be 256-byte aligned.  Its first word is the

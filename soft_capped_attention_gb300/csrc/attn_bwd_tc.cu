@@ -218,7 +218,7 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_
 // two 16-byte halves of rows 4..7 of every 8 swapped (the swizzle).  A warp's
 // store then covers 1 KB of consecutive bytes.
 constexpr uint32_t kNoDx = 0xFFFFFFFFu;
-template <int METHOD, bool MASKED, bool POLY>
+template <int METHOD, bool MASKED, bool POLY, bool DX>
 __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair* cp,
                                          const int4* ci, int jrow, const Xf& xf, const TanhFold& tf,
                                          uint32_t bar_chunk0, int lane, char* pool, uint32_t dxo) {
@@ -237,7 +237,7 @@ __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_ba
     tc_fence_before();                                                                    \
     __syncwarp();                                                                         \
     if (lane == 0) mbar_arrive(bar_chunk0 + 8 * C);                                       \
-    if (dxo != kNoDx) {                                                                   \
+    if (DX && dxo != kNoDx) {                                                             \
       const bool sw = (lane >> 2) & 1;                                                    \
       st_global_v8(pool + 32 * (size_t)(dxo + 128u * C), sw ? xk[4] : xk[0],               \
                    sw ? xk[5] : xk[1], sw ? xk[6] : xk[2], sw ? xk[7] : xk[3],            \
@@ -264,7 +264,7 @@ __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_ba
 // j + 1 while step j's elementwise work runs), and packs P^T / dX^T over its dP^T
 // columns chunk by chunk; dP^T of step j + 1 is issued once every chunk's MMAs
 // are.
-template <int METHOD, int HD>
+template <int METHOD, int HD, bool DX>
 __global__ void __launch_bounds__(NTHREADS, 1)
 dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -494,7 +494,7 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     // tile (1024 units per tile; at most 4 GiB of pool, so units fit 32 bits):
     // block 4 wg (query columns 64 wg ..), key row r
     auto dx_unit = [&](int2 hq) -> uint32_t {
-      if (p.dx_pool == nullptr) return kNoDx;
+      if (!DX) return kNoDx;
       const int lo = p.dx_c >= 0 ? imax32(0, hq.y - p.dx_c) : 0;
       const int d = kt - lo;
       if (d < 0 || d >= p.dx_wmax) {
@@ -563,14 +563,14 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int4* ci = &coli[cb][64 * wg];
       if (tile_full) {
         if (poly)
-          dkv_step<METHOD, false, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, false, true, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
         else
-          dkv_step<METHOD, false, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, false, false, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
       } else {
         if (poly)
-          dkv_step<METHOD, true, true>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, true, true, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
         else
-          dkv_step<METHOD, true, false>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, true, false, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
       }
       mbar_arrive(my_cfree);
       r1 = r2;
@@ -1118,7 +1118,7 @@ cudaError_t launch_bwd_hd(const Params& p, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kdkv = dkv_tc_kernel<METHOD, HD>;
+  auto kdkv = p.dx_pool ? dkv_tc_kernel<METHOD, HD, true> : dkv_tc_kernel<METHOD, HD, false>;
   e = cudaFuncSetAttribute(kdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   prof_begin(CAPATTN_KERNEL_DKV, s);

@@ -59,6 +59,7 @@ struct Params {
   // a query tile can visit under the configuration's causal / window masks.
   void* dx_pool;
   int32_t dx_wmax, dx_c;
+  uint32_t* dq_work;      // work counter of the persistent dQ GEMM (zeroed by the delta kernel)
   // shapes (L query rows, Lk keys)
   int32_t B, L, Lk, Hq, Hkv, D, G;
   int32_t block_q, block_kv, nq, nk, wq, wk;
@@ -73,13 +74,14 @@ struct Params {
 // partial sums of the temperature gradient after it (`total_bwd`), and the
 // stored-dX backward its dX pool after that (`total_dx`; equal to total_bwd
 // when that backward does not apply: fp32, or a pool above kDxPoolMaxBytes).
+// Slot and 32-byte-unit indices of the pool fit 32 bits up to 128 GiB.
 struct WorkspaceLayout {
   size_t status_off, rowinfo_off, qmap_off, kmap_off, qfull_off, total, dtemp_part_off, total_bwd;
   size_t dx_off, total_dx;
   int32_t dx_wmax, dx_c;
 };
 constexpr size_t kDxTileBytes = 128 * 128 * 2;
-constexpr size_t kDxPoolMaxBytes = size_t(4) << 30;
+constexpr size_t kDxPoolMaxBytes = size_t(16) << 30;
 
 WorkspaceLayout workspace_layout(const capattn_config& c, int block_q, int block_kv);
 

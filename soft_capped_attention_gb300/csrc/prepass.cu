@@ -168,7 +168,8 @@ cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s) {
 // each warp taking 16 of the tile's rows: delta[b, h, i] = sum_d O * dO in fp32.
 // The CTAs of head 0 also OR their query tile's bit into the word of every KV
 // tile the tile visits (the key-tile map for the dK/dV kernel, which runs next;
-// rowmap_kernel cleared those words).
+// rowmap_kernel cleared those words), and the first thread zeroes the work
+// counter of the dQ GEMM that follows.
 template <int D>
 __global__ void delta_bf16_kernel(Params p) {
   pdl_trigger();
@@ -177,6 +178,7 @@ __global__ void delta_bf16_kernel(Params p) {
   constexpr int ROWS = 16;     // rows per warp
   const int qt = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((qt | b | h | threadIdx.x) == 0) *p.dq_work = 0u;  // the dQ GEMM's work counter
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o);
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dO);
   float acc[ROWS];

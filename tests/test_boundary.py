@@ -146,16 +146,16 @@ def test_dx_pool_size_is_the_band_of_the_masks(lib, L, Lk, causal, window):
     assert bwd == ((no_pool + 1023) // 1024) * 1024 + pool
 
 
-def test_dx_pool_is_left_out_for_fp32_and_above_4_gib(lib):
+def test_dx_pool_is_left_out_for_fp32_and_above_16_gib(lib):
     c = _cfg(dtype=torch.float32, D=64)
     assert lib.capattn_workspace_bytes(ctypes.byref(c), 1) == lib.capattn_workspace_bytes(ctypes.byref(c), 2)
     # full attention, 128 x 128 tiles: 64 * 128 * 128 tiles of 32 KB = 32 GiB
     c = _cfg(B=64, L=16384, Hq=1, Hkv=1, causal=False)
     assert lib.capattn_workspace_bytes(ctypes.byref(c), 1) == lib.capattn_workspace_bytes(ctypes.byref(c), 2)
-    # just under the cap: 4 GiB exactly is kept
-    c = _cfg(B=8, L=16384, Hq=1, Hkv=1, causal=False)
-    pool = 8 * 128 * 128 * 32768
-    assert pool == 4 << 30
+    # at the cap: 16 GiB exactly is kept
+    c = _cfg(B=32, L=16384, Hq=1, Hkv=1, causal=False)
+    pool = 32 * 128 * 128 * 32768
+    assert pool == 16 << 30
     no_pool = lib.capattn_workspace_bytes(ctypes.byref(c), 2)
     assert lib.capattn_workspace_bytes(ctypes.byref(c), 1) == ((no_pool + 1023) // 1024) * 1024 + pool
 
