@@ -164,8 +164,11 @@ cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// bf16, stored-dX backward: one CTA per (query tile, b, query head) of 8 warps,
-// each warp taking 16 of the tile's rows: delta[b, h, i] = sum_d O * dO in fp32.
+// bf16, stored-dX backward: one CTA per (query tile, b, query head) of 8 warps:
+// delta[b, h, i] = sum_d O * dO in fp32.  A row's D values are read by D / 8
+// lanes, 16 bytes each, so a warp covers 32 / (D / 8) rows per load and the CTA
+// its 128 rows in 128 / (8 * that) rounds; every round's loads are issued
+// before any arithmetic (rows past L read row L - 1 and are dropped).
 // The CTAs of head 0 also OR their query tile's bit into the word of every KV
 // tile the tile visits (the key-tile map for the dK/dV kernel, which runs next;
 // rowmap_kernel cleared those words), and the first thread zeroes the work
@@ -174,48 +177,37 @@ template <int D>
 __global__ void delta_bf16_kernel(Params p) {
   pdl_trigger();
   pdl_wait();
-  constexpr int VEC = D / 32;  // bf16 values per lane: 4 or 2
-  constexpr int ROWS = 16;     // rows per warp
+  constexpr int LPR = D / 8;            // lanes per row
+  constexpr int RPW = 32 / LPR;         // rows per warp and round
+  constexpr int ROUNDS = 128 / (8 * RPW);
   const int qt = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((qt | b | h | threadIdx.x) == 0) *p.dq_work = 0u;  // the dQ GEMM's work counter
-  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o);
-  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dO);
-  float acc[ROWS];
+  const uint4* o = static_cast<const uint4*>(p.o);
+  const uint4* g = static_cast<const uint4*>(p.dO);
+  const int sub = lane / LPR, part = lane % LPR;
+  uint4 a[ROUNDS], c[ROUNDS];
 #pragma unroll
-  for (int k = 0; k < ROWS; ++k) {
-    const int i = qt * 128 + warp * ROWS + k;
-    acc[k] = 0.f;
-    if (i < p.L) {
-      const size_t off = (((size_t)b * p.L + i) * p.Hq + h) * D + lane * VEC;
-      if constexpr (VEC == 4) {
-        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-        const uint2 c = *reinterpret_cast<const uint2*>(g + off);
-        const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
-        const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
-        const float2 c0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.x));
-        const float2 c1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c.y));
-        acc[k] = fmaf(a0.x, c0.x, fmaf(a0.y, c0.y, fmaf(a1.x, c1.x, a1.y * c1.y)));
-      } else {
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off);
-        const uint32_t c = *reinterpret_cast<const uint32_t*>(g + off);
-        const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
-        const float2 c0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c));
-        acc[k] = fmaf(a0.x, c0.x, a0.y * c0.y);
-      }
+  for (int k = 0; k < ROUNDS; ++k) {
+    const int i = imin32(qt * 128 + (k * 8 + warp) * RPW + sub, p.L - 1);
+    const size_t off = (((size_t)b * p.L + i) * p.Hq + h) * LPR + part;
+    a[k] = o[off];
+    c[k] = g[off];
+  }
+#pragma unroll
+  for (int k = 0; k < ROUNDS; ++k) {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&c[k]);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 u = __bfloat1622float2(x[e]), v = __bfloat1622float2(y[e]);
+      acc = fmaf(u.x, v.x, fmaf(u.y, v.y, acc));
     }
-  }
 #pragma unroll
-  for (int k = 0; k < ROWS; ++k) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], off);
-  }
-  if (lane < ROWS) {
-    float mine = acc[0];
-#pragma unroll
-    for (int k = 1; k < ROWS; ++k) mine = lane == k ? acc[k] : mine;
-    const int i = qt * 128 + warp * ROWS + lane;
-    if (i < p.L) p.delta[((size_t)b * p.Hq + h) * p.L + i] = mine;
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    const int i = qt * 128 + (k * 8 + warp) * RPW + sub;
+    if (part == 0 && i < p.L) p.delta[((size_t)b * p.Hq + h) * p.L + i] = acc;
   }
   if (h == 0 && warp == 0) {
     const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
