@@ -540,15 +540,19 @@ struct FwdTcLaunch {
 
 }  // namespace
 
-// Two tiles per CTA (this file) or one tile per CTA with two CTAs per SM
-// (attn_fwd1_tc.cu), chosen from the configuration alone.  Measured on GB300:
-// the one-tile kernel wins where a CTA visits few key tiles among many CTAs
-// (a sliding window: -9 %; packed documents: -9 %), and loses where the loops
-// are long (causal over 2048 keys: +4 %; ranker histories: +4 %; 8192 unmasked
-// keys: +13 %) because it can only single-buffer K and V.
+// Three forward kernels, chosen from the configuration alone by what measured
+// fastest on GB300 (forward times against this file's two-tile kernel):
+//  * a sliding window or segment ids: one tile per CTA, two CTAs per SM
+//    (attn_fwd1_tc.cu; -9 % on a 1024-key window and on packed documents,
+//    where a CTA visits few key tiles and the CTAs' fixed costs dominate);
+//  * ranker bounds: this file's two tiles per CTA (the others were +4 % and
+//    +12 % on ranker histories);
+//  * otherwise (causal or unmasked): one tile per CTA with two score buffers
+//    (attn_fwd2_tc.cu; -3 % causal over 2048 keys, -7 % on 8192 unmasked keys).
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s) {
   if (p.window_len > 0 || p.seg != nullptr) return launch_fwd1_bf16(p, s);
-  return dispatch_cap<FwdTcLaunch>(p.cap.method, p, s);
+  if (p.bounds != nullptr) return dispatch_cap<FwdTcLaunch>(p.cap.method, p, s);
+  return launch_fwd2_bf16(p, s);
 }
 
 }  // namespace capattn

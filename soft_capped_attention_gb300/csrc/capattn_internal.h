@@ -133,6 +133,7 @@ cudaError_t launch_fwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd1_bf16(const Params& p, cudaStream_t s);  // one query tile per CTA
+cudaError_t launch_fwd2_bf16(const Params& p, cudaStream_t s);  // one tile, two score buffers
 cudaError_t launch_bwd_bf16(const Params& p, cudaStream_t s);
 cudaError_t launch_dtemp_reduce(const Params& p, cudaStream_t s);
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, int ctas, cudaStream_t s);

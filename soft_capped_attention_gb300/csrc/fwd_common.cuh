@@ -1,5 +1,6 @@
-// Pieces shared by the two bf16 forward kernels (attn_fwd_tc.cu: two query
-// tiles per CTA; attn_fwd1_tc.cu: one query tile per CTA, two CTAs per SM):
+// Pieces shared by the bf16 forward kernels (attn_fwd_tc.cu: two query tiles
+// per CTA; attn_fwd1_tc.cu: one query tile per CTA, two CTAs per SM;
+// attn_fwd2_tc.cu: one query tile per CTA with two score buffers):
 // tile constants, the score and PV MMA sequences, and the softmax's per-chunk
 // arithmetic (triton_kernels.py make_triton_forward_kernel's cap, temperature,
 // mask and exp2-domain softmax).
