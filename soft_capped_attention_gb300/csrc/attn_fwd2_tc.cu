@@ -273,13 +273,14 @@ fwd2_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
       tc_fence_after();
       const bool full = (ri.x <= k0) && (ri.y >= k0 + BN);
       const bool warp_partial = __any_sync(0xFFFFFFFFu, !full);
+      // the quarter-row's 32 raw scores, read once for both passes
+      uint32_t v[32];
+      tmem_ld32(sb, v);
+      tmem_wait_ld();
       float alpha = 1.f;
       bool poly = false;
       if (!fixed_ref) {
         // ---- pass 1: range of the quarter-row's live raw scores
-        uint32_t v[32];
-        tmem_ld32(sb, v);
-        tmem_wait_ld();
         float vmax, vmin;
         if (!full)
           row_range<true, 32>(v, c0, ri, vmax, vmin);
@@ -348,30 +349,17 @@ fwd2_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
       const bool fast = full && any;
       float psum = 0.f;
       {
-        uint32_t va[16], vb[16], pk[8];
-        tmem_ld16(sb, va);
-        tmem_wait_ld();
-        tmem_ld16(sb + 16, vb);
+        uint32_t pk[16];
         // (warp-wide vote, taken only in steps with partially masked rows)
-        if (warp_partial && sub_dead(ri, c0)) {
+        if (warp_partial && quarter_dead(ri, c0)) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pk[e] = 0u;
+          for (int e = 0; e < 16; ++e) pk[e] = 0u;
         } else {
-          if (fixed_ref) poly = sub_poly<METHOD>(va, tf, xf);
-          psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, tf, rmul, addm, c0, ri, any);
+          if (fixed_ref) poly = quarter_poly<METHOD>(v, tf, xf);
+          psum = p_dispatch32<METHOD>(fast, poly, v, pk, xf, tf, rmul, addm, c0, ri, any);
         }
         __syncwarp();
-        tmem_st8(sb, pk);
-        tmem_wait_ld();
-        if (warp_partial && sub_dead(ri, c0 + 16)) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) pk[e] = 0u;
-        } else {
-          if (fixed_ref) poly = sub_poly<METHOD>(vb, tf, xf);
-          psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, tf, rmul, addm, c0 + 16, ri, any);
-        }
-        __syncwarp();
-        tmem_st8(sb + 8, pk);
+        tmem_st16(sb, pk);
       }
       lsum = lsum * alpha + psum;
       tmem_wait_st();

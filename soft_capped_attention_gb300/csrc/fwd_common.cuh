@@ -188,5 +188,55 @@ __device__ __forceinline__ float p_dispatch(bool full_any, bool poly, const uint
   return p_chunk<METHOD, true, 8>(v, pk, xf, mul, addm, live);
 }
 
+// Live-column bits of the 32 columns j0 .. j0 + 31 of a row (bit k: column
+// j0 + k is in [ri.x, ri.y) or equals ri.z).
+__device__ __forceinline__ uint32_t live_bits32(int4 ri, int j0) {
+  const int lo = min(max(ri.x - j0, 0), 32);
+  const int hi = min(max(ri.y - j0, 0), 32);
+  const uint32_t below_hi = hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u);
+  const uint32_t below_lo = lo >= 32 ? 0xFFFFFFFFu : ((1u << lo) - 1u);
+  uint32_t bits = hi > lo ? (below_hi & ~below_lo) : 0u;
+  const uint32_t ez = (uint32_t)(ri.z - j0);
+  if (ez < 32u) bits |= 1u << ez;
+  return bits;
+}
+
+// sub_dead and sub_poly over 32 columns.
+__device__ __forceinline__ bool quarter_dead(int4 ri, int j0) {
+  const bool live = (ri.x < j0 + 32 && ri.y > j0 && ri.x < ri.y) || (ri.z >= j0 && ri.z < j0 + 32);
+  return __all_sync(0xFFFFFFFFu, !live);
+}
+template <int METHOD>
+__device__ __forceinline__ bool quarter_poly(const uint32_t (&v)[32], const TanhFold& tf, const Xf& xf) {
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      a0 = fmax3_abs(a0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+      a1 = fmax3_abs(a1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+    }
+    return __all_sync(0xFFFFFFFFu, tf.ok && fmaxf(a0, a1) * fabsf(xf.in) <= kTanhPolyMaxU);
+  }
+  return false;
+}
+
+// 32 columns of P (16 packed pairs): masked or not, FMA-pipe tanh or not.
+template <int METHOD>
+__device__ __forceinline__ float p_dispatch32(bool full_any, bool poly, const uint32_t (&v)[32],
+                                             uint32_t (&pk)[16], const Xf& xf, const TanhFold& tf,
+                                             float mul, float addm, int j0, int4 ri, bool any) {
+  if (full_any) {
+    if constexpr (METHOD == CAPATTN_CAP_TANH) {
+      if (poly) return p_chunk_tanh_fold<false, 16>(v, pk, tf, addm, 0xFFFFFFFFu);
+    }
+    return p_chunk<METHOD, false, 16>(v, pk, xf, mul, addm, 0xFFFFFFFFu);
+  }
+  const uint32_t live = any ? live_bits32(ri, j0) : 0u;
+  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+    if (poly) return p_chunk_tanh_fold<true, 16>(v, pk, tf, addm, live);
+  }
+  return p_chunk<METHOD, true, 16>(v, pk, xf, mul, addm, live);
+}
+
 }  // namespace fwdtc
 }  // namespace capattn
