@@ -368,10 +368,13 @@ fwd1_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
       else
         aborted = true;
     }
+    // Every MMA (and so the Q load) has completed before O is read and before
+    // Q's shared memory takes O.
     bool have_o = false;
-    if (cnt > 0 && !aborted) {
-      have_o = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
+    if (n > 0 && !aborted) {
+      const bool done = mbar_wait_warp(bar_final, 0, p.status, &abort_flag);
       tc_fence_after();
+      have_o = done && cnt > 0;
     }
     const bool live = l_row > 0.f;
     const float inv = live ? 1.f / l_row : 0.f;

@@ -495,6 +495,27 @@ def test_autograd_passes_the_lse_gradient():
 
 
 # ---------------------------------------------------------------------------
+# Ranker bounds that leave whole query tiles without a live key next to live
+# ones (the two-tile forward then has an idle tile in a CTA with work): O and
+# the gradients of the dead rows must be exactly zero, the rest match.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bounds_row", [(0, 60, 60, 100), (0, 200, 200, 250), (0, 0, 0, 90)])
+def test_ranker_with_dead_query_tiles(bounds_row):
+    B, L = 2, 700
+    inp = make_case(B, L, 4, 2, 128, torch.bfloat16, "ranker", False, seed=sum(bounds_row))
+    inp["bounds"] = np.array([bounds_row, (0, 300, 300, 380)], np.int32)
+    ap = params("alsc", "ranker", 0.0)
+    for _ in range(3):
+        got = run_gpu(inp, ap, torch.bfloat16)
+        ref = run_oracle(inp, ap)
+        compare(got, ref, torch.bfloat16)
+        dead = np.isneginf(ref["LSE"])  # [B, Hq, L]
+        o = np.transpose(got["O"], (0, 2, 1, 3))[dead]
+        assert dead.any() and np.all(o == 0)
+
+
+# ---------------------------------------------------------------------------
 # Backward reusing the forward's spans and visit maps (CAPATTN_BWD_REUSE_FWD_MAPS).
 # ---------------------------------------------------------------------------
 
