@@ -544,18 +544,34 @@ struct FwdTcLaunch {
 
 }  // namespace
 
-// Three forward kernels, chosen from the configuration alone by what measured
+// Whether every row can use the fixed reference (the persistent forward's
+// only mode): a cap, no temperature, m and l not requested, and the capped
+// logits' window (the same for every row without a temperature) within
+// kSpanMax, checked here with a margin so that the device's fp32 test agrees.
+static bool fixed_reference_everywhere(const Params& p) {
+  if (p.cap.method == CAPATTN_CAP_NONE || p.m != nullptr || p.l != nullptr || p.temp != nullptr)
+    return false;
+  const double l2e = 1.4426950408889634;
+  const double span = p.cap.method == CAPATTN_CAP_ALSC ? fabs((double)p.cap.alsc_out * l2e)
+                                                       : 2.0 * fabs((double)p.cap.cap * l2e);
+  return span <= 0.999 * (double)kSpanMax;
+}
+
+// Four forward kernels, chosen from the configuration alone by what measured
 // fastest on GB300 (forward times against this file's two-tile kernel):
 //  * a sliding window or segment ids: one tile per CTA, two CTAs per SM
 //    (attn_fwd1_tc.cu; -9 % on a 1024-key window and on packed documents,
 //    where a CTA visits few key tiles and the CTAs' fixed costs dominate);
 //  * ranker bounds: this file's two tiles per CTA (the others were +4 % and
 //    +12 % on ranker histories);
+//  * causal or unmasked with the fixed reference everywhere: the persistent
+//    kernel (attn_fwd3_tc.cu);
 //  * otherwise (causal or unmasked): one tile per CTA with two score buffers
 //    (attn_fwd2_tc.cu; -3 % causal over 2048 keys, -7 % on 8192 unmasked keys).
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s) {
   if (p.window_len > 0 || p.seg != nullptr) return launch_fwd1_bf16(p, s);
   if (p.bounds != nullptr) return dispatch_cap<FwdTcLaunch>(p.cap.method, p, s);
+  if (fixed_reference_everywhere(p)) return launch_fwd3_bf16(p, s);
   return launch_fwd2_bf16(p, s);
 }
 

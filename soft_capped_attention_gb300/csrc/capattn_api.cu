@@ -121,6 +121,7 @@ static void fill_params(Params& p, const capattn_config& c, void* ws) {
   char* base = static_cast<char*>(ws);
   p.status = reinterpret_cast<uint32_t*>(base + w.status_off);
   p.dq_work = reinterpret_cast<uint32_t*>(base + w.status_off + 128);  // in the status block
+  p.fwd_work = reinterpret_cast<uint32_t*>(base + w.status_off + 192);
   p.rowinfo = reinterpret_cast<int4*>(base + w.rowinfo_off);
   p.qmap = reinterpret_cast<uint32_t*>(base + w.qmap_off);
   p.kmap = reinterpret_cast<uint32_t*>(base + w.kmap_off);

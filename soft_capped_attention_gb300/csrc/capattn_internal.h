@@ -60,6 +60,7 @@ struct Params {
   void* dx_pool;
   int32_t dx_wmax, dx_c;
   uint32_t* dq_work;      // work counter of the persistent dQ GEMM (zeroed by the delta kernel)
+  uint32_t* fwd_work;     // work counter of the persistent forward (zeroed by rowmap_kernel)
   // shapes (L query rows, Lk keys)
   int32_t B, L, Lk, Hq, Hkv, D, G;
   int32_t block_q, block_kv, nq, nk, wq, wk;
@@ -134,6 +135,7 @@ cudaError_t launch_bwd_fp32(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s);
 cudaError_t launch_fwd1_bf16(const Params& p, cudaStream_t s);  // one query tile per CTA
 cudaError_t launch_fwd2_bf16(const Params& p, cudaStream_t s);  // one tile, two score buffers
+cudaError_t launch_fwd3_bf16(const Params& p, cudaStream_t s);  // persistent, fixed reference
 cudaError_t launch_bwd_bf16(const Params& p, cudaStream_t s);
 cudaError_t launch_dtemp_reduce(const Params& p, cudaStream_t s);
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, int ctas, cudaStream_t s);

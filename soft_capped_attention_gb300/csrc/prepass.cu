@@ -23,6 +23,7 @@ __device__ __forceinline__ void set_bit_range(uint32_t* bm, int a, int c) {
 // the KV tiles its rows touch, and the range of KV tiles every row covers
 // completely (the tiles in which no pair needs a mask test); a tile with rows
 // past L has no fully covered KV tile.
+// The first CTA zeroes the work counter of the persistent forward.
 // The CTA of every 32nd query tile also clears the word of the key-tile map
 // that holds the bits of query tiles [qt, qt + 32), for every KV tile: the
 // bf16 dQ kernel ORs each query tile's bits into that map later (kmap_kernel
@@ -33,6 +34,7 @@ __global__ void rowmap_kernel(Params p) {
   pdl_trigger();
   pdl_wait();
   const int qt = blockIdx.x, b = blockIdx.y;
+  if ((qt | b | threadIdx.x) == 0) *p.fwd_work = 0u;  // the persistent forward's work counter
   for (int w = threadIdx.x; w < p.wk; w += blockDim.x) bm[w] = 0u;
   if ((qt & 31) == 0)
     for (int kt = threadIdx.x; kt < p.nk; kt += blockDim.x)

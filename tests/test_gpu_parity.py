@@ -102,6 +102,8 @@ D64_CASES = [
     # (L = 1 would leave a single live key per row, where dP - delta cancels
     # exactly and dQ, dK are zero: no relative error is defined there)
     (1, 2, 2, 1, "tanh", None, "causal", False, 0.0),
+    (2, 520, 4, 2, "soft_sign", None, "full", False, 0.0),
+    (2, 700, 4, 4, "tanh", None, "causal", False, 0.0),
 ]
 
 
