@@ -166,12 +166,12 @@ cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// bf16, stored-dX backward: one CTA per (query tile, b, query head) of 8 warps:
-// delta[b, h, i] = sum_d O * dO in fp32.  A row's D values are read by D / 8
-// lanes, 16 bytes each, so a warp covers 32 / (D / 8) rows per load and the CTA
-// its 128 rows in 128 / (8 * that) rounds; every round's loads are issued
+// bf16, stored-dX backward: one CTA per (half query tile, b, query head) of 8
+// warps: delta[b, h, i] = sum_d O * dO in fp32.  A row's D values are read by
+// D / 8 lanes, 16 bytes each, so a warp covers 32 / (D / 8) rows per load and
+// the CTA its 64 rows in 64 / (8 * that) rounds; every round's loads are issued
 // before any arithmetic (rows past L read row L - 1 and are dropped).
-// The CTAs of head 0 also OR their query tile's bit into the word of every KV
+// The first CTA of each query tile of head 0 also ORs the tile's bit into the word of every KV
 // tile the tile visits (the key-tile map for the dK/dV kernel, which runs next;
 // rowmap_kernel cleared those words), and the first thread zeroes the work
 // counter of the dQ GEMM that follows.
@@ -181,17 +181,18 @@ __global__ void delta_bf16_kernel(Params p) {
   pdl_wait();
   constexpr int LPR = D / 8;            // lanes per row
   constexpr int RPW = 32 / LPR;         // rows per warp and round
-  constexpr int ROUNDS = 128 / (8 * RPW);
-  const int qt = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+  constexpr int ROUNDS = 64 / (8 * RPW);
+  const int qt = blockIdx.x >> 1, b = blockIdx.y, h = blockIdx.z;
+  const int row0 = qt * 128 + 64 * (blockIdx.x & 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if ((qt | b | h | threadIdx.x) == 0) *p.dq_work = 0u;  // the dQ GEMM's work counter
+  if ((blockIdx.x | b | h | threadIdx.x) == 0) *p.dq_work = 0u;  // the dQ GEMM's work counter
   const uint4* o = static_cast<const uint4*>(p.o);
   const uint4* g = static_cast<const uint4*>(p.dO);
   const int sub = lane / LPR, part = lane % LPR;
   uint4 a[ROUNDS], c[ROUNDS];
 #pragma unroll
   for (int k = 0; k < ROUNDS; ++k) {
-    const int i = imin32(qt * 128 + (k * 8 + warp) * RPW + sub, p.L - 1);
+    const int i = imin32(row0 + (k * 8 + warp) * RPW + sub, p.L - 1);
     const size_t off = (((size_t)b * p.L + i) * p.Hq + h) * LPR + part;
     a[k] = o[off];
     c[k] = g[off];
@@ -208,10 +209,10 @@ __global__ void delta_bf16_kernel(Params p) {
     }
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    const int i = qt * 128 + (k * 8 + warp) * RPW + sub;
+    const int i = row0 + (k * 8 + warp) * RPW + sub;
     if (part == 0 && i < p.L) p.delta[((size_t)b * p.Hq + h) * p.L + i] = acc;
   }
-  if (h == 0 && warp == 0) {
+  if (h == 0 && warp == 0 && (blockIdx.x & 1) == 0) {
     const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
     for (int w = lane; w < p.wk; w += 32) {
       uint32_t bits = map[w];
@@ -227,7 +228,7 @@ __global__ void delta_bf16_kernel(Params p) {
 cudaError_t launch_delta_bf16(const Params& p, cudaStream_t s) {
   prof_begin(CAPATTN_KERNEL_DELTA, s);
   prof_count(CAPATTN_KERNEL_DELTA, 1);
-  const dim3 grid(p.nq, p.B, p.Hq);
+  const dim3 grid(2 * p.nq, p.B, p.Hq);
   const cudaError_t e = p.D == 64 ? launch_pdl(delta_bf16_kernel<64>, grid, dim3(256), 0, s, p)
                                   : launch_pdl(delta_bf16_kernel<128>, grid, dim3(256), 0, s, p);
   if (e != cudaSuccess) return e;
