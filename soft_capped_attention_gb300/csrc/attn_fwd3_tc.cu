@@ -6,8 +6,10 @@
 // mosaic_backward.py _apply_cap_mosaic and an exp2-domain softmax, for the
 // configurations where every row can use the fixed reference of the capped
 // logits (a cap, no temperature tensor, m and l not requested, logit window
-// <= kSpanMax) and the masks are causal or none: each step is one pass over the
-// scores, with no row maximum.
+// <= kSpanMax), with any of the masks: each step is one pass over the scores,
+// with no row maximum.  The key tiles of an item are the pre-pass's visit set
+// of its query tile; each row's live keys are its pre-pass span (in closed form
+// when the mask is causal or none).
 //
 // One CTA per SM takes work items (batch, head, 128-row query tile) from a
 // counter, heaviest (latest) query tiles first; an item without a live key
@@ -69,7 +71,9 @@ __device__ __forceinline__ Item decode_item(const Params& p, int it) {
   return r;
 }
 
-template <int METHOD, int HD>
+// SPANS: the rows' live keys come from the pre-pass (a window, segment ids or
+// ranker bounds); otherwise they are computed in closed form.
+template <int METHOD, int HD, bool SPANS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const Params p) {
@@ -339,10 +343,15 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
       const int n = count_tiles(map, p.wk);
       const int i = w.qt * BM + r;
       const bool valid = i < p.L;
-      // the row's live keys, without a window, segment ids or ranker bounds:
-      // [0, i + 1) causal, [0, Lk) otherwise (the pre-pass's span, in closed form)
-      const int4 ri = valid ? make_int4(0, p.causal ? imin32(i + 1, p.Lk) : p.Lk, -1, 0)
-                            : make_int4(0, 0, -1, 0);
+      // the row's live keys: the pre-pass's span, or in closed form without a
+      // window, segment ids or ranker bounds ([0, i + 1) causal, [0, Lk) otherwise)
+      int4 ri = make_int4(0, 0, -1, 0);
+      if (valid) {
+        if constexpr (SPANS)
+          ri = p.rowinfo[(size_t)w.b * p.L + i];
+        else
+          ri = make_int4(0, p.causal ? imin32(i + 1, p.Lk) : p.Lk, -1, 0);
+      }
       float lsum = 0.f;
       bool ok = true;
       TileIter ti(map, p.wk);
@@ -451,7 +460,8 @@ cudaError_t launch_fwd_hd(const Params& p, cudaStream_t s) {
   if (e == cudaSuccess) e = make_bhld_map(&mk, p.k, p.B, p.Lk, p.Hkv, HD, BN);
   if (e == cudaSuccess) e = make_bhld_map(&mv, p.v, p.B, p.Lk, p.Hkv, HD, BN);
   if (e != cudaSuccess) return e;
-  auto kern = fwd3_tc_kernel<METHOD, HD>;
+  const bool spans = p.window_len > 0 || p.seg != nullptr || p.bounds != nullptr;
+  auto kern = spans ? fwd3_tc_kernel<METHOD, HD, true> : fwd3_tc_kernel<METHOD, HD, false>;
   constexpr int SMEM_BYTES = smem_bytes<HD>();
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;

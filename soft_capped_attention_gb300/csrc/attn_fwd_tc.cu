@@ -559,19 +559,20 @@ static bool fixed_reference_everywhere(const Params& p) {
 
 // Four forward kernels, chosen from the configuration alone by what measured
 // fastest on GB300 (forward times against this file's two-tile kernel):
-//  * a sliding window or segment ids: one tile per CTA, two CTAs per SM
-//    (attn_fwd1_tc.cu; -9 % on a 1024-key window and on packed documents,
-//    where a CTA visits few key tiles and the CTAs' fixed costs dominate);
-//  * ranker bounds: this file's two tiles per CTA (the others were +4 % and
-//    +12 % on ranker histories);
-//  * causal or unmasked with the fixed reference everywhere: the persistent
-//    kernel (attn_fwd3_tc.cu);
+//  * the fixed reference everywhere, any mask: the persistent kernel
+//    (attn_fwd3_tc.cu);
+//  * otherwise, a sliding window or segment ids: one tile per CTA, two CTAs
+//    per SM (attn_fwd1_tc.cu; -9 % on a 1024-key window and on packed
+//    documents, where a CTA visits few key tiles and the CTAs' fixed costs
+//    dominate);
+//  * otherwise, ranker bounds: this file's two tiles per CTA (the others were
+//    +4 % and +12 % on ranker histories);
 //  * otherwise (causal or unmasked): one tile per CTA with two score buffers
 //    (attn_fwd2_tc.cu; -3 % causal over 2048 keys, -7 % on 8192 unmasked keys).
 cudaError_t launch_fwd_bf16(const Params& p, cudaStream_t s) {
+  if (fixed_reference_everywhere(p)) return launch_fwd3_bf16(p, s);
   if (p.window_len > 0 || p.seg != nullptr) return launch_fwd1_bf16(p, s);
   if (p.bounds != nullptr) return dispatch_cap<FwdTcLaunch>(p.cap.method, p, s);
-  if (fixed_reference_everywhere(p)) return launch_fwd3_bf16(p, s);
   return launch_fwd2_bf16(p, s);
 }
 

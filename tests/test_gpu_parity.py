@@ -497,6 +497,37 @@ def test_autograd_passes_the_lse_gradient():
 
 
 # ---------------------------------------------------------------------------
+# Every mask family with the fixed reference (a cap, no temperature, no m / l
+# requested): the persistent forward then takes each row's live keys from the
+# pre-pass spans and its key tiles from the visit sets.
+# ---------------------------------------------------------------------------
+
+PERSISTENT_MASK_CASES = [
+    # (B, L, Hq, Hkv, D, cap, mask)
+    (2, 600, 4, 2, 128, "tanh", "window"),
+    (1, 333, 2, 2, 128, "soft_sign", "window_nc"),
+    (2, 515, 4, 4, 128, "tanh", "packed"),
+    (2, 640, 4, 1, 128, "tanh", "ranker"),
+    (1, 260, 2, 2, 128, "alsc", "packed"),
+    (2, 450, 4, 2, 64, "soft_sign", "ranker"),
+    (1, 700, 2, 1, 64, "tanh", "window"),
+]
+
+
+@pytest.mark.parametrize("case", PERSISTENT_MASK_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_persistent_forward_with_masks(case):
+    B, L, Hq, Hkv, D, cap, mask = case
+    inp = make_case(B, L, Hq, Hkv, D, torch.bfloat16, mask, False, seed=L + 13 * Hq + D)
+    ap = params(cap, mask, 0.0)
+    got = run_gpu(inp, ap, torch.bfloat16)
+    ref = run_oracle(inp, ap)
+    compare(got, ref, torch.bfloat16)
+    dead = np.isneginf(ref["LSE"])
+    if dead.any():
+        assert np.all(np.transpose(got["O"], (0, 2, 1, 3))[dead] == 0)
+
+
+# ---------------------------------------------------------------------------
 # Ranker bounds that leave whole query tiles without a live key next to live
 # ones (the two-tile forward then has an idle tile in a CTA with work): O and
 # the gradients of the dead rows must be exactly zero, the rest match.
