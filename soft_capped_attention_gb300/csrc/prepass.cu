@@ -166,8 +166,8 @@ cudaError_t launch_delta_fp32(const Params& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// bf16, stored-dX backward: one CTA per (half query tile, b, query head) of 8
-// warps: delta[b, h, i] = sum_d O * dO in fp32.  A row's D values are read by
+// bf16, stored-dX backward: one CTA per (query head, half query tile, b) of 8
+// warps, the head fastest: delta[b, h, i] = sum_d O * dO in fp32.  A row's D values are read by
 // D / 8 lanes, 16 bytes each, so a warp covers 32 / (D / 8) rows per load and
 // the CTA its 64 rows in 64 / (8 * that) rounds; every round's loads are issued
 // before any arithmetic (rows past L read row L - 1 and are dropped).
@@ -182,10 +182,13 @@ __global__ void delta_bf16_kernel(Params p) {
   constexpr int LPR = D / 8;            // lanes per row
   constexpr int RPW = 32 / LPR;         // rows per warp and round
   constexpr int ROUNDS = 64 / (8 * RPW);
-  const int qt = blockIdx.x >> 1, b = blockIdx.y, h = blockIdx.z;
-  const int row0 = qt * 128 + 64 * (blockIdx.x & 1);
+  // the head is the fastest grid index: CTAs that run together read the
+  // same rows of every head, one contiguous region of O and dO
+  const int h = (int)(blockIdx.x % (unsigned)p.Hq), rest = (int)(blockIdx.x / (unsigned)p.Hq);
+  const int qt = rest >> 1, half = rest & 1, b = blockIdx.y;
+  const int row0 = qt * 128 + 64 * half;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if ((blockIdx.x | b | h | threadIdx.x) == 0) *p.dq_work = 0u;  // the dQ GEMM's work counter
+  if ((blockIdx.x | b | threadIdx.x) == 0) *p.dq_work = 0u;  // the dQ GEMM's work counter
   const uint4* o = static_cast<const uint4*>(p.o);
   const uint4* g = static_cast<const uint4*>(p.dO);
   const int sub = lane / LPR, part = lane % LPR;
@@ -212,7 +215,7 @@ __global__ void delta_bf16_kernel(Params p) {
     const int i = row0 + (k * 8 + warp) * RPW + sub;
     if (part == 0 && i < p.L) p.delta[((size_t)b * p.Hq + h) * p.L + i] = acc;
   }
-  if (h == 0 && warp == 0 && (blockIdx.x & 1) == 0) {
+  if (h == 0 && warp == 0 && half == 0) {
     const uint32_t* map = p.qmap + ((size_t)b * p.nq + qt) * p.wk;
     for (int w = lane; w < p.wk; w += 32) {
       uint32_t bits = map[w];
@@ -228,7 +231,7 @@ __global__ void delta_bf16_kernel(Params p) {
 cudaError_t launch_delta_bf16(const Params& p, cudaStream_t s) {
   prof_begin(CAPATTN_KERNEL_DELTA, s);
   prof_count(CAPATTN_KERNEL_DELTA, 1);
-  const dim3 grid(2 * p.nq, p.B, p.Hq);
+  const dim3 grid((unsigned)(p.Hq * 2 * p.nq), p.B);
   const cudaError_t e = p.D == 64 ? launch_pdl(delta_bf16_kernel<64>, grid, dim3(256), 0, s, p)
                                   : launch_pdl(delta_bf16_kernel<128>, grid, dim3(256), 0, s, p);
   if (e != cudaSuccess) return e;
