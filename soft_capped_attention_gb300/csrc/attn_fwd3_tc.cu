@@ -82,7 +82,9 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
   constexpr int OQ = HD / 4;  // O columns per thread (a quarter of the row)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * 2 + 2 * KST + 2 * VST + 2 * 2 + 2 * 2 + 2 * 2 + 2];
-  __shared__ int items[2];
+  // item slots: (item, key tiles it visits, first word of its visit bitmap);
+  // the publisher reads the bitmap, so that no reader waits on that load
+  __shared__ int4 items[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -159,29 +161,35 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     int j = 0;                 // steps loaded so far (ring position)
     int qu0 = 0, qu1 = 0;      // items loaded into each Q buffer so far
     for (int k = 0;; ++k) {
-      int it;
+      int4 slot;
       if (role == 2) {
-        it = 0;
+        int it = 0;
         if (lane == 0) it = (int)atomicAdd(p.fwd_work, 1u);
         it = __shfl_sync(0xFFFFFFFFu, it, 0);
-        if (it >= nitems) it = -1;
+        slot = make_int4(-1, 0, 0, 0);
+        if (it < nitems) {
+          const Item w = decode_item(p, it);
+          const uint32_t* map = p.qmap + ((size_t)w.b * p.nq + w.qt) * p.wk;
+          slot = make_int4(it, count_tiles(map, p.wk), (int)map[0], 0);
+        }
         if (k >= 2 && !mbar_wait_warp(bar_iempty + 8 * (k & 1), ((k >> 1) - 1) & 1, p.status, &abort_flag))
           break;
         if (lane == 0) {
-          items[k & 1] = it;
+          items[k & 1] = slot;
           mbar_arrive(bar_ifull + 8 * (k & 1));
         }
         __syncwarp();
       } else {
         if (!mbar_wait_warp(bar_ifull + 8 * (k & 1), (k >> 1) & 1, p.status, &abort_flag)) break;
-        it = *static_cast<volatile int*>(&items[k & 1]);
+        slot = items[k & 1];  // (the wait above is a compiler memory barrier)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_iempty + 8 * (k & 1));
       }
+      const int it = slot.x;
       if (it < 0) break;
       const Item w = decode_item(p, it);
       const uint32_t* map = p.qmap + ((size_t)w.b * p.nq + w.qt) * p.wk;
-      if (count_tiles(map, p.wk) == 0) continue;
+      if (slot.y == 0) continue;
       if (role == 2) {
         const int x = k & 1;
         const int uq = x ? qu1++ : qu0++;
@@ -196,7 +204,7 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
       }
       const int g = w.h / p.G;
       bool ok = true;
-      TileIter ti(map, p.wk);
+      TileIter ti(map, p.wk, (uint32_t)slot.z);
       int t;
       while (ti.next(t)) {
         const int nst = role == 0 ? KST : VST;
@@ -244,12 +252,11 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     int ou0 = 0, ou1 = 0;      // items in each O accumulator so far
     for (int k = 0;; ++k) {
       if (!mbar_wait_warp(bar_ifull + 8 * (k & 1), (k >> 1) & 1, p.status, &abort_flag)) break;
-      const int it = *static_cast<volatile int*>(&items[k & 1]);
+      const int4 slot = items[k & 1];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_iempty + 8 * (k & 1));
-      if (it < 0) break;
-      const Item w = decode_item(p, it);
-      const int n = count_tiles(p.qmap + ((size_t)w.b * p.nq + w.qt) * p.wk, p.wk);
+      if (slot.x < 0) break;
+      const int n = slot.y;
       if (n == 0) continue;
       const int x = k & 1;
       const int uq = x ? qu1++ : qu0++;
@@ -332,15 +339,55 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     int g = 0;                 // steps consumed so far
     int ou0 = 0, ou1 = 0;      // items read from each O accumulator so far
     int ex = 0;                // l exchanges so far
-    for (int k = 0;; ++k) {
+    // The O of an item leaves after the next item's first step (its last P V
+    // completes meanwhile): pend = accumulator | (use parity) << 1, or -1.
+    int pend = -1, pend_b = 0, pend_h = 0, pend_i = 0;
+    float pend_l = 0.f;
+    // writes row pend_i's OQ columns of the pending item's O, 16 at a time,
+    // straight to global memory (O [B, L, Hq, HD] bf16; rows past L are not
+    // written), frees the accumulator and writes the row's LSE
+    auto drain = [&]() -> bool {
+      const int xx = pend & 1;
+      if (!mbar_wait_warp(bar_ofull + 8 * xx, (pend >> 1) & 1, p.status, &abort_flag)) return false;
+      tc_fence_after();
+      const bool pvalid = pend_i < p.L;
+      const bool live = pend_l > 0.f;
+      const float inv = live ? 1.f / pend_l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(out + (((size_t)pend_b * p.L + (pvalid ? pend_i : 0)) * p.Hq + pend_h) * HD +
+                                            OQ * cq);
+      const uint32_t ob = tmem + lane_off + 256u + 128u * (uint32_t)xx + (uint32_t)(OQ * cq);
+#pragma unroll
+      for (int hh = 0; hh < OQ / 16; ++hh) {
+        uint32_t o[16], pk[8];
+        tmem_ld16(ob + 16u * (uint32_t)hh, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          pk[e] = pack_bf16x2(live ? __uint_as_float(o[2 * e]) * inv : 0.f,
+                              live ? __uint_as_float(o[2 * e + 1]) * inv : 0.f);
+        if (pvalid) {
+          dst[2 * hh] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[2 * hh + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      // every read of the accumulator is done: it is free again
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_oempty + 8 * xx);
+      if (pvalid && cq == 0)
+        p.lse[((size_t)pend_b * p.Hq + pend_h) * p.L + pend_i] = live ? (m_use + log2f(pend_l)) * kLn2 : -INFINITY;
+      return true;
+    };
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
       if (!mbar_wait_warp(bar_ifull + 8 * (k & 1), (k >> 1) & 1, p.status, &abort_flag)) break;
-      const int it = *static_cast<volatile int*>(&items[k & 1]);
+      const int4 slot = items[k & 1];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_iempty + 8 * (k & 1));
-      if (it < 0) break;
-      const Item w = decode_item(p, it);
+      if (slot.x < 0) break;
+      const Item w = decode_item(p, slot.x);
       const uint32_t* map = p.qmap + ((size_t)w.b * p.nq + w.qt) * p.wk;
-      const int n = count_tiles(map, p.wk);
+      const int n = slot.y;
       const int i = w.qt * BM + r;
       const bool valid = i < p.L;
       // the row's live keys: the pre-pass's span, or in closed form without a
@@ -353,18 +400,15 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
           ri = make_int4(0, p.causal ? imin32(i + 1, p.Lk) : p.Lk, -1, 0);
       }
       float lsum = 0.f;
-      bool ok = true;
-      TileIter ti(map, p.wk);
+      TileIter ti(map, p.wk, (uint32_t)slot.z);
       int t;
-      for (int st = 0; st < n && ti.next(t); ++st) {
+      // one step: the quarter-row's P over its score buffer, handed to the issuer
+      auto step = [&](int st, int t) -> bool {
         const int gg = g + st;
         const int k0 = t * BN;
         const int c0 = k0 + 32 * cq;
         const uint32_t sb = s_quarter + 128u * (uint32_t)(gg & 1);
-        if (!mbar_wait_warp(bar_sfull + 8 * (gg & 1), (gg >> 1) & 1, p.status, &abort_flag)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait_warp(bar_sfull + 8 * (gg & 1), (gg >> 1) & 1, p.status, &abort_flag)) return false;
         tc_fence_after();
         const bool full = (ri.x <= k0) && (ri.y >= k0 + BN);
         const bool warp_partial = __any_sync(0xFFFFFFFFu, !full);
@@ -384,13 +428,24 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pfull + 8 * (gg & 1));
+        return true;
+      };
+      int st = 0;
+      if (n > 0 && ti.next(t)) {
+        ok = step(0, t);
+        st = 1;
       }
+      // the previous item's O, once this item's first P is handed over (its
+      // last P V has completed meanwhile)
+      if (ok && n > 0 && pend >= 0) {
+        ok = drain();
+        pend = -1;
+      }
+      for (; ok && st < n && ti.next(t); ++st) ok = step(st, t);
       if (!ok) break;
       g += n;
-      // ---- epilogue of the item
-      float l_row = 0.f;
+      // ---- the item's l, and its O / LSE (now or after the next item's first step)
       const int x = k & 1;
-      bool have_o = false;
       if (n > 0) {
         // l of the whole row: the four quarters add their parts
         float* xs = xch + (ex & 1) * 4 * BM;
@@ -398,48 +453,31 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_xch);
         if (!mbar_wait_warp(bar_xch, ex & 1, p.status, &abort_flag)) break;
+        float l_row = 0.f;
 #pragma unroll
         for (int o4 = 0; o4 < 4; ++o4) l_row += xs[o4 * BM + r];
         ++ex;
         const int uo = x ? ou1++ : ou0++;
-        if (!mbar_wait_warp(bar_ofull + 8 * x, uo & 1, p.status, &abort_flag)) break;
-        tc_fence_after();
-        have_o = true;
-      }
-      const bool live = l_row > 0.f;
-      const float inv = live ? 1.f / l_row : 0.f;
-      // this thread's OQ columns of the row, 16 at a time, straight to global
-      // memory (O [B, L, Hq, HD] bf16; rows past L are not written)
-      uint4* dst = reinterpret_cast<uint4*>(out + (((size_t)w.b * p.L + (valid ? i : 0)) * p.Hq + w.h) * HD +
-                                            OQ * cq);
-      const uint32_t ob = tmem + lane_off + 256u + 128u * (uint32_t)x + (uint32_t)(OQ * cq);
-#pragma unroll
-      for (int hh = 0; hh < OQ / 16; ++hh) {
-        uint32_t o[16], pk[8];
-        if (have_o) {
-          tmem_ld16(ob + 16u * (uint32_t)hh, o);
-          tmem_wait_ld();
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float a = (have_o && live) ? __uint_as_float(o[2 * e]) * inv : 0.f;
-          const float bb = (have_o && live) ? __uint_as_float(o[2 * e + 1]) * inv : 0.f;
-          pk[e] = pack_bf16x2(a, bb);
+        pend = x | ((uo & 1) << 1);
+        pend_b = w.b;
+        pend_h = w.h;
+        pend_i = i;
+        pend_l = l_row;
+      } else {
+        // no live key tile: the previous item's O first, then zero rows
+        if (pend >= 0) {
+          if (!drain()) break;
+          pend = -1;
         }
         if (valid) {
-          dst[2 * hh] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[2 * hh + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          uint4* dst = reinterpret_cast<uint4*>(out + (((size_t)w.b * p.L + i) * p.Hq + w.h) * HD + OQ * cq);
+#pragma unroll
+          for (int e = 0; e < OQ / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+          if (cq == 0) p.lse[((size_t)w.b * p.Hq + w.h) * p.L + i] = -INFINITY;
         }
       }
-      if (have_o) {
-        // every read of the accumulator is done: it is free again
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_oempty + 8 * x);
-      }
-      if (valid && cq == 0)
-        p.lse[((size_t)w.b * p.Hq + w.h) * p.L + i] = live ? (m_use + log2f(l_row)) * kLn2 : -INFINITY;
     }
+    if (pend >= 0 && __all_sync(0xFFFFFFFFu, abort_flag == 0)) drain();
   }
   __syncwarp();  // every warp reaches the CTA barrier converged
   tc_fence_before();

@@ -345,6 +345,8 @@ struct TileIter {
   int nwords, w;
   uint32_t bits;
   __device__ TileIter(const uint32_t* m, int n) : map(m), nwords(n), w(0), bits(n > 0 ? m[0] : 0u) {}
+  // the first word already read (the later ones are loaded when reached)
+  __device__ TileIter(const uint32_t* m, int n, uint32_t first) : map(m), nwords(n), w(0), bits(first) {}
   __device__ bool next(int& t) {
     while (bits == 0u) {
       if (++w >= nwords) return false;
