@@ -331,7 +331,7 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
       x_hi = fmaxf(radd, rmul + radd);
       span = fabsf(rmul);
     }
-    const float m_use = x_hi - fmaxf(0.f, span - kSpanLo);  // the fixed reference
+    const float m_use = fixed_reference(x_hi, span);
     const float addm = radd - m_use;
     TanhFold tf{};
     if constexpr (METHOD == CAPATTN_CAP_TANH) tf = tanh_fold(xf.in, rmul);

@@ -176,7 +176,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   }
   const bool fixed_ref = (METHOD != CAPATTN_CAP_NONE) && p.m == nullptr && p.l == nullptr &&
                          __syncthreads_and(warp < 2 || span <= kSpanMax);
-  const float m_fixed = x_hi - fmaxf(0.f, span - kSpanLo);
+  const float m_fixed = fixed_reference(x_hi, span);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer

@@ -25,12 +25,19 @@ constexpr int tile_bytes() { return (HD / 64) * SLAB; }
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // Capped logits of a row lie in a window [x_hi - W, x_hi] (log2 units) known
 // before any score is seen: W = 2 |mul| for tanh and soft_sign (|f| < 1), |mul|
-// for ALSC (0 < f < 1).  With the fixed reference m = x_hi - max(0, W - kSpanLo)
-// every exponent x - m lies in [-kSpanLo, W - kSpanLo]: no term underflows
-// ex2's normal range and, while W <= kSpanMax, none overflows fp32 even summed
-// over a row of 2^20 keys.
+// for ALSC (0 < f < 1).  With the fixed reference
+//   m = x_hi - min(max(0, W - kSpanLo), kTopMax)
+// every exponent x - m lies in [-max(kSpanLo, W - kTopMax), min(W - kSpanLo,
+// kTopMax)]: at most 2^100 (no overflow in fp32 even summed over a row of 2^20
+// keys) and, while W <= kSpanMax, at least 2^-124 (inside ex2's normal range,
+// which ends at 2^-126).  Windows up to kSpanLo + kTopMax put the bottom at
+// -kSpanLo; wider ones trade bottom margin for the same top.
 constexpr float kSpanLo = 120.0f;
-constexpr float kSpanMax = 220.0f;
+constexpr float kTopMax = 100.0f;
+constexpr float kSpanMax = 224.0f;
+__device__ __forceinline__ float fixed_reference(float x_hi, float span) {
+  return x_hi - fminf(fmaxf(0.f, span - kSpanLo), kTopMax);
+}
 
 // S = Q K^T from the tiles' K-major descriptors.
 template <int HD>

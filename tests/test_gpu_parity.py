@@ -268,6 +268,26 @@ def test_scores_at_the_bottom_of_the_cap_window():
     assert np.max(np.abs(got["LSE"] - ref["LSE"])) <= 1e-3
 
 
+@pytest.mark.parametrize("sign", [1.0, -1.0], ids=["top", "bottom"])
+def test_alsc_window_just_over_the_plain_split(sign):
+    # ALSC cap 30, alpha 2, beta 0.5: a logit window of 220.13 (log2 units),
+    # just over kSpanLo + kTopMax, where the fixed reference keeps the top
+    # exponent at 100 and lets the bottom go a little below -120.  Scores far
+    # above (top) or below (bottom) the cap put every logit at that end.
+    B, L, H, D = 1, 256, 2, 128
+    rng = np.random.default_rng(37)
+    base = np.abs(rng.standard_normal((B, L, H, D))).astype(np.float32) + 0.5
+    inp = {"q": round_to_bf16(base * 4.0), "k": round_to_bf16(sign * base * 4.0),
+           "v": round_to_bf16(rng.standard_normal((B, L, H, D)).astype(np.float32)),
+           "do": round_to_bf16(rng.standard_normal((B, L, H, D)).astype(np.float32)),
+           "temp": None, "seg": None, "bounds": None}
+    ap = params("alsc", "full", 0.0)
+    got, ref = run_gpu(inp, ap, torch.bfloat16), run_oracle(inp, ap)
+    assert np.max(np.abs(got["O"] - ref["O"])) <= 2e-2
+    assert np.all(np.isfinite(got["LSE"]))
+    assert np.max(np.abs(got["LSE"] - ref["LSE"])) <= 1e-3
+
+
 def test_wide_cap_window_uses_running_max():
     # tanh cap 200: the logit window (2 * 200 * log2 e) is wider than the fixed
     # reference allows, so the forward keeps the running max.
