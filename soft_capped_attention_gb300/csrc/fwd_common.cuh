@@ -23,6 +23,9 @@ constexpr int SLAB = 128 * 64 * 2;          // one [128][64] bf16 box
 template <int HD>
 constexpr int tile_bytes() { return (HD / 64) * SLAB; }
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+// of the 16 column pairs of a 32-column pass, those whose tanh runs on the FMA
+// pipe (polynomial) when the range allows; the others use MUFU
+constexpr int kFwdPolyPairs = 12;
 // Capped logits of a row lie in a window [x_hi - W, x_hi] (log2 units) known
 // before any score is seen: W = 2 |mul| for tanh and soft_sign (|f| < 1), |mul|
 // for ALSC (0 < f < 1).  With the fixed reference
@@ -121,6 +124,38 @@ __device__ __forceinline__ float p_chunk_tanh_fold(const uint32_t (&v)[2 * NP], 
     f2_split(tanh_fold_eval(f2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), tf, add2),
              x0, x1);
     float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if constexpr (MASKED) {
+      if (!(live & (1u << (2 * e)))) p0 = 0.f;
+      if (!(live & (2u << (2 * e)))) p1 = 0.f;
+    }
+    acc = f2_add(acc, f2(p0, p1));
+    pk[e] = pack_bf16x2(p0, p1);
+  }
+  float s0, s1;
+  f2_split(acc, s0, s1);
+  return s0 + s1;
+}
+
+// The same with the tanh of the last NP - NPOLY column pairs on MUFU
+// (tanh.approx) instead of the FMA pipe, balancing the two pipes.
+template <bool MASKED, int NP, int NPOLY>
+__device__ __forceinline__ float p_chunk_tanh_mixed(const uint32_t (&v)[2 * NP], uint32_t (&pk)[NP],
+                                                    const TanhFold& tf, const Xf& xf, float mul, float addm,
+                                                    uint32_t live) {
+  const F2 add2 = f2(addm, addm);
+  F2 acc = f2(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < NP; ++e) {
+    float p0, p1;
+    if (e < NPOLY) {
+      float x0, x1;
+      f2_split(tanh_fold_eval(f2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), tf, add2), x0, x1);
+      p0 = ex2_approx(x0);
+      p1 = ex2_approx(x1);
+    } else {
+      p0 = ex2_approx(fmaf(mul, cap_f<CAPATTN_CAP_TANH>(__uint_as_float(v[2 * e]), xf), addm));
+      p1 = ex2_approx(fmaf(mul, cap_f<CAPATTN_CAP_TANH>(__uint_as_float(v[2 * e + 1]), xf), addm));
+    }
     if constexpr (MASKED) {
       if (!(live & (1u << (2 * e)))) p0 = 0.f;
       if (!(live & (2u << (2 * e)))) p1 = 0.f;
@@ -234,13 +269,13 @@ __device__ __forceinline__ float p_dispatch32(bool full_any, bool poly, const ui
                                              float mul, float addm, int j0, int4 ri, bool any) {
   if (full_any) {
     if constexpr (METHOD == CAPATTN_CAP_TANH) {
-      if (poly) return p_chunk_tanh_fold<false, 16>(v, pk, tf, addm, 0xFFFFFFFFu);
+      if (poly) return p_chunk_tanh_mixed<false, 16, kFwdPolyPairs>(v, pk, tf, xf, mul, addm, 0xFFFFFFFFu);
     }
     return p_chunk<METHOD, false, 16>(v, pk, xf, mul, addm, 0xFFFFFFFFu);
   }
   const uint32_t live = any ? live_bits32(ri, j0) : 0u;
   if constexpr (METHOD == CAPATTN_CAP_TANH) {
-    if (poly) return p_chunk_tanh_fold<true, 16>(v, pk, tf, addm, live);
+    if (poly) return p_chunk_tanh_mixed<true, 16, kFwdPolyPairs>(v, pk, tf, xf, mul, addm, live);
   }
   return p_chunk<METHOD, true, 16>(v, pk, xf, mul, addm, live);
 }
