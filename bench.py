@@ -40,6 +40,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -162,12 +163,24 @@ class ClockSampler:
                 "window": "an untimed soak of the same step (--soak-seconds), then the timed steps"}
 
 
-def kernel_source_hash() -> str:
+_C_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def kernel_source_hash(csrc: str = None) -> str:
+    """Hash of the kernel sources' code: C / C++ / CUDA files without their
+    comments and with whitespace collapsed (a comment edit keeps the hash),
+    other files as they are."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "soft_capped_attention_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "soft_capped_attention_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        path = os.path.join(csrc, f)
+        if not os.path.isfile(path):
+            continue
+        with open(path, "rb") as fh:
+            data = fh.read()
+        if f.endswith((".cu", ".cuh", ".h", ".cpp", ".c")):
+            data = " ".join(_C_COMMENT.sub(" ", data.decode()).split()).encode()
+        h.update(f.encode() + data)
     return h.hexdigest()[:16]
 
 

@@ -19,9 +19,13 @@
 // softmax works on step j + 1.  Across items, Q and O are double-buffered (two
 // Q tiles in shared memory, two O accumulators in TMEM), so the next item's Q
 // is loaded ahead and its first scores are computed while the softmax warps
-// finish the current item: l, O out of TMEM and straight to global memory.
+// finish the current item; they take the row's l at once and drain the item's
+// O (out of TMEM, straight to global memory) after handing over the next
+// item's first P, by which time the item's last P V has completed.
 // Warp roles (20 warps):
-//   warp 19      fetches the items (a two-slot ring in shared memory) and
+//   warp 19      fetches the items (a two-slot ring in shared memory, each slot
+//                with the item's key-tile count and the first word of its
+//                visit bitmap, so that no reader waits on that load) and
 //                loads each item's Q into buffer x, running up to two items
 //                ahead; warps 0 and 18 follow the items and load the K and V
 //                tiles into two-stage rings;
