@@ -306,6 +306,18 @@ capattn_status capattn_mask_bits_host(const capattn_config* cfg, const int32_t* 
                                       size_t n_words);
 
 /*
+ * The polynomial the kernels use for the ALSC cap on the FMA pipe (a
+ * restatement of mosaic_backward.py _apply_cap_mosaic's sigmoid, for speed):
+ * sigma(alpha / cap * sm_scale * X + alpha * beta) - sigma(alpha * beta)
+ *   = X * (coeffs[0] + coeffs[1] X + ... + coeffs[6] X^6)
+ * for a raw score X (q . k, before sm_scale) with |X| <= *xmax; outside that
+ * range (decided per warp and step) the kernels evaluate the sigmoid itself.
+ * coeffs: host, 7 floats; xmax: host.  CAPATTN_ERR_INVALID_ARG unless the
+ * config is valid with cap_method CAPATTN_CAP_ALSC and cap > 0.
+ */
+capattn_status capattn_debug_alsc_poly(const capattn_config* cfg, float* coeffs, float* xmax);
+
+/*
  * Forward without any allocation or workspace argument (the pages have no
  * counterpart; this is an addition for callers that cannot allocate, such as
  * plugins inside a framework that owns all device memory and gives them no

@@ -109,7 +109,8 @@ EXPORTED_SYMBOLS = ("capattn_status_string", "capattn_validate_config", "capattn
                     "capattn_device_status", "capattn_ranker_bounds_from_ids",
                     "capattn_visit_map_host", "capattn_visit_map_device", "capattn_mask_bits_host",
                     "capattn_profile_enable", "capattn_profile_select", "capattn_profile_read", "capattn_kernel_name",
-                    "capattn_fwd_noalloc", "capattn_noalloc_status", "capattn_check_bounded_wait")
+                    "capattn_fwd_noalloc", "capattn_noalloc_status", "capattn_check_bounded_wait",
+                    "capattn_debug_alsc_poly")
 KERNEL_KINDS = ("prepass", "fwd", "delta", "dkv", "dq")
 
 

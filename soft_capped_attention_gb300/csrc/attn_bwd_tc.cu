@@ -147,9 +147,14 @@ template <int METHOD, bool POLY, bool DT = false>
 __device__ __forceinline__ void dkv_pair(float X0, float X1, float dp0, float dp1, const Xf& xf,
                                          const TanhFold& tf, const ColPair& c, bool l0, bool l1,
                                          uint32_t& pk, uint32_t& xk, const DtempRow* dr = nullptr,
-                                         F2* dacc = nullptr) {
+                                         F2* dacc = nullptr, const CapConsts* cap = nullptr) {
   F2 f, e;
-  if constexpr (METHOD == CAPATTN_CAP_TANH) {
+  if constexpr (METHOD == CAPATTN_CAP_ALSC && POLY) {
+    // the sigmoid on the FMA pipe (the caller checked |X| <= alsc_xmax for the
+    // warp); -f' = f^2 - f
+    f = f2_add(f2(cap->alsc_sb, cap->alsc_sb), alsc_poly2(f2(X0, X1), *cap));
+    e = f2_mul(f, f2_add(f, f2(-1.f, -1.f)));
+  } else if constexpr (METHOD == CAPATTN_CAP_TANH) {
     if constexpr (POLY) {
       f = tanh_fold_eval(f2(X0, X1), tf, f2(0.f, 0.f));   // tanh(in X) = X Q(X^2)
     } else {
@@ -187,7 +192,8 @@ constexpr int kDkvPolyPairs = 5;  // of the 8 column pairs of a chunk: tanh on t
 template <int METHOD, bool MASKED, bool POLY, int C>
 __device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_t (&dp)[16],
                                           const ColPair* cp, const int4* ci, int jrow, const Xf& xf,
-                                          const TanhFold& tf, uint32_t (&pk)[8], uint32_t (&xk)[8]) {
+                                          const TanhFold& tf, const CapConsts& cap, uint32_t (&pk)[8],
+                                          uint32_t (&xk)[8]) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const ColPair c = cp[8 * C + e];
@@ -199,8 +205,8 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&s)[64], const uint32_
     }
     const float X0 = __uint_as_float(s[16 * C + 2 * e]), X1 = __uint_as_float(s[16 * C + 2 * e + 1]);
     const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
-    if (POLY && e < kDkvPolyPairs)
-      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, tf, c, l0, l1, pk[e], xk[e]);
+    if (POLY && (METHOD == CAPATTN_CAP_ALSC || e < kDkvPolyPairs))
+      dkv_pair<METHOD, true>(X0, X1, d0, d1, xf, tf, c, l0, l1, pk[e], xk[e], nullptr, nullptr, &cap);
     else
       dkv_pair<METHOD, false>(X0, X1, d0, d1, xf, tf, c, l0, l1, pk[e], xk[e]);
   }
@@ -221,14 +227,15 @@ constexpr uint32_t kNoDx = 0xFFFFFFFFu;
 template <int METHOD, bool MASKED, bool POLY, bool DX>
 __device__ __forceinline__ void dkv_step(const uint32_t (&s)[64], uint32_t dp_base, const ColPair* cp,
                                          const int4* ci, int jrow, const Xf& xf, const TanhFold& tf,
-                                         uint32_t bar_chunk0, int lane, char* pool, uint32_t dxo) {
+                                         const CapConsts& cap, uint32_t bar_chunk0, int lane, char* pool,
+                                         uint32_t dxo) {
   uint32_t da[16], db[16], pk[8], xk[8];
   tmem_ld16(dp_base, da);
   tmem_wait_ld();
 #define CAPATTN_DKV_CHUNK(C, CUR, NXT)                                                     \
   {                                                                                       \
     if (C < 3) tmem_ld16(dp_base + 16 * (C + 1), NXT);                                    \
-    dkv_chunk<METHOD, MASKED, POLY, C>(s, CUR, cp, ci, jrow, xf, tf, pk, xk);             \
+    dkv_chunk<METHOD, MASKED, POLY, C>(s, CUR, cp, ci, jrow, xf, tf, cap, pk, xk);        \
     __syncwarp();                                                                         \
     tmem_st8(dp_base + 16 * C, pk);                                                       \
     tmem_st8(dp_base + 16 * C + 8, xk);                                                   \
@@ -548,11 +555,14 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_sfree);
       bool poly = false;
-      if constexpr (METHOD == CAPATTN_CAP_TANH) {
+      if constexpr (METHOD == CAPATTN_CAP_TANH || METHOD == CAPATTN_CAP_ALSC) {
         float am = 0.f;
 #pragma unroll
         for (int e = 0; e < 64; e += 2) am = fmax3_abs(am, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-        poly = __all_sync(0xFFFFFFFFu, tf.ok && am * fabsf(xf.in) <= kTanhPolyMaxU);
+        if constexpr (METHOD == CAPATTN_CAP_TANH)
+          poly = __all_sync(0xFFFFFFFFu, tf.ok && am * fabsf(xf.in) <= kTanhPolyMaxU);
+        else
+          poly = __all_sync(0xFFFFFFFFu, am <= p.cap.alsc_xmax);  // the sigmoid on the FMA pipe
       }
       if (!mbar_wait_warp(bar_dp, step & 1, p.status, &abort_flag)) {
         aborted = true;
@@ -563,14 +573,14 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int4* ci = &coli[cb][64 * wg];
       if (tile_full) {
         if (poly)
-          dkv_step<METHOD, false, true, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, false, true, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, p.cap, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
         else
-          dkv_step<METHOD, false, false, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, false, false, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, p.cap, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
       } else {
         if (poly)
-          dkv_step<METHOD, true, true, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, true, true, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, p.cap, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
         else
-          dkv_step<METHOD, true, false, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
+          dkv_step<METHOD, true, false, DX>(sv, dp_cols, cp, ci, jrow, xf, tf, p.cap, bar_chunk, lane, static_cast<char*>(p.dx_pool), dxo);
       }
       mbar_arrive(my_cfree);
       r1 = r2;
@@ -640,7 +650,7 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&s)[64], const uint32_t
     const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
     uint32_t pk;
     if (POLY && e < kDkvPolyPairs)
-      dkv_pair<METHOD, true, DT>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e], &dr, &dacc);
+      dkv_pair<METHOD, METHOD == CAPATTN_CAP_TANH, DT>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e], &dr, &dacc);
     else
       dkv_pair<METHOD, false, DT>(X0, X1, d0, d1, xf, tf, rc, l0, l1, pk, xk[e], &dr, &dacc);
   }

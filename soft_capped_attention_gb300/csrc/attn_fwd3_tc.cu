@@ -422,6 +422,10 @@ fwd3_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         if (warp_partial && quarter_dead(ri, c0)) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) pk[e] = 0u;
+        } else if (METHOD == CAPATTN_CAP_ALSC && quarter_alsc_poly(v, p.cap.alsc_xmax)) {
+          // the sigmoid on the FMA pipe: mul (f - sigma(alpha beta)) - m
+          lsum += full ? p_chunk_alsc<false, 16>(v, pk, p.cap, rmul, -m_use, 0xFFFFFFFFu)
+                       : p_chunk_alsc<true, 16>(v, pk, p.cap, rmul, -m_use, live_bits32(ri, c0));
         } else {
           const bool poly = quarter_poly<METHOD>(v, tf, xf);
           lsum += p_dispatch32<METHOD>(full, poly, v, pk, xf, tf, rmul, addm, c0, ri, true);

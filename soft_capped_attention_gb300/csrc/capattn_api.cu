@@ -82,6 +82,47 @@ static capattn_status validate(const capattn_config* c) {
   return CAPATTN_OK;
 }
 
+// sigma(b + d) - sigma(b) = d * g(d) for |d| <= kAlscPolyD: g interpolated at
+// the 7 Chebyshev nodes of [-kAlscPolyD, kAlscPolyD] (degree 6, error ~1e-8
+// against g's values of 0.1 .. 0.25), then written in the raw score X = d / u:
+// sigma - sigma(b) = X * sum_k gu[k] X^k with gu[k] = g_k u^(k + 1).
+static constexpr double kAlscPolyD = 0.5;
+static void alsc_poly_fit(double b, double sb, double u, float gu[7], float* xmax) {
+  const double pi = 3.14159265358979323846;
+  double a[7][8];  // Vandermonde rows in t = d / D, with the values g(d) appended
+  for (int j = 0; j < 7; ++j) {
+    const double t = cos((2.0 * j + 1.0) * pi / 14.0);
+    const double d = kAlscPolyD * t;
+    const double g = fabs(d) < 1e-9 ? sb * (1.0 - sb) : (1.0 / (1.0 + exp(-(b + d))) - sb) / d;
+    double tk = 1.0;
+    for (int k = 0; k < 7; ++k) {
+      a[j][k] = tk;
+      tk *= t;
+    }
+    a[j][7] = g;
+  }
+  // Gaussian elimination with partial pivoting
+  for (int c = 0; c < 7; ++c) {
+    int piv = c;
+    for (int r = c + 1; r < 7; ++r)
+      if (fabs(a[r][c]) > fabs(a[piv][c])) piv = r;
+    for (int k = 0; k < 8; ++k) std::swap(a[c][k], a[piv][k]);
+    for (int r = 0; r < 7; ++r) {
+      if (r == c) continue;
+      const double f = a[r][c] / a[c][c];
+      for (int k = c; k < 8; ++k) a[r][k] -= f * a[c][k];
+    }
+  }
+  double up = u;       // u^(k + 1)
+  double dk = 1.0;     // D^k
+  for (int k = 0; k < 7; ++k) {
+    gu[k] = (float)(a[k][7] / a[k][k] / dk * up);
+    up *= u;
+    dk *= kAlscPolyD;
+  }
+  *xmax = u > 0.0 ? (float)(kAlscPolyD / u) : 0.f;
+}
+
 static CapConsts make_cap(const capattn_config& c) {
   CapConsts k;
   memset(&k, 0, sizeof(k));
@@ -98,6 +139,7 @@ static CapConsts make_cap(const capattn_config& c) {
     k.alsc_out = (float)(cap / denom);
     k.alsc_sb = (float)sb;
     k.alsc_dout = (float)((double)c.alpha / denom);
+    alsc_poly_fit(ab, sb, (double)c.sm_scale * (double)c.alpha / cap, k.alsc_gu, &k.alsc_xmax);
   }
   return k;
 }
@@ -227,6 +269,17 @@ static capattn_status bwd_impl(const capattn_config* cfg, const void* q, const v
 }
 
 extern "C" {
+
+capattn_status capattn_debug_alsc_poly(const capattn_config* cfg, float* coeffs, float* xmax) {
+  const capattn_status st = validate(cfg);
+  if (st != CAPATTN_OK) return st;
+  if (!coeffs || !xmax || cfg->cap_method != CAPATTN_CAP_ALSC || !(cfg->cap > 0.f)) return CAPATTN_ERR_INVALID_ARG;
+  const CapConsts k = make_cap(*cfg);
+  for (int i = 0; i < 7; ++i) coeffs[i] = k.alsc_gu[i];
+  *xmax = k.alsc_xmax;
+  return CAPATTN_OK;
+}
+
 
 const char* capattn_status_string(capattn_status s) {
   switch (s) {

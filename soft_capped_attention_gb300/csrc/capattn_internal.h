@@ -23,6 +23,11 @@ struct CapConsts {
   float alsc_out;     // ALSC: cap / denom
   float alsc_sb;      // ALSC: sigma(alpha * beta)
   float alsc_dout;    // ALSC: derivative scale alpha / denom
+  // ALSC on the FMA pipe: sigma(alsc_a * sm_scale * X + alsc_b) - alsc_sb
+  // = X * sum_k alsc_gu[k] X^k for a raw score X with |X| <= alsc_xmax
+  // (an interpolating polynomial; alsc_xmax 0: none)
+  float alsc_gu[7];
+  float alsc_xmax;
 };
 
 struct Params {

@@ -168,6 +168,44 @@ __device__ __forceinline__ float p_chunk_tanh_mixed(const uint32_t (&v)[2 * NP],
   return s0 + s1;
 }
 
+// ALSC with the sigmoid on the FMA pipe (alsc_poly2; every |X| <= alsc_xmax):
+// NP column pairs of P = 2^(mul * (f(X) - sigma(alpha beta)) + addm0), packed
+// to bf16 into pk; returns their sum.  (addm0 = addm - radd of the plain form.)
+template <bool MASKED, int NP>
+__device__ __forceinline__ float p_chunk_alsc(const uint32_t (&v)[2 * NP], uint32_t (&pk)[NP],
+                                              const CapConsts& cap, float mul, float addm0, uint32_t live) {
+  const F2 mul2 = f2(mul, mul), add2 = f2(addm0, addm0);
+  F2 acc = f2(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < NP; ++e) {
+    float x0, x1;
+    const F2 d = alsc_poly2(f2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), cap);
+    f2_split(f2_fma(mul2, d, add2), x0, x1);
+    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if constexpr (MASKED) {
+      if (!(live & (1u << (2 * e)))) p0 = 0.f;
+      if (!(live & (2u << (2 * e)))) p1 = 0.f;
+    }
+    acc = f2_add(acc, f2(p0, p1));
+    pk[e] = pack_bf16x2(p0, p1);
+  }
+  float s0, s1;
+  f2_split(acc, s0, s1);
+  return s0 + s1;
+}
+
+// Whether every raw score of the warp's 32 columns is within the ALSC
+// polynomial's range (warp-wide vote).
+__device__ __forceinline__ bool quarter_alsc_poly(const uint32_t (&v)[32], float xmax) {
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    a0 = fmax3_abs(a0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+    a1 = fmax3_abs(a1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+  }
+  return __all_sync(0xFFFFFFFFu, fmaxf(a0, a1) <= xmax);
+}
+
 // NP column pairs of P = 2^(mul * f(X) + addm), packed to bf16 into pk; returns
 // their sum.  With MASKED, bit k of `live` says whether column k is live.  (No
 // TMEM access here: callers branch per row, and the warp-wide tcgen05 store

@@ -223,6 +223,19 @@ __device__ __forceinline__ F2 tanh_fold_eval(F2 X, const TanhFold& t, F2 add) {
   return f2_fma(X, q, add);
 }
 
+// ALSC's sigmoid on the FMA pipe for a pair of raw scores with |X| <= k.alsc_xmax:
+// sigma(z) - sigma(alpha beta) = X * sum_j alsc_gu[j] X^j (host-fitted polynomial).
+__device__ __forceinline__ F2 alsc_poly2(F2 X, const CapConsts& k) {
+  F2 q = f2(k.alsc_gu[6], k.alsc_gu[6]);
+  q = f2_fma(q, X, f2(k.alsc_gu[5], k.alsc_gu[5]));
+  q = f2_fma(q, X, f2(k.alsc_gu[4], k.alsc_gu[4]));
+  q = f2_fma(q, X, f2(k.alsc_gu[3], k.alsc_gu[3]));
+  q = f2_fma(q, X, f2(k.alsc_gu[2], k.alsc_gu[2]));
+  q = f2_fma(q, X, f2(k.alsc_gu[1], k.alsc_gu[1]));
+  q = f2_fma(q, X, f2(k.alsc_gu[0], k.alsc_gu[0]));
+  return f2_mul(X, q);
+}
+
 __device__ __forceinline__ F2 tanh_poly2(F2 u) {
   const F2 w = f2_mul(u, u);
   F2 p = f2_fma(f2(kTanhC3, kTanhC3), w, f2(kTanhC2, kTanhC2));

@@ -348,3 +348,38 @@ def test_unequal_lengths_visit_maps_match_oracle(lib, mask, L, Lk, dtype):
         got = ca.capattn_visit_map_host(c, None, None, which)
         ref = np.concatenate([_pack(V if which == ca.VISIT_Q_TILES else V.T)] * 2, axis=0).reshape(-1)
         assert np.array_equal(got, ref)
+
+
+# ALSC on the FMA pipe: the host-fitted polynomial the kernels use in place of
+# the sigmoid when every raw score of a warp's step lies within xmax.
+@pytest.mark.parametrize("cap,alpha,beta,sm_scale", [
+    (30.0, 2.0, 0.5, 1.0 / np.sqrt(128.0)),   # the windowed GQA and ranker workloads
+    (30.0, 4.0, 0.5, 0.125),                  # mosaic_backward.py's test cap
+    (20.0, 1.0, 0.0, 1.0 / np.sqrt(64.0)),
+    (50.0, 8.0, -0.25, 1.0 / np.sqrt(128.0)),
+    (5.0, 0.5, 3.0, 0.3),
+])
+def test_alsc_polynomial_matches_the_sigmoid(lib, cap, alpha, beta, sm_scale):
+    ap = ca.AttnParams(sm_scale=float(sm_scale), cap_method="alsc", cap=cap, alpha=alpha, beta=beta)
+    cfg = ca.make_config(ap, 1, 128, 2, 2, 128, torch.bfloat16)
+    coeffs = (ctypes.c_float * 7)()
+    xmax = ctypes.c_float(0.0)
+    assert lib.capattn_debug_alsc_poly(ctypes.byref(cfg), coeffs, ctypes.byref(xmax)) == 0
+    g = np.array(list(coeffs), np.float64)
+    u = sm_scale * alpha / cap
+    assert abs(xmax.value * u - 0.5) < 1e-6
+    x = np.linspace(-xmax.value, xmax.value, 4001)
+    sig = lambda z: 1.0 / (1.0 + np.exp(-z))
+    exact = sig(u * x + alpha * beta) - sig(alpha * beta)
+    poly = x * np.polyval(g[::-1], x)
+    # float32 coefficients: a few ulps of the result's scale (|exact| <= 0.25)
+    assert np.max(np.abs(poly - exact)) <= 2e-7
+    assert abs(poly[2000]) == 0.0  # exactly zero at X = 0
+
+
+def test_alsc_polynomial_needs_an_alsc_cap(lib):
+    ap = ca.AttnParams(sm_scale=0.1, cap_method="tanh", cap=30.0)
+    cfg = ca.make_config(ap, 1, 128, 2, 2, 128, torch.bfloat16)
+    coeffs = (ctypes.c_float * 7)()
+    xmax = ctypes.c_float(0.0)
+    assert lib.capattn_debug_alsc_poly(ctypes.byref(cfg), coeffs, ctypes.byref(xmax)) == 1
