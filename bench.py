@@ -184,13 +184,49 @@ def kernel_source_hash(csrc: str = None) -> str:
     return h.hexdigest()[:16]
 
 
+_INCLUDE = re.compile(r'#include\s+"([^"]+)"')
+
+
+def kernel_files(source: str, csrc: str = None) -> list:
+    """A kernel's translation unit, the csrc headers it includes (transitively)
+    and the host layer that sizes its launches and workspace."""
+    csrc = csrc or os.path.join(ROOT, "soft_capped_attention_gb300", "csrc")
+    seen, todo = set(), [source, "capattn_api.cu"]
+    while todo:
+        f = os.path.normpath(todo.pop())
+        if f in seen or not os.path.isfile(os.path.join(csrc, f)):
+            continue  # (system headers)
+        seen.add(f)
+        with open(os.path.join(csrc, f)) as fh:
+            base = os.path.dirname(f)
+            todo.extend(os.path.join(base, i) for i in _INCLUDE.findall(fh.read()))
+    return sorted(seen)
+
+
+def files_hash(files, csrc: str = None) -> str:
+    """kernel_source_hash over the given csrc files only."""
+    csrc = csrc or os.path.join(ROOT, "soft_capped_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(files):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            data = fh.read()
+        if f.endswith((".cu", ".cuh", ".h", ".cpp", ".c")):
+            data = " ".join(_C_COMMENT.sub(" ", data.decode()).split()).encode()
+        h.update(f.encode() + data)
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel: str, workload: str):
-    """ncu DRAM bytes per launch of `kernel` on `workload`, if taken on this source."""
+    """ncu DRAM bytes per launch of `kernel` on `workload`, if taken on this
+    kernel's code (its source file with the headers it includes, when the
+    capture names it; otherwise all kernel sources)."""
     try:
         with open(TRAFFIC) as f:
             t = json.load(f)
         e = t[workload][kernel]
-        if e.get("source_hash") != kernel_source_hash():
+        src = e.get("source_file")
+        now = files_hash(kernel_files(src)) if src else kernel_source_hash()
+        if e.get("source_hash") != now:
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:

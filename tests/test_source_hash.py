@@ -37,3 +37,31 @@ def test_code_changes_alter_the_hash(tmp_path):
     assert "constexpr float kTopMax = 100.0f;" in src
     f.write_text(src.replace("constexpr float kTopMax = 100.0f;", "constexpr float kTopMax = 99.0f;"))
     assert bench.kernel_source_hash(str(d)) != h0
+
+
+def _copy_tree(tmp_path):
+    """The package's csrc and the public header, in the same relative layout."""
+    root = tmp_path / "repo"
+    shutil.copytree(CSRC, root / "soft_capped_attention_gb300" / "csrc",
+                    ignore=shutil.ignore_patterns("__pycache__"))
+    shutil.copytree(os.path.join(os.path.dirname(os.path.dirname(CSRC)), "include"), root / "include")
+    return root / "soft_capped_attention_gb300" / "csrc"
+
+
+def test_a_kernels_tag_covers_its_own_files(tmp_path):
+    d = _copy_tree(tmp_path)
+    tag = lambda src: bench.files_hash(bench.kernel_files(src, str(d)), str(d))
+    files = bench.kernel_files("attn_bwd_tc.cu", str(d))
+    assert "attn_bwd_tc.cu" in files and "tc_common.cuh" in files and "capattn_api.cu" in files
+    assert os.path.normpath("../../include/capattn.h") in files
+    assert "attn_fwd1_tc.cu" not in files and "fwd_common.cuh" not in files
+    dkv0, fwd0 = tag("attn_bwd_tc.cu"), tag("attn_fwd3_tc.cu")
+    f = d / "attn_fwd1_tc.cu"          # another kernel's file: dK/dV's tag stays
+    f.write_text(f.read_text().replace("constexpr", "constexpr ", 1) + "\nstatic int unrelated_change = 1;\n")
+    assert tag("attn_bwd_tc.cu") == dkv0
+    f = d / "fwd_common.cuh"           # the forwards' header: the forward's tag moves
+    f.write_text(f.read_text() + "\nconstexpr int another_constant = 3;\n")
+    assert tag("attn_bwd_tc.cu") == dkv0 and tag("attn_fwd3_tc.cu") != fwd0
+    f = d / "tc_common.cuh"            # a header both include: both move
+    f.write_text(f.read_text() + "\nconstexpr int shared_constant = 4;\n")
+    assert tag("attn_bwd_tc.cu") != dkv0
