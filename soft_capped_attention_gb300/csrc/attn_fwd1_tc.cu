@@ -287,6 +287,9 @@ fwd1_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
       // two halves of a row see the same range, so they decide alike)
       if constexpr (METHOD == CAPATTN_CAP_TANH)
         poly = __all_sync(0xFFFFFFFFu, tf.ok && fmaxf(vmax, -vmin) * fabsf(xf.in) <= kTanhPolyMaxU);
+      // ALSC's sigmoid on the FMA pipe when every live score is in the polynomial's range
+      if constexpr (METHOD == CAPATTN_CAP_ALSC)
+        poly = __all_sync(0xFFFFFFFFu, fmaxf(vmax, -vmin) <= p.cap.alsc_xmax);
       m_true = fmaxf(m_true, x_max);
       const float m_new = fmaxf(m_use, x_max);
       const bool resc = m_new > m_use + kRescaleThreshold;
@@ -326,8 +329,9 @@ fwd1_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = 0u;
           } else {
-            if (fixed_ref) poly = sub_poly<METHOD>(va, tf, xf);
-            psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, tf, rmul, addm, c0 + 16 * c, ri, any);
+            if (fixed_ref)
+              poly = METHOD == CAPATTN_CAP_ALSC ? sub_alsc_poly(va, p.cap.alsc_xmax) : sub_poly<METHOD>(va, tf, xf);
+            psum += p_dispatch<METHOD>(fast, poly, va, pk, xf, tf, rmul, addm, c0 + 16 * c, ri, any, &p.cap);
           }
           __syncwarp();
           tmem_st8(s_base + 8 * c, pk);
@@ -338,8 +342,9 @@ fwd1_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = 0u;
           } else {
-            if (fixed_ref) poly = sub_poly<METHOD>(vb, tf, xf);
-            psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, tf, rmul, addm, c0 + 16 * (c + 1), ri, any);
+            if (fixed_ref)
+              poly = METHOD == CAPATTN_CAP_ALSC ? sub_alsc_poly(vb, p.cap.alsc_xmax) : sub_poly<METHOD>(vb, tf, xf);
+            psum += p_dispatch<METHOD>(fast, poly, vb, pk, xf, tf, rmul, addm, c0 + 16 * (c + 1), ri, any, &p.cap);
           }
           __syncwarp();
           tmem_st8(s_base + 8 * (c + 1), pk);

@@ -194,6 +194,15 @@ __device__ __forceinline__ float p_chunk_alsc(const uint32_t (&v)[2 * NP], uint3
   return s0 + s1;
 }
 
+// Whether every raw score of the warp's 16 columns is within the ALSC
+// polynomial's range (warp-wide vote).
+__device__ __forceinline__ bool sub_alsc_poly(const uint32_t (&v)[16], float xmax) {
+  float am = 0.f;
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) am = fmax3_abs(am, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+  return __all_sync(0xFFFFFFFFu, am <= xmax);
+}
+
 // Whether every raw score of the warp's 32 columns is within the ALSC
 // polynomial's range (warp-wide vote).
 __device__ __forceinline__ bool quarter_alsc_poly(const uint32_t (&v)[32], float xmax) {
@@ -254,7 +263,16 @@ __device__ __forceinline__ bool sub_poly(const uint32_t (&v)[16], const TanhFold
 template <int METHOD>
 __device__ __forceinline__ float p_dispatch(bool full_any, bool poly, const uint32_t (&v)[16],
                                            uint32_t (&pk)[8], const Xf& xf, const TanhFold& tf,
-                                           float mul, float addm, int j0, int4 ri, bool any) {
+                                           float mul, float addm, int j0, int4 ri, bool any,
+                                           const CapConsts* cap = nullptr) {
+  if constexpr (METHOD == CAPATTN_CAP_ALSC) {
+    // the sigmoid on the FMA pipe (the caller voted the range)
+    if (poly && cap) {
+      const float addm0 = addm + mul * cap->alsc_sb;
+      if (full_any) return p_chunk_alsc<false, 8>(v, pk, *cap, mul, addm0, 0xFFFFu);
+      return p_chunk_alsc<true, 8>(v, pk, *cap, mul, addm0, any ? live_bits16(ri, j0) : 0u);
+    }
+  }
   if (full_any) {
     if constexpr (METHOD == CAPATTN_CAP_TANH) {
       if (poly) return p_chunk_tanh_fold<false, 8>(v, pk, tf, addm, 0xFFFFu);
