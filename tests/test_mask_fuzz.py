@@ -5,7 +5,8 @@ This sweep draws lengths, windows, segment layouts and ranker bounds from
 edge-heavy distributions: windows of 1 and windows longer than the sequence,
 a single segment and every position its own segment, empty history or
 candidate ranges, ranges that overlap or touch the sequence ends, and
-lengths one off a tile boundary.  Each draw compares the live-pair bits of
+lengths one off a tile boundary, and query lengths apart from key lengths.
+Each draw compares the live-pair bits of
 every batch row and both visit maps (at the bf16 and fp32 tile sizes) with
 the oracle's brute-force mask, bit for bit."""
 
@@ -131,6 +132,30 @@ def test_random_masks_match_oracle(lib, seed):
         for which in (ca.VISIT_Q_TILES, ca.VISIT_KV_TILES):
             got = ca.capattn_visit_map_host(c, seg, bounds, which)
             ref = np.concatenate([_pack(V if which == ca.VISIT_Q_TILES else V.T) for V in Vs],
+                                 axis=0).reshape(-1)
+            assert np.array_equal(got, ref), (dtype, which)
+
+
+@pytest.mark.parametrize("seed", range(N_DRAWS // 2))
+def test_random_unequal_lengths_match_oracle(lib, seed):
+    """Query and key lengths drawn apart (segment ids and ranker bounds need
+    equal lengths, so only the causal and window masks apply)."""
+    rng = np.random.default_rng(2000003 + seed)
+    L, Lk = _length(rng), _length(rng)
+    causal = bool(rng.integers(0, 2))
+    window = _window(rng, max(L, Lk))
+    ap = ca.AttnParams(sm_scale=0.1, cap_method="tanh", cap=5.0, causal=causal, window_len=window)
+    ocfg = orc.OracleConfig(sm_scale=1.0, causal=causal, window_len=window)
+    c = ca.make_config(ap, 1, L, 2, 2, 128, torch.bfloat16, Lk=Lk)
+    bits = ca.capattn_mask_bits_host(c, 0)
+    assert bits.shape == (L, Lk) and np.array_equal(bits, orc.mask_matrix(L, ocfg, Lk=Lk))
+    for D, dtype in ((128, torch.bfloat16), (64, torch.float32)):
+        c = ca.make_config(ap, 2, L, 2, 2, D, dtype, Lk=Lk)
+        bq, bk = ca.capattn_tile_sizes(c)
+        V = orc.visit_matrix(L, bq, bk, ocfg, Lk=Lk)
+        for which in (ca.VISIT_Q_TILES, ca.VISIT_KV_TILES):
+            got = ca.capattn_visit_map_host(c, None, None, which)
+            ref = np.concatenate([_pack(V if which == ca.VISIT_Q_TILES else V.T)] * 2,
                                  axis=0).reshape(-1)
             assert np.array_equal(got, ref), (dtype, which)
 
