@@ -4,11 +4,10 @@ The fixed cases in test_boundary.py cover each mask kind at a few lengths.
 This sweep draws lengths, windows, segment layouts and ranker bounds from
 edge-heavy distributions: windows of 1 and windows longer than the sequence,
 a single segment and every position its own segment, empty history or
-candidate ranges, ranges that overlap or touch the sequence ends, and
-lengths one off a tile boundary, and query lengths apart from key lengths.
-Each draw compares the live-pair bits of
-every batch row and both visit maps (at the bf16 and fp32 tile sizes) with
-the oracle's brute-force mask, bit for bit."""
+candidate ranges, ranges that overlap or touch the sequence ends, lengths one
+off a tile boundary, and query lengths apart from key lengths.  Each draw
+compares the live-pair bits of every batch row and both visit maps (at the
+bf16 and fp32 tile sizes) with the oracle's brute-force mask, bit for bit."""
 
 import os
 
