@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from oracle import capattn_oracle as orc
-from oracle.brute_force import brute_attention
+from oracle.brute_force import _live, brute_attention
 
 CAPS = [("none", 0.0, 0.0, 0.0), ("tanh", 5.0, 0.0, 0.0), ("soft_sign", 3.0, 0.0, 0.0),
         ("alsc", 4.0, 2.0, 0.5)]
@@ -563,6 +563,48 @@ def test_visit_matrix_matches_tile_scan():
             Mp[:L, :L] = M
             ref = Mp.reshape(nq, bq, nk, bk).any(axis=(1, 3))
             assert np.array_equal(V, ref)
+
+
+
+def test_visit_matrix_a_lone_live_key_at_a_tile_edge():
+    # History = key 7 alone, the last column of the first 8-wide KV tile;
+    # candidates 8..19 see that key and themselves.  Live pairs, worked out by
+    # hand: (7, 7), (i, 7) and (i, i) for i in 8..19.
+    cfg = orc.OracleConfig(sm_scale=1)
+    V = orc.visit_matrix(24, 8, 8, cfg, None, (7, 8, 8, 20))
+    assert V.astype(int).tolist() == [[1, 0, 0], [1, 1, 0], [1, 0, 1]]
+    # the same pairs through 4-row query tiles and 16-wide KV tiles: rows 0..3
+    # and 20..23 hold no live pair, only rows 16..19 reach the second KV tile
+    V = orc.visit_matrix(24, 4, 16, cfg, None, (7, 8, 8, 20))
+    assert V.astype(int).tolist() == [[0, 0], [1, 0], [1, 0], [1, 0], [1, 1], [0, 0]]
+
+
+def test_visit_matrix_matches_scalar_liveness():
+    """Tile (qt, kt) is visited iff some pair in it is live by the scalar
+    restatement of the masks (triple loop over tiles, rows and keys)."""
+    rng = np.random.default_rng(31)
+    for _ in range(40):
+        L = int(rng.integers(1, 40))
+        causal = bool(rng.integers(0, 2))
+        window = int(rng.choice([0, 1, 2, 5, 50]))
+        sg = np.cumsum(rng.random(L) < 0.2).astype(np.int32) if rng.integers(0, 2) else None
+        bd = None
+        if rng.integers(0, 2):
+            hl = int(rng.integers(0, L + 1))
+            hu = int(rng.integers(hl, L + 1))
+            cl = int(rng.integers(0, L + 1))
+            bd = (hl, hu, cl, int(rng.integers(cl, L + 1)))
+        bq, bk = int(rng.choice([1, 3, 4, 8])), int(rng.choice([1, 2, 4, 8]))
+        cfg = orc.OracleConfig(sm_scale=1, causal=causal, window_len=window)
+        V = orc.visit_matrix(L, bq, bk, cfg, sg, bd)
+        nq, nk = -(-L // bq), -(-L // bk)
+        assert V.shape == (nq, nk)
+        for qt in range(nq):
+            for kt in range(nk):
+                live = any(_live(i, j, causal, window, sg, bd)
+                           for i in range(qt * bq, min(L, (qt + 1) * bq))
+                           for j in range(kt * bk, min(L, (kt + 1) * bk)))
+                assert V[qt, kt] == live, (L, bq, bk, qt, kt)
 
 
 def test_pair_counts_closed_forms():
