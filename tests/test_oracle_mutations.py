@@ -49,12 +49,22 @@ MUTATIONS = [
      "- m_safe[:, None]), 0.0)\n    O = P @ v", 1),
     ("gqa_heads_interleaved", "g = h // G", "g = h % Hkv", 1),
     ("scores_without_scale", "s = cfg.sm_scale * (q_rows @ k.T)", "s = q_rows @ k.T", 2),
+    ("m_over_masked_keys", "m = t_live.max(axis=1)", "m = t.max(axis=1)", 1),
+    ("l_without_max_shift", "e = np.where(M, np.exp(np.where(M, t, 0.0) - m_safe[:, None]), 0.0)",
+     "e = np.where(M, np.exp(np.where(M, t, 0.0)), 0.0)", 1),
+    ("masked_p_leaks", "P = np.where(M, np.exp(np.where(M, t, 0.0) - lse_safe[:, None]), 0.0)\n    O = P @ v",
+     "P = np.exp(t - lse_safe[:, None])\n    O = P @ v", 1),
+    ("window_two_sided", "M &= j > i - cfg.window_len",
+     "M &= (j > i - cfg.window_len) & (j < i + cfg.window_len)", 1),
     ("dead_row_lse_zero", "np.log(np.where(live, l, 1.0)), -np.inf)",
      "np.log(np.where(live, l, 1.0)), 0.0)", 1),
     # backward
     ("backward_without_delta", "dT = P * (dP - delta_rows[:, None])", "dT = P * dP", 1),
     ("z_loss_sign", "+ cfg.z_loss_weight * P * lse_safe[:, None]\n    if dlse_rows",
      "- cfg.z_loss_weight * P * lse_safe[:, None]\n    if dlse_rows", 1),
+    ("backward_masked_p_leaks",
+     "P = np.where(M, np.exp(np.where(M, t, 0.0) - lse_safe[:, None]), 0.0)\n    dP = do_rows @ v.T",
+     "P = np.exp(t - lse_safe[:, None])\n    dP = do_rows @ v.T", 1),
     ("dlse_dropped", "dT = dT + P * np.where(live, dlse_rows, 0.0)[:, None]", "dT = dT", 1),
     ("dx_without_scale", "dX = cfg.sm_scale * cap_derivative(s, cfg)", "dX = cap_derivative(s, cfg)", 1),
     ("dx_without_temperature", "* temp_rows[:, None] * dT", "* dT", 1),
@@ -70,6 +80,8 @@ MUTATIONS = [
      "dtemp[b, rows] += np.sum(dT * s, axis=1)", 1),
     ("dtemp_without_z_loss", "+ cfg.z_loss_weight * P * lse_safe[:, None]\n                if dLSE",
      "\n                if dLSE", 1),
+    ("dtemp_first_head_only", "dtemp[b, rows] += np.sum(dT * c, axis=1)",
+     "dtemp[b, rows] += np.sum(dT * c, axis=1) if h == 0 else 0.0", 1),
     ("dtemp_without_dlse", "dT = dT + P * np.where(live, dLSE[b, h, rows], 0.0)[:, None]",
      "dT = dT", 1),
     # ranker bounds, visit matrices, pair counts, row blocks
