@@ -498,7 +498,8 @@ dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     int2 fr_nxt = qfull_of(have1, nqt);
     int2 hq_nxt = make_int2(g * p.G + nh, nqt);
     // stored-dX backward: this thread's first 32-byte unit in the step's dX^T
-    // tile (1024 units per tile; at most 4 GiB of pool, so units fit 32 bits):
+    // tile (1024 units per tile; the pool is at most 16 GiB = 2^29 units, so
+    // units fit 32 bits):
     // block 4 wg (query columns 64 wg ..), key row r
     auto dx_unit = [&](int2 hq) -> uint32_t {
       if (!DX) return kNoDx;
