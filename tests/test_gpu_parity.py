@@ -151,6 +151,9 @@ FP32_CASES = [
     (2, 190, 2, 2, 64, "soft_sign", "packed", False, 0.0),
     (2, 150, 4, 2, 128, "alsc", "ranker", False, 0.02),
     (1, 65, 2, 2, 64, "none", "window_nc", True, 0.0),
+    # rows past the window (the cases above have windows longer than L)
+    (1, 300, 2, 1, 64, "tanh", "window", True, 0.0),
+    (2, 190, 2, 2, 128, "soft_sign", "window_nc", False, 0.0),
 ]
 
 

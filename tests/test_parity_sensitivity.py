@@ -36,6 +36,8 @@ ALSC_WINDOW = ("bf16", tp.BF16_CASES[2])     # (1, 513, 4, 1, alsc, window, temp
 SOFTSIGN_PACKED = ("bf16", tp.BF16_CASES[3])
 ALSC_RANKER = ("bf16", tp.BF16_CASES[4])
 TANH_WINDOW_NC = ("bf16", tp.BF16_CASES[5])
+FP32_WINDOW = ("fp32", tp.FP32_CASES[6])     # (1, 300, 2, 1, 64, tanh, window 200)
+FP32_WINDOW_NC = ("fp32", tp.FP32_CASES[7])  # (2, 190, 2, 2, 128, soft_sign, window 77, not causal)
 
 # mistake -> the GPU parity case whose comparison has to reject it
 CATCHER = {
@@ -110,7 +112,12 @@ def _rejected(kind, case, bad, good):
     """Whether the GPU test of this kind rejects `bad`'s outputs (True) or
     would pass them (False); each branch repeats that test's assertions."""
     try:
-        if kind in ("bf16", "curved", "z"):
+        if kind == "fp32":  # test_fp32_matches_oracle
+            B, L, Hq, Hkv, D, cap, mask, temp, z = case
+            inp = tp.make_case(B, L, Hq, Hkv, D, torch.float32, mask, temp, seed=L * 3 + D)
+            ap = tp.params(cap, mask, z)
+            compare(_outputs(bad, inp, ap), _outputs(good, inp, ap), torch.float32)
+        elif kind in ("bf16", "curved", "z"):
             if kind == "bf16":
                 B, L, Hq, Hkv, cap, mask, temp, z = case
                 inp = tp.make_case(B, L, Hq, Hkv, 128, torch.bfloat16, mask, temp, seed=L * 7 + Hq)
@@ -148,6 +155,11 @@ def _rejected(kind, case, bad, good):
     return False
 
 
+# the fp32 path has kernels of its own: its window cases must catch the window mistakes too
+FP32_CATCHER = {"window_inclusive": FP32_WINDOW, "window_two_sided": FP32_WINDOW_NC,
+                "causal_strict": FP32_WINDOW}
+
+
 def test_every_kernel_mistake_has_a_catcher():
     names = {m[0] for m in MUTATIONS}
     assert set(CATCHER) | NOT_KERNEL == names
@@ -161,8 +173,15 @@ def test_gpu_comparison_rejects_the_mistake(name, old, new, count):
     assert _rejected(kind, case, _oracle(old, new, count), _oracle()), name
 
 
+@pytest.mark.parametrize("name", sorted(FP32_CATCHER))
+def test_fp32_comparison_rejects_the_window_mistakes(name):
+    _, old, new, count = next(m for m in MUTATIONS if m[0] == name)
+    kind, case = FP32_CATCHER[name]
+    assert _rejected(kind, case, _oracle(old, new, count), _oracle()), name
+
+
 def test_gpu_comparisons_accept_the_true_oracle():
     # the control: every catcher passes the unmodified oracle's own outputs
     good = _oracle()
-    for kind, case in {(k, c) for k, c in CATCHER.values()}:
+    for kind, case in {(k, c) for k, c in list(CATCHER.values()) + list(FP32_CATCHER.values())}:
         assert not _rejected(kind, case, good, good), (kind, case)
